@@ -1,0 +1,269 @@
+"""Pins for the oracle: checks against facts the pages and the mathematics
+fix, never against the oracle's own formula.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees.  They
+are collected by ``test_oracle_pins.py`` and re-run against planted mistakes
+by ``test_oracle_mutants.py``.
+
+Sources of truth used here:
+  * torch's CPU float64 ``scaled_dot_product_attention`` and ``logsumexp``
+    (independent library implementations of the definition);
+  * closed forms: Q = 0 gives the mean of the visible V rows and LSE = ln(count);
+    a causal row 0 is V[0] with LSE = scale q0.k0; scale 0 gives the mean;
+    a single key gives that V row; joint permutations of K/V rows (non-causal)
+    leave O unchanged;
+  * invariance under a shared orthogonal rotation of Q and K ("FlashAttention-3:
+    async pipelines on Hopper", section "how incoherent processing flattens
+    outliers": scores are unchanged in exact arithmetic), with the Hadamard
+    matrix from scipy;
+  * the tiled online recurrence equals the two-pass result (wmrh.cn article,
+    sec. 2.1: the tiled result is the same as the global one);
+  * torch.float8_e4m3fn for the E4M3 codec, and 448 as its maximum (wmrh.cn
+    article, sec. 3.3).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import scipy.linalg
+import torch
+
+import attn_inputs as gen
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "pages_constants.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _torch_ref(q, k, v, causal, scale):
+    """torch CPU float64 SDPA with an explicit bottom-right causal mask, plus
+    torch.logsumexp of the scaled masked scores."""
+    q = torch.as_tensor(np.asarray(q, dtype=np.float64))
+    k = torch.as_tensor(np.asarray(k, dtype=np.float64))
+    v = torch.as_tensor(np.asarray(v, dtype=np.float64))
+    Hq, Hkv = q.shape[1], k.shape[1]
+    if Hq != Hkv:
+        k = k.repeat_interleave(Hq // Hkv, dim=1)
+        v = v.repeat_interleave(Hq // Hkv, dim=1)
+    Nq, Nk = q.shape[2], k.shape[2]
+    mask = None
+    if causal:
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = j <= i + (Nk - Nq)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+    s = scale * (q @ k.transpose(-1, -2))
+    if mask is not None:
+        s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    return o.numpy(), lse.numpy()
+
+
+def _sylvester(d):
+    return scipy.linalg.hadamard(d).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+
+def pin_library_cross_check(oracle):
+    cases = [
+        # (B, Hq, Hkv, Nq, Nk, d, causal, scale)
+        (1, 2, 2, 128, 128, 64, False, 1 / 8),
+        (1, 2, 2, 128, 128, 64, True, 1 / 8),
+        (2, 4, 2, 37, 37, 16, True, 0.3),
+        (1, 3, 1, 20, 50, 8, True, 0.5),
+        (1, 2, 2, 50, 20, 8, False, -0.7),
+    ]
+    for t, (B, Hq, Hkv, Nq, Nk, d, causal, scale) in enumerate(cases):
+        q = gen.normal((B, Hq, Nq, d), 10 + t, 0).astype(np.float64)
+        k = gen.normal((B, Hkv, Nk, d), 10 + t, 1).astype(np.float64)
+        v = gen.normal((B, Hkv, Nk, d), 10 + t, 2).astype(np.float64)
+        o, lse = oracle.attn_fwd(q, k, v, causal=causal, scale=scale)
+        o_ref, lse_ref = _torch_ref(q, k, v, causal, scale)
+        assert np.allclose(o, o_ref, rtol=0, atol=1e-12), f"case {t}: O differs from torch SDPA"
+        assert np.allclose(lse, lse_ref, rtol=0, atol=1e-12), f"case {t}: LSE differs from torch.logsumexp"
+
+
+def pin_zero_query(oracle):
+    B, H, N, d = 1, 2, 96, 32
+    k = gen.normal((B, H, N, d), 20, 1).astype(np.float64)
+    v = gen.normal((B, H, N, d), 20, 2).astype(np.float64)
+    q = np.zeros((B, H, N, d))
+    o, lse = oracle.attn_fwd(q, k, v, causal=False, scale=0.125)
+    assert np.allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape), atol=1e-13)
+    assert np.allclose(lse, math.log(N), atol=1e-13)
+    o, lse = oracle.attn_fwd(q, k, v, causal=True, scale=0.125)
+    prefix = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    assert np.allclose(o, prefix, atol=1e-13)
+    assert np.allclose(lse, np.log(np.arange(1, N + 1))[None, None, :], atol=1e-13)
+
+
+def pin_causal_row0(oracle):
+    B, H, N, d = 2, 2, 64, 16
+    q, k, v = (a.astype(np.float64) for a in gen.qkv_normal((B, H, N, d), 21))
+    scale = 0.37
+    o, lse = oracle.attn_fwd(q, k, v, causal=True, scale=scale)
+    assert np.array_equal(o[:, :, 0, :], v[:, :, 0, :]), "causal row 0 must be V[0] exactly"
+    expect = scale * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0])
+    assert np.allclose(lse[:, :, 0], expect, atol=1e-13)
+
+
+def pin_special_cases(oracle):
+    B, H, N, d = 1, 1, 33, 8
+    q, k, v = (a.astype(np.float64) for a in gen.qkv_normal((B, H, N, d), 22))
+    # scale 0: uniform weights
+    o, lse = oracle.attn_fwd(q, k, v, causal=False, scale=0.0)
+    assert np.allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape), atol=1e-13)
+    assert np.allclose(lse, math.log(N), atol=1e-13)
+    # a single key
+    o, lse = oracle.attn_fwd(q, k[:, :, :1], v[:, :, :1], causal=False, scale=0.5)
+    assert np.allclose(o, np.broadcast_to(v[:, :, :1], o.shape), atol=1e-15)
+    assert np.allclose(lse, 0.5 * (q[0, 0] @ k[0, 0, 0])[None, None, :], atol=1e-13)
+    # joint permutation of K/V rows
+    perm = np.random.Generator(np.random.PCG64(5)).permutation(N)
+    o1, l1 = oracle.attn_fwd(q, k, v, scale=0.3)
+    o2, l2 = oracle.attn_fwd(q, k[:, :, perm], v[:, :, perm], scale=0.3)
+    assert np.allclose(o1, o2, atol=1e-13) and np.allclose(l1, l2, atol=1e-13)
+    # one dominant key: the output is that key's value row
+    kk = np.zeros((1, 1, 4, 2))
+    kk[0, 0, :, 0] = [0.0, 1.0, 2.0, 3.0]
+    vv = np.arange(8, dtype=np.float64).reshape(1, 1, 4, 2)
+    qq = np.array([[[[1.0, 0.0]]]])
+    o, lse = oracle.attn_fwd(qq, kk, vv, scale=200.0)
+    assert np.allclose(o[0, 0, 0], vv[0, 0, 3], atol=1e-12)
+    assert abs(lse[0, 0, 0] - 600.0) < 1e-12
+
+
+def pin_rotation_invariance(oracle):
+    B, H, N, d = 1, 2, 40, 32
+    q, k, v = (a.astype(np.float64) for a in gen.qkv_normal((B, H, N, d), 23))
+    signs = gen.hadamard_signs(d, 7).astype(np.float64)
+    M = np.diag(signs) @ _sylvester(d) / math.sqrt(d)
+    assert np.allclose(M @ M.T, np.eye(d), atol=1e-14)
+    for causal in (False, True):
+        o1, l1 = oracle.attn_fwd(q, k, v, causal=causal, scale=0.2)
+        o2, l2 = oracle.attn_fwd(q @ M, k @ M, v, causal=causal, scale=0.2)
+        assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+
+
+def pin_online_recurrence(oracle):
+    B, Hq, Hkv, N, d = 1, 2, 1, 300, 16
+    q = gen.normal((B, Hq, N, d), 24, 0).astype(np.float64) * 2.0
+    k = gen.normal((B, Hkv, N, d), 24, 1).astype(np.float64)
+    v = gen.normal((B, Hkv, N, d), 24, 2).astype(np.float64)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal=causal, scale=0.5)
+        for tile in (1, 7, 128, N):
+            for tau in (0.0, 8.0 * math.log(2.0)):
+                o2, l2 = oracle.online_attn_fwd(q, k, v, causal=causal, scale=0.5, tile=tile, tau=tau)
+                assert np.allclose(o, o2, rtol=0, atol=1e-12), (causal, tile, tau)
+                assert np.allclose(lse, l2, rtol=0, atol=1e-12), (causal, tile, tau)
+
+
+def pin_row_subset(oracle):
+    B, H, N, d = 1, 2, 200, 16
+    q, k, v = (a.astype(np.float64) for a in gen.qkv_normal((B, H, N, d), 25))
+    rows = gen.sample_rows(N, 20, 1)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal=causal, scale=0.25)
+        os_, ls_ = oracle.attn_fwd(q, k, v, causal=causal, scale=0.25, rows=rows)
+        assert np.array_equal(o[:, :, rows], os_) and np.array_equal(lse[:, :, rows], ls_)
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 codec, rotation and quantiser
+# --------------------------------------------------------------------------
+
+def pin_e4m3_decode(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    got = oracle.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.nanmax(got) == _golden()["e4m3_max"]["value"]
+
+
+def pin_e4m3_encode(oracle):
+    finite = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    grid = np.unique(np.abs(finite[np.isfinite(finite)]))
+    mids = (grid[1:] + grid[:-1]) / 2.0            # exact ties
+    rng = np.random.Generator(np.random.PCG64(9))
+    vals = np.concatenate([grid, mids, np.nextafter(mids, 0), np.nextafter(mids, 1000),
+                           rng.uniform(-448, 448, 5000), rng.standard_normal(5000) * 1e-2,
+                           rng.standard_normal(5000) * 1e-3]).astype(np.float32)
+    vals = np.concatenate([vals, -vals])
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(vals)
+    assert np.array_equal(got, ref), "E4M3 encoding must match torch's round-to-nearest-even"
+    # saturation at the largest finite value (satfinite)
+    big = np.array([448.0, 449.0, 463.9, 464.0, 500.0, 1e30, -1e30], dtype=np.float32)
+    assert np.array_equal(oracle.e4m3_decode(oracle.e4m3_encode(big)),
+                          np.array([448, 448, 448, 448, 448, 448, -448], dtype=np.float32))
+
+
+def pin_fwht(oracle):
+    for d in (8, 64, 128, 256):
+        x = gen.normal((5, d), 30 + d)
+        signs = gen.hadamard_signs(d, d)
+        y = oracle.fwht_f32(x, signs).astype(np.float64)
+        exact = (x.astype(np.float64) * signs) @ _sylvester(d).T
+        bound = math.log2(d) * np.finfo(np.float32).eps * np.abs(x).astype(np.float64).sum(axis=1,
+                                                                                           keepdims=True)
+        assert np.all(np.abs(y - exact) <= bound + 1e-30), d
+        M = np.diag(signs.astype(np.float64)) @ _sylvester(d) / math.sqrt(d)
+        assert np.allclose(oracle.rotate(x, signs), x.astype(np.float64) @ M, atol=1e-12)
+
+
+def pin_quantiser(oracle):
+    rows = _golden()["quant_block_rows"]["value"]
+    B, H, N, d = 1, 2, 300, 64                      # ragged last block (44 rows)
+    x = gen.outliers((B, H, N, d), 40)
+    signs = gen.hadamard_signs(d, 41)
+    for sg in (None, signs):
+        for per_tensor in (False, True):
+            codes, ds = oracle.quant_e4m3(x, signs=sg, per_tensor=per_tensor, block_rows=rows)
+            assert ds.shape == (B, H, 3)
+            target = x.astype(np.float64) if sg is None else oracle.rotate(x, sg)
+            deq = oracle.dequant_e4m3(codes, ds, block_rows=rows)
+            # every block: the largest magnitude maps to +-448; error within half
+            # an E4M3 step (relative 2^-4 for normals, 2^-10 * scale below)
+            blocks = [(b, h, r0) for b in range(B) for h in range(H) for r0 in range(0, N, rows)]
+            for (b, h, r0) in blocks:
+                cb = codes[b, h, r0:r0 + rows]
+                tb = target[b, h, r0:r0 + rows]
+                db = deq[b, h, r0:r0 + rows]
+                s = ds[b, h, r0 // rows]
+                if not per_tensor:
+                    mags = oracle.e4m3_decode(cb & 0x7F)
+                    assert mags.max() == 448.0
+                    amax = np.abs(tb).max()
+                    assert abs(amax / 448.0 - s) <= 1e-6 * amax / 448.0
+                err = np.abs(db - tb)
+                tol = np.maximum(np.abs(tb) * 2.0 ** -4, 2.0 ** -10 * s) * (1 + 1e-5)
+                assert np.all(err <= tol)
+            if per_tensor:
+                assert np.all(ds == ds.flat[0])
+                assert oracle.e4m3_decode(codes & 0x7F).max() == 448.0
+
+
+def pin_flop_convention(oracle):
+    g = _golden()["matmul_flops_per_exp_d128"]["value"]
+    B, H, N, d = 1, 1, 1024, 128
+    assert gen.flops(B, H, N, d, False) / (N * N) == g
+    assert gen.flops(B, H, N, d, True) == gen.flops(B, H, N, d, False) / 2
+
+
+ALL_PINS = [
+    pin_library_cross_check, pin_zero_query, pin_causal_row0, pin_special_cases,
+    pin_rotation_invariance, pin_online_recurrence, pin_row_subset,
+    pin_e4m3_decode, pin_e4m3_encode, pin_fwht, pin_quantiser, pin_flop_convention,
+]

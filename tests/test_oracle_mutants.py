@@ -1,0 +1,54 @@
+"""Planted mistakes in the oracle must fail at least one pin (CPU only).
+
+Each mutant is a one-line edit of a copy of oracle/oracle.c (a dropped term,
+a wrong sign, index or operand, a wrong constant), compiled to a temporary
+library and run through the pins of ``oracle_pins``.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "scale_dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "max_not_subtracted": ("const double p = exp(s[j] - m);", "const double p = exp(s[j]);"),
+    "causal_diagonal_excluded": ("int64_t lim = i + (Nk - Nq) + 1;", "int64_t lim = i + (Nk - Nq);"),
+    "value_is_key": ("const double* vb = v + (b * Hkv", "const double* vb = k + (b * Hkv"),
+    "gqa_head_map": ("const double* kb = k + (b * Hkv + h / group)", "const double* kb = k + (b * Hkv + h % Hkv)"),
+    "lse_log2": ("lse[bh * R + r] = m + log(l);", "lse[bh * R + r] = m + log2(l);"),
+    "dot_index": ("dot += qi[c] * kj[c];", "dot += qi[c] * kj[0];"),
+    "no_normalisation": ("oi[c] = acc[c] / l;", "oi[c] = acc[c];"),
+    "e4m3_ties_away": ("double qn = nearbyint(ldexp(a, 3 - E));", "double qn = round(ldexp(a, 3 - E));"),
+    "e4m3_bias": ("const int field = E + 7;", "const int field = E + 8;"),
+    "quant_xmax_127": ("amax / 448.0f", "amax / 127.0f"),
+    "fwht_sign": ("y[c + h] = a - b;", "y[c + h] = b - a;"),
+    "signs_ignored": ("(signs && signs[c] < 0) ? -x[c] : x[c]", "x[c]"),
+    "rotation_norm_missing": ("(float)(1.0 / sqrt((double)d))", "1.0f"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique"
+    src = tmp_path / "oracle_mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
+                    "-o", str(lib), str(src), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_LIB", None)
+    monkeypatch.setattr(oracle._build, "build", lambda force=False: str(lib))
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(oracle)
+        except AssertionError:
+            failed.append(pin.__name__)
+    monkeypatch.setattr(oracle, "_LIB", None)
+    assert failed, f"mutant {name} passed every pin"
