@@ -1,0 +1,170 @@
+"""Fused exact attention forward for NVIDIA GB300 (sm_103a).
+
+The product is the C library ``libfa.so`` (C ABI declared in
+``include/fa.h``; hand-written CUDA kernels under ``csrc/``).  This package is
+a thin ctypes binding with the same entry-point names: it checks tensor
+shapes, allocates outputs with torch, passes raw device pointers and the
+current CUDA stream, and turns status codes into exceptions.  Every step of
+the computation runs in the library's kernels; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+__all__ = ["fwd", "fwd_fp8", "quant_fp8", "check_device_error", "lib", "FaError",
+           "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+           "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS"]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_DTYPE_BF16, FA_DTYPE_FP16 = 0, 1
+FP8_BLOCK_ROWS = 128
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib().fa_status_string(status).decode()}")
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"libfa.so has not been built ({_LIB_PATH}); run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, i32, vp]
+        lib.fa_fwd.restype = i32
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, vp, vp, vp, vp]
+        lib.fa_fwd_fp8.restype = i32
+        lib.fa_quant_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp]
+        lib.fa_quant_fp8.restype = i32
+        lib.fa_status_string.argtypes = [i32]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_check_device_error.argtypes = [vp]
+        lib.fa_check_device_error.restype = i32
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i32
+        _LIB = lib
+    return _LIB
+
+
+def lib():
+    """The loaded ctypes library (raw C entry points)."""
+    return _lib()
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def _check_qkv(q, k, v, allowed):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+        if t.dtype not in allowed:
+            raise ValueError(f"{name} has dtype {t.dtype}; expected one of {allowed}")
+    if not (q.shape == k.shape == v.shape and q.dtype == k.dtype == v.dtype and
+            q.device == k.device == v.device):
+        raise ValueError("q, k, v must share shape, dtype and device")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """BF16/FP16 attention forward (``fa_fwd``).  Returns (O, LSE)."""
+    _check_qkv(q, k, v, (torch.bfloat16, torch.float16))
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    dt = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    with torch.cuda.device(q.device):
+        st = _lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           B, H, N, d, int(bool(causal)), float(scale), dt, _stream(q))
+    _check(st, "fa_fwd")
+    return out, lse
+
+
+def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_descale: torch.Tensor,
+            k_descale: torch.Tensor, v_descale: torch.Tensor, causal: bool = False,
+            scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """FP8 E4M3 attention forward (``fa_fwd_fp8``).  q8/k8/v8 hold E4M3 codes
+    (uint8 or float8_e4m3fn), descales are [B, H, ceil(N/128)] fp32.
+    Returns (O bf16, LSE fp32)."""
+    _check_qkv(q8, k8, v8, (torch.uint8, torch.float8_e4m3fn))
+    B, H, N, d = q8.shape
+    nblk = (N + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, H, nblk) or not t.is_contiguous() or \
+                t.device != q8.device:
+            raise ValueError(f"{name} must be a contiguous fp32 [B, H, {nblk}] tensor on {q8.device}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        st = _lib().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, N, d, int(bool(causal)), float(scale), q_descale.data_ptr(),
+                               k_descale.data_ptr(), v_descale.data_ptr(), _stream(q8))
+    _check(st, "fa_fwd_fp8")
+    return out, lse
+
+
+def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: torch.Tensor | None = None):
+    """fp32 [B, H, N, d] -> (E4M3 codes uint8 [B, H, N, d], descale fp32
+    [B, H, ceil(N/128)]) via ``fa_quant_fp8``.  ``signs``: d entries of +-1
+    (host sequence / numpy / CPU tensor) for the Hadamard rotation, or None."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 \
+            or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 [B, H, N, d] CUDA tensor")
+    B, H, N, d = x.shape
+    nblk = (N + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS
+    x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    ds = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    sp = None
+    keep = None
+    if signs is not None:
+        keep = (ctypes.c_int8 * d)(*[int(s) for s in (signs.tolist() if hasattr(signs, "tolist") else signs)])
+        sp = ctypes.cast(keep, ctypes.c_void_p)
+    ws = None
+    if per_tensor:
+        if workspace is None:
+            workspace = torch.empty((1,), dtype=torch.float32, device=x.device)
+        ws = workspace.data_ptr()
+    with torch.cuda.device(x.device):
+        st = _lib().fa_quant_fp8(x.data_ptr(), x8.data_ptr(), ds.data_ptr(), B, H, N, d, sp,
+                                 int(bool(per_tensor)), ws, _stream(x))
+    _check(st, "fa_quant_fp8")
+    del keep
+    return x8, ds
+
+
+def check_device_error(device=None):
+    """Synchronise the current stream and raise FaError if a kernel reported
+    a pipeline timeout since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = _lib().fa_check_device_error(torch.cuda.current_stream(dev).cuda_stream)
+    _check(st, "fa_check_device_error")

@@ -1,0 +1,258 @@
+// api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument checks,
+// TMA descriptor encoding, kernel selection and launch on the caller's
+// stream.  No device memory is allocated here; the only device state is the
+// library's error word (a __device__ int per device).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "attn_fwd.cuh"
+#include "quant_fp8.h"
+
+namespace fa {
+template <int ELEM, int D, bool CAUSAL>
+cudaError_t launch_attn(const AttnLaunch& L);
+}
+
+namespace {
+
+__device__ int g_fa_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fa_status device_setup(int* dev_out, int** err_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_fa_device_error) != cudaSuccess) return FA_ERR_CUDA;
+      st.err_word = static_cast<int*>(p);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.checked = true;
+  }
+  if (!st.supported) return FA_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  *err_out = st.err_word;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D tiled map over a contiguous [BH, N, d] tensor: box = (128-byte row
+// chunk) x 128 rows x 1 head, 128-byte swizzle, out-of-range rows read as 0.
+fa_status encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t BH,
+                     int64_t N, int64_t d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)(d * elem_bytes), (cuuint64_t)(N * d * elem_bytes)};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int64_t B,
+                       int64_t H, int64_t N, int64_t d, float scale, bool* empty) {
+  if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  *empty = (B == 0 || H == 0 || N == 0);
+  if (*empty) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  // index ranges used by the kernels: grid.x = B*H, grid.y = ceil(N / 256)
+  if (B * H > 0x7fffffffLL || N > (int64_t)65535 * 256 || B * H * N > ((int64_t)1 << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+template <int ELEM>
+fa_status dispatch(const fa::AttnLaunch& L, int64_t d, int causal) {
+  cudaError_t e = cudaErrorInvalidValue;
+  if (d == 64) {
+    if constexpr (ELEM == fa::kE4M3) return FA_ERR_UNSUPPORTED;
+    else e = causal ? fa::launch_attn<ELEM, 64, true>(L) : fa::launch_attn<ELEM, 64, false>(L);
+  } else if (d == 128) {
+    e = causal ? fa::launch_attn<ELEM, 128, true>(L) : fa::launch_attn<ELEM, 128, false>(L);
+  } else if (d == 256) {
+    e = causal ? fa::launch_attn<ELEM, 256, true>(L) : fa::launch_attn<ELEM, 256, false>(L);
+  } else {
+    return FA_ERR_UNSUPPORTED;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t N,
+                 int64_t d, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  bool empty = false;
+  fa_status st = check_common(q, k, v, o, lse, B, H, N, d, scale, &empty);
+  if (st != FA_OK || empty) return st;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  fa::AttnLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const CUtensorMapDataType dt =
+      dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((st = encode_map(&L.q, q, dt, 2, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k, dt, 2, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v, dt, 2, B * H, N, d)) != FA_OK) return st;
+  L.prm.o = o;
+  L.prm.lse = lse;
+  L.prm.err = err;
+  L.prm.N = (int)N;
+  L.prm.nblk = (int)((N + 127) / 128);
+  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  L.BH = (int)(B * H);
+  L.stream = stream;
+  return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int64_t B, int64_t H,
+                     int64_t N, int64_t d, int causal, float scale, const float* q_descale, const float* k_descale,
+                     const float* v_descale, cudaStream_t stream) {
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  bool empty = false;
+  fa_status st = check_common(q8, k8, v8, o, lse, B, H, N, d, scale, &empty);
+  if (st != FA_OK || empty) return st;
+  if (d == 64) return FA_ERR_UNSUPPORTED;  // FP8 rows must span the 128-byte swizzle
+  if (!q_descale || !k_descale || !v_descale) return FA_ERR_INVALID_ARG;
+  if (((uintptr_t)k_descale & 3u) || ((uintptr_t)v_descale & 3u) || ((uintptr_t)q_descale & 3u))
+    return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  fa::AttnLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  if ((st = encode_map(&L.q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
+  L.prm.o = o;
+  L.prm.lse = lse;
+  L.prm.q_ds = q_descale;
+  L.prm.k_ds = k_descale;
+  L.prm.v_ds = v_descale;
+  L.prm.err = err;
+  L.prm.N = (int)N;
+  L.prm.nblk = (int)((N + 127) / 128);
+  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  L.BH = (int)(B * H);
+  L.stream = stream;
+  return dispatch<fa::kE4M3>(L, d, causal);
+}
+
+fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                       const int8_t* hadamard_signs, int per_tensor, float* workspace, cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (per_tensor != 0 && per_tensor != 1) return FA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x8) || ((uintptr_t)descale & 3u)) return FA_ERR_INVALID_ARG;
+  if (per_tensor && (!workspace || ((uintptr_t)workspace & 3u))) return FA_ERR_INVALID_ARG;
+  if (B * H > 65535 || N > ((int64_t)1 << 31) - 128) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+
+  fa::QuantLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  if (hadamard_signs) {
+    for (int64_t i = 0; i < d; ++i) {
+      const int8_t sgn = hadamard_signs[i];
+      if (sgn != 1 && sgn != -1) return FA_ERR_INVALID_ARG;
+      if (sgn < 0) L.signs.w[i >> 5] |= 1u << (i & 31);
+    }
+    L.rot = 1;
+    L.rinv = (float)(1.0 / std::sqrt((double)d));
+  } else {
+    L.rot = 0;
+    L.rinv = 1.0f;
+  }
+  L.x = x;
+  L.x8 = static_cast<uint8_t*>(x8);
+  L.descale = descale;
+  L.amax_ws = workspace;
+  L.BH = (int)(B * H);
+  L.N = (int)N;
+  L.d = (int)d;
+  L.nblk = (int)((N + 127) / 128);
+  L.per_tensor = per_tensor;
+  L.stream = stream;
+  return fa::launch_quant(L) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+const char* fa_status_string(fa_status status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dimension or device (needs sm_103)";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel pipeline wait ran out of time";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_check_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_fa_device_error, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_device_error, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// Instances of the attention forward kernel for bf16 operands.
+#include "attn_fwd.cuh"
+
+namespace fa {
+template cudaError_t launch_attn<kBF16, 64, false>(const AttnLaunch&);
+template cudaError_t launch_attn<kBF16, 64, true>(const AttnLaunch&);
+template cudaError_t launch_attn<kBF16, 128, false>(const AttnLaunch&);
+template cudaError_t launch_attn<kBF16, 128, true>(const AttnLaunch&);
+template cudaError_t launch_attn<kBF16, 256, false>(const AttnLaunch&);
+template cudaError_t launch_attn<kBF16, 256, true>(const AttnLaunch&);
+}  // namespace fa

@@ -1,0 +1,626 @@
+// attn_fwd.cuh -- fused exact attention forward for sm_103a (tcgen05 + TMEM +
+// TMA), one template for BF16 / FP16 / FP8-E4M3 operands.
+//
+// What it computes (per query row i of head (b,h)):
+//   S_ij = scale * q_i . k_j  (FP8: times the Q-block and K-block descales),
+//   O_i  = sum_j softmax_j(S_i.) v_j,   LSE_i = ln sum_j exp(S_ij),
+// by the online-softmax recurrence over 128-key tiles: running maximum m,
+// running sum l and an fp32 accumulator o that is rescaled by exp(m_old -
+// m_new) whenever m moves, O = o / l at the end (wmrh.cn FlashAttention V3
+// article, sec. 2.1; "FlashAttention-3: async pipelines on Hopper", section
+// "Online Softmax is still the core of exact merging").  The N x N scores
+// live only in tensor memory, one 128 x 128 tile at a time.
+//
+// CTA organisation (warp-specialised roles, chosen for Blackwell rather than
+// the Hopper producer / consumer-warpgroup split of the pages):
+//   * load warp    one thread issues TMA copies: the Q tile(s) once, then K
+//                  and V tiles through an NS-slot shared-memory ring with
+//                  full/empty mbarriers ("FlashAttention-3: async pipelines
+//                  on Hopper", section "first overlap: producer and consumer
+//                  in parallel": stage = j mod s, two states per stage).
+//   * MMA warp     one thread issues every tcgen05.mma: S = Q K^T into TMEM,
+//                  then O += P V with P read from TMEM; it also allocates TMEM.
+//   * softmax      one warpgroup per Q tile, one thread per query row: reads
+//                  S from TMEM, masks, takes the row max, rescales O in TMEM
+//                  when the max moved by more than TAU (exact: o, l, m stay
+//                  consistent), writes P back into TMEM over S, keeps l; at
+//                  the end divides by l and stores O and LSE.
+// With two Q tiles per CTA (d <= 128) the MMA warp interleaves the two
+// tiles, so the tensor core works on one tile's GEMMs while the other tile's
+// softmax runs (the Blackwell form of the pages' ping-pong of two consumer
+// warpgroups, section "second overlap").  With one Q tile (d = 256) S is
+// double-buffered in TMEM and Q K_{j+1}^T runs during softmax j (the pages'
+// intra-warpgroup two-stage pipeline, section "third overlap").
+// Causal: key tiles above the diagonal are never loaded or multiplied; the
+// diagonal tile is masked (section "why causal shapes are harder to
+// schedule").
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+enum ElemKind : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
+
+constexpr int kBM = 128;  // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kSmemLimit = 232448;
+
+template <int ELEM, int D, bool CAUSAL>
+struct AttnCfg {
+  static constexpr int ES = (ELEM == kE4M3) ? 1 : 2;           // bytes per element
+  static constexpr int MMA_KIND = (ELEM == kE4M3) ? 1 : 0;     // kind::f16 or kind::f8f6f4
+  static constexpr int ROW_BYTES = D * ES;
+  static_assert(ROW_BYTES % 128 == 0, "rows must be a multiple of the 128-byte swizzle span");
+  static constexpr int CH_ELEMS = 128 / ES;                    // elements per 128-byte chunk
+  static constexpr int NCH = ROW_BYTES / 128;                  // chunks per row
+  static constexpr int CHUNK_BYTES = 128 * 128;                // 128 rows x 128 bytes
+  static constexpr int NQT = (D <= 128) ? 2 : 1;               // Q tiles per CTA
+  static constexpr int TILE_BYTES = kBN * ROW_BYTES;           // one K or V tile
+  static constexpr int SLOT_BYTES = TILE_BYTES < 32768 ? TILE_BYTES : 32768;
+  static constexpr int SPT = TILE_BYTES / SLOT_BYTES;          // ring slots per tile
+  static constexpr int SLOT_CH = SLOT_BYTES / CHUNK_BYTES;     // chunks per slot
+  static constexpr int SLOT_D = SLOT_CH * CH_ELEMS;            // head-dim columns per slot
+  static constexpr int Q_BYTES = NQT * kBM * ROW_BYTES;
+  static constexpr int NS_MAX = (kSmemLimit - 1024 - 1024 - Q_BYTES) / SLOT_BYTES;
+  static constexpr int NS = NS_MAX > 8 ? 8 : NS_MAX;           // ring depth
+  static_assert(NS >= 2 * SPT, "ring too shallow");
+  static constexpr int KSTEP = 32 / ES;                        // MMA K per instruction (32 bytes)
+  static constexpr int KSTEPS_QK = D / KSTEP;
+  static constexpr int KSTEPS_PV = kBN / KSTEP;
+  static constexpr int P_COLS = kBN * ES / 4;                  // TMEM columns of P per row
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL0 = 0;                        // S/P buffers at 0 and 128
+  static constexpr uint32_t O_COL0 = 256;                      // O accumulators from 256
+  static_assert(O_COL0 + NQT * D <= TMEM_COLS, "TMEM budget");
+  static constexpr int SOFTMAX_WARPS = 4 * NQT;
+  static constexpr int MMA_WARP = SOFTMAX_WARPS;
+  static constexpr int LOAD_WARP = SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // lazy-rescale threshold (log2 units): P <= 2^TAU.  FP8 P must stay far
+  // below the E4M3 maximum, so FP8 rescales whenever the max moves.
+  static constexpr float TAU = (ELEM == kE4M3) ? 0.0f : 8.0f;
+  // FP8: P is stored as p * 2^8 * (s_Vj / max_j s_Vj) <= 256 < 448
+  static constexpr float P8_SCALE = 256.0f;
+  static constexpr uint32_t A_FMT = (ELEM == kBF16) ? 1u : 0u;  // bf16=1, f16=0, e4m3=0
+  static constexpr uint32_t IDESC_QK = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN);
+  static constexpr uint32_t IDESC_PV = instr_desc(A_FMT, A_FMT, 0, 1, 128, SLOT_D);
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NS * SLOT_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 1024 + 1024;  // + barriers + alignment slack
+  static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+};
+
+struct AttnParams {
+  void* o;              // [BH, N, D] bf16 / f16 (FP8 path: bf16)
+  float* lse;           // [BH, N]
+  const float* q_ds;    // FP8 only: [BH, nblk]
+  const float* k_ds;
+  const float* v_ds;
+  int* err;             // device error word
+  int N;
+  int nblk;             // ceil(N / 128)
+  float scale_log2;     // scale * log2(e)
+};
+
+// Barriers in shared memory.
+template <int NS>
+struct Bars {
+  uint64_t q_full;
+  uint64_t full[NS];
+  uint64_t empty[NS];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_ready[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Number of key tiles a Q tile starting at row q0 visits.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_tiles_for(int q0, int nkv) {
+  if constexpr (CAUSAL) {
+    int last = q0 / kBN + (kBM / kBN) - 1;  // diagonal tile (kBM == kBN)
+    return last + 1 < nkv ? last + 1 : nkv;
+  } else {
+    return nkv;
+  }
+}
+
+// The ring carries K and V tiles in the order the MMA warp consumes them:
+//   two Q tiles : K0 V0 K1 V1 ...            (S(j+1) is issued after PV(j))
+//   one Q tile  : K0 K1 V0 K2 V1 K3 V2 ...   (S(j+2) is issued after PV(j))
+
+template <int ELEM, int D, bool CAUSAL>
+__global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnParams prm) {
+  using C = AttnCfg<ELEM, D, CAUSAL>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars<C::NS>* bars = reinterpret_cast<Bars<C::NS>*>(smem + C::OFF_BAR);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int N = prm.N;
+  const int group = (CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.y);  // heaviest first when causal
+  const int q_base = group * (C::NQT * kBM);
+  const int nkv = (N + kBN - 1) / kBN;
+
+  // per-tile activity and key-tile counts
+  int Jt[2];
+  bool active[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = q_base + t * kBM;
+    active[t] = (t < C::NQT) && (q0 < N);
+    Jt[t] = active[t] ? kv_tiles_for<CAUSAL>(q0, nkv) : 0;
+  }
+  const int J = Jt[0] > Jt[1] ? Jt[0] : Jt[1];
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_ready[t], 1);
+      mbar_init(&bars->o_full[t], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ load --
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = policy_evict_last();
+      const uint64_t pol_q = policy_evict_first();
+      uint32_t qbytes = 0;
+      for (int t = 0; t < C::NQT; ++t) qbytes += active[t] ? (uint32_t)(kBM * C::ROW_BYTES) : 0u;
+      mbar_arrive_expect_tx(&bars->q_full, qbytes);
+      for (int t = 0; t < C::NQT; ++t) {
+        if (!active[t]) continue;
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_load_3d_hint(smem + C::OFF_Q + (t * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, &bars->q_full,
+                           ch * C::CH_ELEMS, q_base + t * kBM, bh, pol_q);
+      }
+      int pos = 0;
+      bool ok = true;
+      // one K or V tile (SPT ring slots) into the ring
+      auto load_tile = [&](bool is_v, int j) {
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+        for (int sp = 0; sp < C::SPT && ok; ++sp, ++pos) {
+          const int slot = pos % C::NS;
+          const uint32_t ph = (uint32_t)((pos / C::NS) & 1);
+          if (!mbar_wait(&bars->empty[slot], ph ^ 1u, abort_flag, prm.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
+          for (int ch = 0; ch < C::SLOT_CH; ++ch)
+            tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,
+                             &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, bh, pol_kv);
+        }
+      };
+      if constexpr (C::NQT == 2) {
+        for (int j = 0; j < J && ok; ++j) {
+          load_tile(false, j);
+          load_tile(true, j);
+        }
+      } else {
+        for (int j = 0; j < J && j < 2 && ok; ++j) load_tile(false, j);
+        for (int j = 0; j < J && ok; ++j) {
+          load_tile(true, j);
+          if (j + 2 < J) load_tile(false, j + 2);
+        }
+      }
+      // Never leave with copies in flight: wait (bounded) for the last fill
+      // of every slot that was used.
+      const int used = pos < C::NS ? pos : C::NS;
+      for (int k = 0; k < used; ++k) {
+        const int p_last = pos - 1 - k;
+        const int slot = p_last % C::NS;
+        const uint32_t ph = (uint32_t)((p_last / C::NS) & 1);
+        uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&bars->full[slot], ph) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
+        }
+      }
+      {
+        uint64_t t0 = globaltimer();
+        while (qbytes && !mbar_try_wait(&bars->q_full, 0) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      const uint32_t q_s = smem_u32(smem + C::OFF_Q);
+      const uint32_t ring_s = smem_u32(smem + C::OFF_RING);
+      int pos = 0;  // ring position of the next item to consume
+      bool ok = (J > 0) ? mbar_wait(&bars->q_full, 0, abort_flag, prm.err) : true;
+
+      // wait for a whole tile (SPT slots) at the current ring position
+      auto wait_tile = [&](int p) -> bool {
+        for (int sp = 0; sp < C::SPT; ++sp) {
+          const int slot = (p + sp) % C::NS;
+          if (!mbar_wait(&bars->full[slot], (uint32_t)(((p + sp) / C::NS) & 1), abort_flag, prm.err))
+            return false;
+        }
+        tc_fence_after();
+        return true;
+      };
+      auto release_tile = [&](int p) {
+        for (int sp = 0; sp < C::SPT; ++sp) mma_commit(&bars->empty[(p + sp) % C::NS]);
+      };
+      // S_buf = Q_t K^T for the K tile at ring position p
+      auto issue_qk = [&](int t, int buf, int p) {
+        const uint32_t d_tmem = tmem + C::S_COL0 + buf * kBN;
+#pragma unroll
+        for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
+          const int byte_k = ks * 32;                         // byte offset along the row
+          const int ch = byte_k / 128;
+          const int in_ch = byte_k % 128;
+          const int sp = ch / C::SLOT_CH;                     // which slot of the tile
+          const int ch_in_slot = ch % C::SLOT_CH;
+          const uint32_t a = q_s + (t * C::NCH + ch) * C::CHUNK_BYTES + in_ch;
+          const uint32_t b = ring_s + ((p + sp) % C::NS) * C::SLOT_BYTES + ch_in_slot * C::CHUNK_BYTES + in_ch;
+          mma_ss<C::MMA_KIND>(d_tmem, smem_desc(a, 16, 1024, 2), smem_desc(b, 16, 1024, 2), C::IDESC_QK,
+                              ks > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_buf V for the V tile at ring position p
+      auto issue_pv = [&](int t, int buf, int p, bool acc) {
+        const uint32_t p_tmem = tmem + C::S_COL0 + buf * kBN;
+#pragma unroll
+        for (int sp = 0; sp < C::SPT; ++sp) {
+          const uint32_t d_tmem = tmem + C::O_COL0 + t * D + sp * C::SLOT_D;
+          const uint32_t vbase = ring_s + ((p + sp) % C::NS) * C::SLOT_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
+            // keys ks*KSTEP .. +KSTEP-1 are KSTEP/8 groups of 8 rows (1024 B each)
+            const uint32_t b = vbase + ks * (C::KSTEP / 8) * 1024;
+            mma_ts<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, smem_desc(b, C::CHUNK_BYTES, 1024, 2), C::IDESC_PV,
+                                (acc || ks > 0) ? 1u : 0u);
+          }
+        }
+      };
+
+      if constexpr (C::NQT == 2) {
+        // prologue: S_t(0) for both tiles
+        if (ok && J > 0) {
+          ok = wait_tile(pos);
+          if (ok) {
+            for (int t = 0; t < 2; ++t)
+              if (Jt[t] > 0) {
+                issue_qk(t, t, pos);
+                mma_commit(&bars->s_full[t]);
+              }
+            release_tile(pos);
+          }
+          pos += C::SPT;
+        }
+        for (int j = 0; j < J && ok; ++j) {
+          const int pv_pos = pos;            // V_j
+          const int k_pos = pos + C::SPT;    // K_{j+1}
+          bool v_ready = false, k_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= Jt[t]) continue;
+            if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
+            ok = mbar_wait(&bars->p_full[t], (uint32_t)(j & 1), abort_flag, prm.err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, t, pv_pos, j > 0);
+            if (j + 1 < Jt[t]) {
+              if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
+              issue_qk(t, t, k_pos);
+              mma_commit(&bars->s_full[t]);
+            } else {
+              mma_commit(&bars->o_full[t]);
+            }
+          }
+          if (!ok) break;
+          release_tile(pv_pos);
+          pos += C::SPT;
+          if (j + 1 < J) {
+            release_tile(k_pos);
+            pos += C::SPT;
+          }
+        }
+      } else {
+        // one Q tile, S double-buffered: S(0), S(1), then PV(j), S(j+2)
+        const int Jn = Jt[0];
+        int k_pos[2] = {0, 0};
+        for (int j = 0; j < 2 && j < Jn && ok; ++j) {
+          ok = wait_tile(pos);
+          if (!ok) break;
+          issue_qk(0, j, pos);
+          mma_commit(&bars->s_full[j]);
+          release_tile(pos);
+          k_pos[j] = pos;
+          pos += C::SPT;
+        }
+        for (int j = 0; j < Jn && ok; ++j) {
+          const int b = j & 1;
+          ok = wait_tile(pos);  // V_j
+          if (!ok) break;
+          ok = mbar_wait(&bars->p_full[b], (uint32_t)((j >> 1) & 1), abort_flag, prm.err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, b, pos, j > 0);
+          mma_commit(&bars->o_ready[b]);
+          release_tile(pos);
+          pos += C::SPT;
+          if (j + 2 < Jn) {
+            ok = wait_tile(pos);  // K_{j+2}
+            if (!ok) break;
+            issue_qk(0, b, pos);
+            mma_commit(&bars->s_full[b]);
+            release_tile(pos);
+            pos += C::SPT;
+          }
+        }
+        if (ok && Jn > 0) mma_commit(&bars->o_full[0]);
+        (void)k_pos;
+      }
+      // drain: every MMA issued by this thread has completed before TMEM is freed
+      mma_commit(&bars->drain);
+      uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&bars->drain, 0) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- softmax --
+    const int t = warp / 4;                 // Q tile of this warpgroup
+    const int wq = warp % 4;                // TMEM lane quarter
+    const int r = wq * 32 + lane;           // row within the tile
+    const int q0 = q_base + t * kBM;
+    const int row = q0 + r;
+    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const int Jn = Jt[t];
+    const bool neg = prm.scale_log2 < 0.0f;
+
+    float m_run = -INFINITY;  // reference maximum, log2 units
+    float l_run = 0.0f;
+    float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
+    int o_seen[2] = {0, 0};   // one-Q-tile mode: o_ready phases consumed per buffer
+    bool ok = true;
+    const int bh_blk = bh * prm.nblk;
+    float qds = 1.0f, vmax = 1.0f;
+    if (ELEM == kE4M3 && Jn > 0) {
+      qds = prm.q_ds[bh_blk + q0 / kBM];
+      vmax = 0.0f;
+      for (int b = 0; b < prm.nblk; ++b) vmax = fmaxf(vmax, prm.v_ds[bh_blk + b]);
+      if (!(vmax > 0.0f)) vmax = 1.0f;
+      v_mult = vmax / C::P8_SCALE;
+    }
+
+    for (int j = 0; j < Jn && ok; ++j) {
+      const int buf = (C::NQT == 2) ? t : (j & 1);
+      const uint32_t ph = (C::NQT == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], ph, abort_flag, prm.err));
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (C::NQT == 1) {
+        // PV(j-2) completed before S(j) (issue order), so its o_ready phase
+        // is already done: consume it to keep the phase count in step.
+        if (j >= 2 && o_seen[buf] < ((j - 2) >> 1) + 1) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bars->o_ready[buf], (uint32_t)(o_seen[buf] & 1), abort_flag, prm.err));
+          o_seen[buf]++;
+          if (!ok) break;
+        }
+      }
+      const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
+      float s[kBN];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c4 = 0; c4 < kBN / 32; ++c4) {
+          tmem_ld32(s_addr + c4 * 32, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
+        }
+        tmem_wait_ld();
+      }
+      // scale of this tile (log2 units)
+      float cj = prm.scale_log2;
+      float pv_fac = 1.0f;
+      if constexpr (ELEM == kE4M3) {
+        cj *= qds * prm.k_ds[bh_blk + j];
+        pv_fac = C::P8_SCALE * (prm.v_ds[bh_blk + j] / vmax);
+      }
+      const int col0 = j * kBN;
+      const bool need_mask = (col0 + kBN > N) || (CAUSAL && col0 + kBN - 1 > q0);
+      const float mask_val = neg ? INFINITY : -INFINITY;
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const int col = col0 + c;
+          const bool masked = (col >= N) || (CAUSAL && col > row);
+          s[c] = masked ? mask_val : s[c];
+        }
+      }
+      float mx;
+      if (!neg) {
+        mx = s[0];
+#pragma unroll
+        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      } else {
+        mx = s[0];
+#pragma unroll
+        for (int c = 1; c < kBN; ++c) mx = fminf(mx, s[c]);
+      }
+      const float mx2 = mx * cj;
+      float alpha = 1.0f;
+      const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY);
+      if (move) {
+        alpha = ex2(m_run - mx2);  // 0 on the first tile
+        m_run = mx2;
+      }
+      l_run *= alpha;
+      // rescale O when any row of the warp moved (never on the first tile)
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        if constexpr (C::NQT == 1) {
+          // O holds PV(j-1): wait for it
+          const int pb = (j - 1) & 1;
+          if (o_seen[pb] < ((j - 1) >> 1) + 1) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->o_ready[pb], (uint32_t)(o_seen[pb] & 1), abort_flag, prm.err));
+            o_seen[pb]++;
+            if (!ok) break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t u[32];
+          tmem_ld32(o_addr + c0, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(o_addr + c0, u);
+        }
+        tmem_wait_st();
+      }
+      // P = 2^(s*cj - m), row sum, pack and write back over S
+      const float nm = -m_run;
+      float lsum = 0.0f;
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const float p = ex2(fmaf(s[c], cj, nm));
+          s[c] = (s[c] == mask_val) ? 0.0f : p;
+          lsum += s[c];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          s[c] = ex2(fmaf(s[c], cj, nm));
+          lsum += s[c];
+        }
+      }
+      l_run += lsum;
+      {
+        uint32_t u[32];
+        if constexpr (ELEM == kE4M3) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            u[i] = pack_e4m3x4(s[4 * i] * pv_fac, s[4 * i + 1] * pv_fac, s[4 * i + 2] * pv_fac,
+                               s[4 * i + 3] * pv_fac);
+          tmem_st32(s_addr, u);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float a = s[h * 64 + 2 * i], b = s[h * 64 + 2 * i + 1];
+              u[i] = (ELEM == kBF16) ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+            }
+            tmem_st32(s_addr + h * 32, u);
+          }
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[buf]);
+    }
+
+    // ---------------------------------------------------------- epilogue --
+    if (ok && Jn > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], 0, abort_flag, prm.err));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = (l_run > 0.0f) ? (1.0f / l_run) : 0.0f;
+        const float f = inv_l * v_mult;
+        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+        const bool store = row < N;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + (size_t)(store ? row : 0)) * D * 2;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t u[32];
+          tmem_ld32(o_addr + c0, u);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = __uint_as_float(u[2 * i]) * f, b = __uint_as_float(u[2 * i + 1]) * f;
+            w[i] = (ELEM == kFP16) ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+          }
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa
+
+namespace fa {
+
+// Everything one launch needs; filled by the C-ABI layer.
+struct AttnLaunch {
+  CUtensorMap q, k, v;
+  AttnParams prm;
+  int BH;
+  cudaStream_t stream;
+};
+
+template <int ELEM, int D, bool CAUSAL>
+cudaError_t launch_attn(const AttnLaunch& L) {
+  using C = AttnCfg<ELEM, D, CAUSAL>;
+  auto kern = attn_fwd_kernel<ELEM, D, CAUSAL>;
+  static bool attr_done[64] = {};  // the attribute is per function and device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  const int groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
+  dim3 grid(L.BH, groups, 1);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.prm);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,196 @@
+// quant_fp8.cu -- fp32 -> FP8 E4M3 with one scale per 128-row block (or one
+// per tensor), optionally after the incoherent-processing rotation
+// x -> x diag(sigma) H_d / sqrt(d) ("FlashAttention-3: async pipelines on
+// Hopper", sections "why block quantization beats a per-tensor scale" and
+// "how incoherent processing flattens outliers"; E4M3 maximum 448 from the
+// wmrh.cn FlashAttention V3 article, sec. 3.3).
+//
+// One CTA per (head, 128-row block), one warp per row at a time.  Each lane
+// holds d/32 consecutive elements; the Walsh-Hadamard butterfly runs inside
+// the lane for strides below d/32 and across lanes (shuffle) above, stride
+// 1, 2, 4, ... in fp32, so every element sees the same sequence of fp32
+// additions as the plain in-place butterfly.  The rotated rows stay in shared
+// memory between the amax pass and the encode pass.  The 1/sqrt(d) factor is
+// folded into the stored descale, so the codes are RNE(y / s) with
+// s = amax(y) / 448 of the unnormalised rotated block y.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "quant_fp8.h"
+
+namespace fa {
+
+template <int D>
+__device__ __forceinline__ void rotate_row(float (&v)[D / 32], int lane, const SignBits& sg, bool rot) {
+  constexpr int E = D / 32;
+  if (!rot) return;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = lane * E + e;
+    if ((sg.w[i >> 5] >> (i & 31)) & 1u) v[e] = -v[e];
+  }
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (!(e & h)) {
+        const float a = v[e], b = v[e + h];
+        v[e] = __fadd_rn(a, b);
+        v[e + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[e], m);
+      v[e] = (lane & m) ? __fsub_rn(p, v[e]) : __fadd_rn(v[e], p);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// MODE 0: per-block scale.  MODE 1: per-tensor amax into *amax_ws (atomic).
+// MODE 2: per-tensor encode with the amax in *amax_ws.
+template <int D, int MODE>
+__global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
+                                                         float* __restrict__ descale, int N, int nblk,
+                                                         SignBits sg, int rot, float rinv,
+                                                         float* __restrict__ amax_ws) {
+  constexpr int E = D / 32;
+  constexpr int ROWS = 128;
+  extern __shared__ __align__(16) float ys[];  // [ROWS][D] (MODE 0 only)
+  __shared__ float red[8];
+  const int blk = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blk * ROWS;
+  const int nrows = min(ROWS, N - r0);
+  const size_t base = ((size_t)bh * N + r0) * D;
+
+  float amax = 0.0f;
+  for (int r = warp; r < nrows; r += 8) {
+    float v[E];
+    const float* src = x + base + (size_t)r * D + lane * E;
+    if constexpr (E == 2) {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
+    } else {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        const float4 t = reinterpret_cast<const float4*>(src)[q];
+        v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
+      }
+    }
+    rotate_row<D>(v, lane, sg, rot != 0);
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+    if constexpr (MODE == 0) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) ys[r * D + lane * E + e] = v[e];
+    } else if constexpr (MODE == 2) {
+      // per-tensor encode: scale known up front
+      const float am = *amax_ws;
+      const float s = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+      uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
+      if constexpr (E == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+          const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * q], s), __fdiv_rn(v[4 * q + 1], s));
+          const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * q + 2], s), __fdiv_rn(v[4 * q + 3], s));
+          reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
+        }
+      }
+    }
+  }
+  if constexpr (MODE == 2) {
+    if (threadIdx.x == 0) {
+      const float am = *amax_ws;
+      const float s = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+      descale[(size_t)bh * nblk + blk] = __fmul_rn(s, rinv);
+    }
+    return;
+  }
+  // block amax
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float a = (lane < 8) ? red[lane] : 0.0f;
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+    if (lane == 0) red[0] = a;
+  }
+  __syncthreads();
+  amax = red[0];
+  if constexpr (MODE == 1) {
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(amax_ws), __float_as_int(amax));
+    return;
+  } else {
+    const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    for (int r = warp; r < nrows; r += 8) {
+      uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
+      const float* y = ys + r * D + lane * E;
+      if constexpr (E == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s));
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+          const uint32_t lo = e4m3x2(__fdiv_rn(y[4 * q], s), __fdiv_rn(y[4 * q + 1], s));
+          const uint32_t hi = e4m3x2(__fdiv_rn(y[4 * q + 2], s), __fdiv_rn(y[4 * q + 3], s));
+          reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
+        }
+      }
+    }
+    if (threadIdx.x == 0) descale[(size_t)bh * nblk + blk] = __fmul_rn(s, rinv);
+  }
+}
+
+template <int D>
+static cudaError_t launch_quant_d(const QuantLaunch& L) {
+  const dim3 grid(L.nblk, L.BH, 1);
+  const size_t smem = 128u * D * sizeof(float);
+  if (!L.per_tensor) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+      e = cudaFuncSetAttribute(quant_e4m3_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    quant_e4m3_kernel<D, 0><<<grid, 256, smem, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot,
+                                                             L.rinv, nullptr);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaMemsetAsync(L.amax_ws, 0, sizeof(float), L.stream);
+  if (e != cudaSuccess) return e;
+  quant_e4m3_kernel<D, 1><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
+                                                       L.amax_ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quant_e4m3_kernel<D, 2><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
+                                                       L.amax_ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const QuantLaunch& L) {
+  switch (L.d) {
+    case 64: return launch_quant_d<64>(L);
+    case 128: return launch_quant_d<128>(L);
+    case 256: return launch_quant_d<256>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

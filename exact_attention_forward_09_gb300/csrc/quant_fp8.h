@@ -1,0 +1,29 @@
+// quant_fp8.h -- launch interface of the FP8 E4M3 quantisation kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// d <= 256 sign bits of the random diagonal: bit i set <=> sigma_i = -1.
+struct SignBits {
+  uint32_t w[8];
+};
+
+struct QuantLaunch {
+  const float* x;   // [BH, N, d] fp32
+  uint8_t* x8;      // [BH, N, d] E4M3 codes
+  float* descale;   // [BH, nblk]
+  float* amax_ws;   // per-tensor mode: one float of scratch
+  int BH, N, d, nblk;
+  int per_tensor;
+  int rot;
+  float rinv;       // 1/sqrt(d) as fp32 when rotating, else 1
+  SignBits signs;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_quant(const QuantLaunch& L);
+
+}  // namespace fa

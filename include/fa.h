@@ -1,0 +1,148 @@
+/*
+ * fa.h -- C ABI of the fused exact attention forward library (libfa.so) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation.  Exact scaled-dot-product attention, forward pass:
+ *     S = scale * Q K^T,   P = softmax(S) row-wise,   O = P V,
+ *     LSE_i = ln sum_j exp(S_ij)
+ * (definition: wmrh.cn FlashAttention V3 article, sec. 1.1 "self-attention
+ * and the O(N^2) problem").  The kernels stream K/V tiles through shared
+ * memory and run the online-softmax recurrence -- running row max m, running
+ * row sum l, rescaled accumulator o, initially -inf, 0, 0, output o/l after
+ * the last tile (same article, sec. 2.1; "FlashAttention-3: async pipelines
+ * on Hopper" (charlestar.github.io), section "Online Softmax is still the
+ * core of exact merging") -- so the N x N score matrix never reaches HBM.
+ * Causal attention keeps the lower triangle, key j <= query i, and skips the
+ * key tiles above the diagonal ("FlashAttention-3: async pipelines on
+ * Hopper", section "why causal shapes are harder to schedule").  The LSE
+ * output is not defined on the pages; here it is the natural log of the sum
+ * of exponentials of the scaled, masked scores, in fp32.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous row-major [B, H, N, d] (PyTorch SDPA order,
+ *     wmrh.cn article sec. 6.4); LSE is [B, H, N] fp32.
+ *   - Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *     16-byte aligned, owned by the caller.  Inputs are only read; outputs are
+ *     fully overwritten.  The library allocates no memory in these calls.
+ *   - Work is enqueued on `stream` and the call returns without waiting.
+ *     A launch error is reported as FA_ERR_CUDA; errors found by the kernels
+ *     (a pipeline wait that ran out of time) are reported later by
+ *     fa_check_device_error().
+ *   - B*H*N == 0 is valid and does nothing.
+ *   - Head dimension d must be 64, 128 or 256.  The library runs only on
+ *     compute capability 10.3 (sm_103a); anything else is FA_ERR_UNSUPPORTED.
+ *     There is no fallback path.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, non-finite scale, bad dtype */
+    FA_ERR_UNSUPPORTED = 2,   /* head dimension or device not supported                            */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or kernel launch failed                 */
+    FA_ERR_TIMEOUT = 4        /* a kernel's pipeline wait ran out of time (see fa_check_device_error) */
+} fa_status;
+
+typedef enum {
+    FA_DTYPE_BF16 = 0,
+    FA_DTYPE_FP16 = 1
+} fa_dtype;
+
+/* Maximum number of rows per FP8 quantisation block (one scale per block). */
+#define FA_FP8_BLOCK_ROWS 128
+
+/*
+ * fa_fwd -- BF16 / FP16 attention forward.
+ *   q, k, v  [B, H, N, d] of `dtype` (device, read only)
+ *   o        [B, H, N, d] of `dtype` (device, written), rounded to nearest even
+ *   lse      [B, H, N] fp32 (device, written)
+ *   causal   0: every key visible; 1: key j visible to query i iff j <= i
+ *   scale    multiplies Q K^T before the softmax (usually 1/sqrt(d)); finite
+ *   dtype    FA_DTYPE_BF16 or FA_DTYPE_FP16
+ * Softmax statistics and accumulation are fp32; P is rounded to `dtype`
+ * before the P V product ("FlashAttention-3: async pipelines on Hopper",
+ * section "Online Softmax is still the core of exact merging": FP16/BF16
+ * keep the rescaling and accumulation state in FP32).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int64_t B, int64_t H, int64_t N, int64_t d,
+                 int causal, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * fa_fwd_fp8 -- FP8 E4M3 attention forward with per-block scales.
+ *   q8, k8, v8  [B, H, N, d] E4M3 codes (device, read only), as written by
+ *               fa_quant_fp8; real value = decode(code) * descale of its block
+ *   q_descale, k_descale, v_descale
+ *               [B, H, ceil(N/128)] fp32 (device): one scale per 128-row block
+ *               ("FlashAttention-3: async pipelines on Hopper", section "why
+ *               block quantization beats a per-tensor scale": the Q/K block
+ *               scales are restored on each score tile, the V block scale is
+ *               applied with the P V product)
+ *   o           [B, H, N, d] bf16 (device, written);  lse [B, H, N] fp32
+ *   causal, scale as in fa_fwd.
+ * Q K^T and P V run on the FP8 tensor cores with fp32 accumulation; the
+ * softmax state is fp32 ("FlashAttention-3: async pipelines on Hopper",
+ * section "FP8 attention is still not FP8 end to end").  If Q and K were
+ * rotated by the same orthogonal matrix (fa_quant_fp8 with signs), the
+ * scores are unchanged and O needs no correction; V is never rotated.
+ */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t N, int64_t d,
+                     int causal, float scale,
+                     const float* q_descale, const float* k_descale, const float* v_descale,
+                     cudaStream_t stream);
+
+/*
+ * fa_quant_fp8 -- quantise fp32 [B, H, N, d] to E4M3 with one scale per
+ * 128-row block (per_tensor = 0) or one scale for the whole tensor
+ * (per_tensor = 1, the baseline), optionally after the incoherent-processing
+ * rotation x -> x diag(signs) H_d / sqrt(d) ("FlashAttention-3: async
+ * pipelines on Hopper", section "how incoherent processing flattens
+ * outliers": a random +-1 diagonal combined with a Hadamard matrix, applied
+ * to both Q and K, never to V).
+ *   x              [B, H, N, d] fp32 (device, read only)
+ *   x8             [B, H, N, d] E4M3 codes (device, written)
+ *   descale        [B, H, ceil(N/128)] fp32 (device, written): the value to
+ *                  multiply a code by; scale = amax/448 of the (rotated) block
+ *                  (wmrh.cn article sec. 3.3: 448 is the E4M3 maximum), 1 for
+ *                  an all-zero block, times 1/sqrt(d) when rotating
+ *   hadamard_signs HOST pointer to d int8 entries of +1/-1, or NULL for no
+ *                  rotation; read during the call only
+ *   per_tensor     0 or 1
+ *   workspace      per_tensor = 1: DEVICE pointer to one float of scratch
+ *                  (overwritten; calls sharing it must not overlap on the GPU);
+ *                  per_tensor = 0: ignored, may be NULL
+ * Codes are round-to-nearest-even of (y / scale) in fp32, saturated at 448.
+ */
+fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
+                       int64_t B, int64_t H, int64_t N, int64_t d,
+                       const int8_t* hadamard_signs, int per_tensor, float* workspace,
+                       cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(fa_status status);
+
+/*
+ * fa_check_device_error -- synchronises `stream`, then reports and clears the
+ * library's device error word on the current device: FA_ERR_TIMEOUT if a
+ * kernel gave up on a pipeline wait since the last check, FA_ERR_CUDA if the
+ * synchronisation itself failed, else FA_OK.
+ */
+fa_status fa_check_device_error(cudaStream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,88 @@
+"""The C-ABI library loads, exports every entry point include/fa.h declares,
+and rejects bad arguments on the host (CPU only: no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa_lib():
+    from exact_attention_forward_09_gb300 import build
+    build.build()
+    import exact_attention_forward_09_gb300 as fa
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_fp8", "fa_quant_fp8", "fa_status_string", "fa_check_device_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(fa_lib):
+    for name in declared_functions():
+        assert hasattr(fa_lib, name), f"{name} declared in fa.h but not exported by libfa.so"
+
+
+def test_symbols_are_plain_c(fa_lib):
+    # extern "C": the unmangled name resolves
+    for name in declared_functions():
+        ctypes.cast(getattr(fa_lib, name), ctypes.c_void_p)
+
+
+def test_status_strings(fa_lib):
+    for code in range(5):
+        s = fa_lib.fa_status_string(code).decode()
+        assert s.startswith("FA_")
+    assert fa_lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+    assert fa_lib.fa_version() >= 100
+
+
+def test_host_argument_checks(fa_lib):
+    import exact_attention_forward_09_gb300 as fa
+    p = 1 << 20  # any 16-byte-aligned non-null value: these calls return before any CUDA call
+    # negative size
+    assert fa_lib.fa_fwd(p, p, p, p, p, -1, 1, 1, 64, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    # non-finite scale
+    assert fa_lib.fa_fwd(p, p, p, p, p, 1, 1, 1, 64, 0, float("nan"), 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd(p, p, p, p, p, 1, 1, 1, 64, 0, float("inf"), 0, None) == fa.FA_ERR_INVALID_ARG
+    # bad dtype / causal flag
+    assert fa_lib.fa_fwd(p, p, p, p, p, 1, 1, 1, 64, 0, 0.1, 7, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd(p, p, p, p, p, 1, 1, 1, 64, 2, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    # unsupported head dimension
+    assert fa_lib.fa_fwd(p, p, p, p, p, 1, 1, 1, 96, 0, 0.1, 0, None) == fa.FA_ERR_UNSUPPORTED
+    # null / misaligned pointers
+    assert fa_lib.fa_fwd(None, p, p, p, p, 1, 1, 1, 64, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd(p + 2, p, p, p, p, 1, 1, 1, 64, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    # empty problem: a no-op, even with null pointers
+    assert fa_lib.fa_fwd(None, None, None, None, None, 0, 4, 128, 64, 0, 0.1, 0, None) == fa.FA_OK
+    assert fa_lib.fa_fwd(None, None, None, None, None, 2, 4, 0, 128, 1, 0.1, 1, None) == fa.FA_OK
+    # FP8: d = 64 unsupported, missing descales invalid
+    assert fa_lib.fa_fwd_fp8(p, p, p, p, p, 1, 1, 1, 64, 0, 0.1, p, p, p, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_fwd_fp8(p, p, p, p, p, 1, 1, 1, 128, 0, 0.1, None, p, p, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_fp8(None, None, None, None, None, 0, 1, 1, 128, 0, 0.1, None, None, None,
+                             None) == fa.FA_OK
+    # quantiser
+    assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 100, None, 0, None, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 1, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 3, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8(None, None, None, 1, 0, 1, 128, None, 0, None, None) == fa.FA_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import exact_attention_forward_09_gb300 as fa
+    monkeypatch.setattr(fa, "_LIB", None)
+    monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        fa.lib()

@@ -1,0 +1,172 @@
+"""BF16/FP16 attention forward on the GPU against the fp64 oracle, element by
+element, through the C ABI (binding -> libfa.so).
+
+Tolerances (N(0,1) inputs): O max-abs <= 1e-2, O RMSE <= 2e-3, LSE max-abs
+<= 1e-3.  Small shapes are checked on every row; the full-size workloads on a
+seeded sample of rows (always including 0, 127, 128, N-1).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+from gpu_util import assert_bf16_bound, assert_bf16_parity, errors, make_qkv, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_09_gb300 as fa
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+    return fa
+
+
+def _run(fa, B, H, N, d, causal, seed, dtype=torch.bfloat16, scale=None, rows=None):
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    host, (q, k, v) = make_qkv(B, H, N, d, seed, dtype)
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    fa.check_device_error()
+    o_ref, l_ref = oracle_rows(host, causal, scale, rows)
+    return errors(o, lse, o_ref, l_ref, rows)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny(fa, causal):
+    c = gen.TINY
+    err = _run(fa, c["B"], c["H"], c["N"], c["d"], causal, c["seed"], scale=c["scale"])
+    assert_bf16_parity(err, f"tiny causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [1, 100, 128, 129, 255, 257, 384, 640])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_and_tiles(fa, d, N, causal):
+    # N spans: a single row, below one tile, exact tiles, a ragged tail, and
+    # key-tile counts below / equal to / above the ring depth
+    err = _run(fa, 2, 3, N, d, causal, seed=1000 + N + d)
+    assert_bf16_parity(err, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp16(fa, d, causal):
+    err = _run(fa, 1, 4, 300, d, causal, seed=77 + d, dtype=torch.float16)
+    assert_bf16_parity(err, f"fp16 d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_mid_sampled(fa, causal, dtype):
+    c = gen.MID
+    rows = gen.sample_rows(c["N"], 128, 11)
+    err = _run(fa, c["B"], c["H"], c["N"], c["d"], causal, c["seed"], dtype=dtype, rows=rows)
+    assert_bf16_parity(err, f"mid causal={causal} {dtype}")
+
+
+@pytest.mark.parametrize("cfg", gen.sweep_configs(), ids=lambda c: c[0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_sampled(fa, cfg, causal):
+    name, B, H, N, d, seed = cfg
+    rows = gen.sample_rows(N, 48, seed)
+    err = _run(fa, B, H, N, d, causal, seed, rows=rows)
+    assert_bf16_parity(err, f"{name} causal={causal}")
+
+
+def test_long_context_sampled(fa):
+    c = gen.LONG
+    rows = gen.sample_rows(c["N"], 256, 5)
+    err = _run(fa, c["B"], c["H"], c["N"], c["d"], True, c["seed"], rows=rows)
+    assert_bf16_parity(err, "long causal")
+
+
+def test_special_inputs(fa):
+    B, H, N, d = 1, 2, 300, 128
+    host, (q, k, v) = make_qkv(B, H, N, d, 5)
+    # Q = 0: every row is the mean of its visible V rows, LSE = ln(count)
+    qz = torch.zeros_like(q)
+    o, lse = fa.fwd(qz, k, v, causal=False)
+    vf = host[2].double().numpy()
+    assert np.abs(o.float().cpu().numpy() - vf.mean(axis=2, keepdims=True)).max() < 1e-2
+    assert np.abs(lse.cpu().numpy() - math.log(N)).max() < 1e-3
+    o, lse = fa.fwd(qz, k, v, causal=True)
+    pref = np.cumsum(vf, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    assert np.abs(o.float().cpu().numpy() - pref).max() < 1e-2
+    assert np.abs(lse.cpu().numpy() - np.log(np.arange(1, N + 1))[None, None]).max() < 1e-3
+    # causal row 0 is V[0] (to bf16 rounding)
+    o, lse = fa.fwd(q, k, v, causal=True)
+    assert torch.equal(o[:, :, 0].cpu(), host[2][:, :, 0])
+    # negative and zero scale
+    for sc in (-0.09, 0.0):
+        o, lse = fa.fwd(q, k, v, causal=True, scale=sc)
+        o_ref, l_ref = oracle_rows(host, True, sc)
+        assert_bf16_parity(errors(o, lse, o_ref, l_ref), f"scale={sc}")
+    fa.check_device_error()
+
+
+def test_large_scores_lazy_rescale(fa):
+    # keys scaled up along the sequence: a large score spread and rising
+    # maxima exercise the rescale path.  Not N(0,1), so the bound is the one
+    # derived from the bf16 roundings (assert_bf16_bound).
+    B, H, N, d = 1, 2, 1024, 64
+    host, (q, k, v) = make_qkv(B, H, N, d, 6)
+    ramp = torch.linspace(0.2, 3.0, N).view(1, 1, N, 1)
+    k2 = (host[1].float() * ramp).to(torch.bfloat16)
+    host2 = [host[0], k2, host[2]]
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k2.cuda(), v, causal=causal, scale=0.5)
+        o_ref, l_ref = oracle_rows(host2, causal, 0.5)
+        err = errors(o, lse, o_ref, l_ref)
+        assert err["finite"] and err["lse_maxabs"] <= 1e-3, err
+        assert_bf16_bound(o, o_ref, float(host[2].float().abs().max()), f"ramp causal={causal}")
+
+
+def test_deterministic(fa):
+    host, (q, k, v) = make_qkv(2, 4, 1000, 128, 8)
+    o1, l1 = fa.fwd(q, k, v, causal=True)
+    o2, l2 = fa.fwd(q, k, v, causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_two_streams_and_graph(fa):
+    host, (q, k, v) = make_qkv(2, 4, 700, 128, 9)
+    ref_o, ref_l = fa.fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for s, causal in ((s1, False), (s2, True)):
+        with torch.cuda.stream(s):
+            outs.append(fa.fwd(q, k, v, causal=causal))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], ref_o) and torch.equal(outs[0][1], ref_l)
+    o_c, l_c = fa.fwd(q, k, v, causal=True)
+    assert torch.equal(outs[1][0], o_c)
+    # CUDA graph capture and replay
+    o_g = torch.empty_like(q)
+    l_g = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fa.fwd(q, k, v, causal=False, out=o_g, lse=l_g)  # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fa.fwd(q, k, v, causal=False, out=o_g, lse=l_g)
+    o_g.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, ref_o) and torch.equal(l_g, ref_l)
+    fa.check_device_error()
+
+
+def test_back_to_back_shapes(fa):
+    rng = np.random.Generator(np.random.PCG64(123))
+    for it in range(12):
+        d = int(rng.choice([64, 128, 256]))
+        N = int(rng.integers(1, 700))
+        causal = bool(rng.integers(0, 2))
+        err = _run(fa, 1, 2, N, d, causal, seed=2000 + it)
+        assert_bf16_parity(err, f"iter {it}: N={N} d={d} causal={causal}")
