@@ -1,0 +1,431 @@
+"""Benchmark of the fused attention forward on one GB300 (or N replicas).
+
+One step = one fa_fwd call on the workload (every step of the hot path runs
+inside that one kernel launch).  Default workload ("mid"): B=4, H=16,
+N=2048, d=128, bf16 Q/K/V drawn from N(0,1), non-causal, scale 1/sqrt(128).
+
+Timing: W untimed warm-up steps, then K timed steps; before each step a
+512 MB buffer is written to flush L2 (outside the timed events); each step is
+bracketed by CUDA events on the stream the kernel is launched on; the
+reported time is the sum over the K steps, the max over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(independent problems, no data-path collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import attn_inputs as gen  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (BF16, FP8) and % of GB300 dense tensor peak, 1 GPU"
+KERNEL_SOURCES = ["exact_attention_forward_09_gb300/csrc/attn_fwd.cuh",
+                  "exact_attention_forward_09_gb300/csrc/ptx.cuh"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    ent = t.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = max(smax, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm -------
+def run_ours(args, rank, world, device):
+    import torch
+    import exact_attention_forward_09_gb300 as fa
+
+    B, H, N, d = args.B, args.H, args.N, args.d
+    causal = args.causal
+    scale = 1.0 / math.sqrt(d)
+    dtype = torch.bfloat16
+    g = torch.Generator(device=device)
+    g.manual_seed(1 + rank)
+    q = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
+    k = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
+    v = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+    flush = torch.empty(512 * 1024 * 1024 // 4, device=device, dtype=torch.float32)
+    stream = torch.cuda.current_stream(device)
+    flops = gen.flops(B, H, N, d, causal)
+
+    def step():
+        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.check_device_error(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    _barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    _barrier(world)
+    clocks = sampler.stop()
+    fa.check_device_error(device)
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = _max_over_ranks(sum(times_ms), world, device)
+    launch_ms = sum(times_ms) / len(times_ms)
+
+    # end to end through the public API: pinned host inputs -> device, kernel,
+    # result back to pinned host memory, every step
+    qh = q.cpu().pin_memory()
+    kh = k.cpu().pin_memory()
+    vh = v.cpu().pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa.fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, device) / n_e2e
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = run_extra(args, device)
+
+    return dict(times_ms=times_ms, total_ms=total_ms, launch_ms=launch_ms, flops=flops, clocks=clocks,
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, extra=extra)
+
+
+def _time_launches(fn, steps, device, flush):
+    import torch
+    stream = torch.cuda.current_stream(device)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        ts.append(a.elapsed_time(b))
+    return sum(ts) / len(ts)
+
+
+def run_extra(args, device):
+    """Secondary points (not the headline): causal and fp16 on the same
+    workload, the spec region N >= 4k at d = 128, and the FP8 path."""
+    import torch
+    import exact_attention_forward_09_gb300 as fa
+
+    peaks, _ = load_peaks()
+    flush = torch.empty(512 * 1024 * 1024 // 4, device=device, dtype=torch.float32)
+    out = {}
+    g = torch.Generator(device=device)
+    g.manual_seed(7)
+
+    def bf(B, H, N, d, causal, dtype=torch.bfloat16, reps=5):
+        q, k, v = (torch.randn((B, H, N, d), device=device, generator=g).to(dtype) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+        fn = lambda: fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        fn()
+        ms = _time_launches(fn, reps, device, flush)
+        tf = gen.flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+
+    out["mid_causal_bf16"] = bf(4, 16, 2048, 128, True)
+    out["mid_fp16"] = bf(4, 16, 2048, 128, False, torch.float16)
+    for N in (4096, 8192, 16384):
+        B = gen.TOTAL_TOKENS // N
+        out[f"sweep_N{N}_d128"] = bf(B, 16, N, 128, False)
+        out[f"sweep_N{N}_d128_causal"] = bf(B, 16, N, 128, True)
+    out["sweep_N8192_d64"] = bf(2, 32, 8192, 64, False)
+    out["sweep_N8192_d256"] = bf(2, 8, 8192, 256, False)
+
+    # FP8: quantise (block scales + Hadamard on Q and K) then attention
+    fp8_peak = peaks["bf16_tflops"] * 2.0
+    for N in (4096, 16384):
+        B = gen.TOTAL_TOKENS // N
+        x = [torch.randn((B, 16, N, 128), device=device, generator=g) for _ in range(3)]
+        signs = gen.hadamard_signs(128, 4)
+        q8, qs = fa.quant_fp8(x[0], signs=signs)
+        k8, ks = fa.quant_fp8(x[1], signs=signs)
+        v8, vs = fa.quant_fp8(x[2])
+        o = torch.empty((B, 16, N, 128), device=device, dtype=torch.bfloat16)
+        lse = torch.empty((B, 16, N), device=device, dtype=torch.float32)
+        fn = lambda: fa.fwd_fp8(q8, k8, v8, qs, ks, vs, out=o, lse=lse)
+        fn()
+        ms = _time_launches(fn, 5, device, flush)
+        tf = gen.flops(B, 16, N, 128, False) / (ms * 1e-3) / 1e12
+        qfn = lambda: fa.quant_fp8(x[0], signs=signs)
+        qms = _time_launches(qfn, 5, device, flush)
+        qbytes = x[0].numel() * 5  # 4 B read + 1 B written per element
+        out[f"fp8_N{N}_d128"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                 "frac_of_fp8_peak": round(tf / fp8_peak, 3),
+                                 "quant_ms_per_tensor": round(qms, 4),
+                                 "quant_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1)}
+    out["fp8_peak_note"] = "FP8 peak = measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"
+    return out
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------- CPU oracle timing -----
+def time_oracle(B, H, N, d, causal, budget_s: float, max_heads: int | None = None):
+    """Time the fp64 oracle as it stands on a bounded sample of the workload:
+    the first h heads (all rows), h chosen from a one-head calibration so the
+    run takes about `budget_s`.  Returns (TFLOPS, seconds, sample text, threads)."""
+    import numpy as np
+    import oracle
+
+    threads = oracle.max_threads()
+    shape = (1, 1, N, d)
+    q, k, v = gen.qkv_normal(shape, 99)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+    t1 = time.perf_counter() - t0
+    heads = max(1, min(B * H, int(budget_s / max(t1, 1e-6))))
+    if max_heads:
+        heads = min(heads, max_heads)
+    q, k, v = gen.qkv_normal((1, heads, N, d), 98)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+    el = time.perf_counter() - t0
+    fl = gen.flops(1, heads, N, d, causal)
+    return fl / el / 1e12, el, f"{heads} of {B * H} heads, all {N} rows each, fp64", threads
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as it stands: each step is a bounded sample (one head
+    of the workload, all rows).  Rank 0 only."""
+    import oracle
+
+    if rank != 0:
+        return
+    B, H, N, d, causal = args.B, args.H, args.N, args.d, args.causal
+    threads = oracle.max_threads()
+    q, k, v = gen.qkv_normal((1, 1, N, d), 97)
+    for _ in range(args.warmup):
+        oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+    el = time.perf_counter() - t0
+    fl = gen.flops(1, 1, N, d, causal) * args.steps
+    val = fl / el / 1e12
+    sample = f"one head of {B * H} (all {N} rows) per step, fp64 C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(args),
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(args):
+    return {"workload": f"{args.workload}: B={args.B} H={args.H} N={args.N} d={args.d} bf16 "
+                        f"{'causal' if args.causal else 'non-causal'} scale=1/sqrt(d)",
+            "B": args.B, "H": args.H, "N": args.N, "d": args.d, "causal": bool(args.causal),
+            "l2": "flushed before every timed step (512 MB write, outside the timed events)",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mid", choices=["mid", "sweep4k", "sweep16k", "long"])
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    shapes = {"mid": (4, 16, 2048, 128), "sweep4k": (4, 16, 4096, 128), "sweep16k": (1, 16, 16384, 128),
+              "long": (1, 16, 65536, 128)}
+    args.B, args.H, args.N, args.d = shapes[args.workload]
+    if args.workload == "long":
+        args.causal = True
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    res = run_ours(args, rank, world, device)
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        tflops = res["flops"] * world / (res["total_ms"] * 1e-3 / args.steps) / 1e12
+        achieved = res["flops"] / (res["launch_ms"] * 1e-3) / 1e12
+        e2e_tflops = res["flops"] * world / (res["e2e_ms"] * 1e-3) / 1e12
+        cpu_tf, cpu_s, cpu_sample, cpu_threads = time_oracle(args.B, args.H, args.N, args.d, args.causal,
+                                                              args.cpu_budget)
+        traffic = load_traffic(args.workload + ("_causal" if args.causal else ""))
+        line = {
+            "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["total_ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config(args),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst (cuBLAS GEMM)",
+                         "kernel": "attn_fwd_kernel<bf16,128,non-causal>",
+                         "algorithmic_flops_per_launch": res["flops"]},
+            "cpu_baseline": {"value": cpu_tf, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
+                             "sample": cpu_sample, "seconds": round(cpu_s, 2)},
+            "e2e": {"value": e2e_tflops, "unit": "TFLOPS", "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": args.steps,
+            "clocks": res["clocks"],
+            "extra": res["extra"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

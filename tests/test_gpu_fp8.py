@@ -1,0 +1,116 @@
+"""FP8 E4M3 path on the GPU against the oracle, through the C ABI.
+
+* fa_quant_fp8 must reproduce the oracle's quantiser bit for bit (codes and
+  descales), with and without the Hadamard rotation, per block and per tensor.
+* fa_fwd_fp8 is fed codes made by the ORACLE quantiser (never the GPU's) and
+  compared (a) with the oracle on the dequantised inputs -- LSE to 1e-3, O
+  RMSE to 3e-2 (P is rounded to E4M3 in the kernel) -- and (b) with the
+  oracle on the unquantised fp32 inputs: O RMSE <= 3e-2.
+* Block scales + Hadamard must give a lower O RMSE than a per-tensor scale on
+  inputs with rare large outliers ("FlashAttention-3: async pipelines on
+  Hopper", section "why FP8 numeric tests must match the model's
+  distribution").
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle
+from gpu_util import FP8_O_RMSE
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_09_gb300 as fa
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+    return fa
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [1, 127, 300, 1024])
+@pytest.mark.parametrize("rot", [False, True])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quant_bit_exact(fa, d, N, rot, per_tensor):
+    x = gen.outliers((2, 3, N, d), 50 + N + d)
+    signs = gen.hadamard_signs(d, 4) if rot else None
+    codes_ref, ds_ref = oracle.quant_e4m3(x, signs=signs, per_tensor=per_tensor)
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs, per_tensor=per_tensor)
+    fa.check_device_error()
+    codes = codes.cpu().numpy()
+    ds = ds.cpu().numpy()
+    mism = int((codes != codes_ref).sum())
+    assert mism == 0, f"{mism} E4M3 codes differ from the oracle quantiser"
+    assert np.array_equal(ds.view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
+
+
+def test_quant_zero_block(fa):
+    x = np.zeros((1, 1, 200, 128), dtype=np.float32)
+    x[0, 0, 150, 3] = 2.0  # second block non-zero, first all zero
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda())
+    codes_ref, ds_ref = oracle.quant_e4m3(x)
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+    assert np.array_equal(ds.cpu().numpy(), ds_ref)
+    assert ds_ref[0, 0, 0] == 1.0 and codes_ref[0, 0, 150, 3] == 0x7E
+
+
+def _fp8_case(fa, B, H, N, d, causal, rot, per_tensor, seed, rows=None, sigma=10.0):
+    q, k, v = gen.qkv_outliers((B, H, N, d), seed, sigma=sigma)
+    signs = gen.hadamard_signs(d, 4) if rot else None
+    qc, qs = oracle.quant_e4m3(q, signs=signs, per_tensor=per_tensor)
+    kc, ks = oracle.quant_e4m3(k, signs=signs, per_tensor=per_tensor)
+    vc, vs = oracle.quant_e4m3(v, signs=None, per_tensor=per_tensor)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd_fp8(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=causal, scale=scale)
+    fa.check_device_error()
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    # (a) oracle on the dequantised inputs (same rotated coordinates)
+    qd, kd, vd = oracle.dequant_e4m3(qc, qs), oracle.dequant_e4m3(kc, ks), oracle.dequant_e4m3(vc, vs)
+    o_dq, l_dq = oracle.attn_fwd(qd, kd, vd, causal=causal, scale=scale, rows=rows)
+    # (b) oracle on the unquantised fp32 inputs
+    o_ex, l_ex = oracle.attn_fwd(q, k, v, causal=causal, scale=scale, rows=rows)
+    rmse = lambda a, b: float(math.sqrt(((a - b) ** 2).mean()))
+    return dict(rmse_dq=rmse(o, o_dq), lse_dq=float(np.abs(lse - l_dq).max()),
+                rmse_exact=rmse(o, o_ex), lse_exact=float(np.abs(lse - l_ex).max()),
+                finite=bool(np.isfinite(o).all() and np.isfinite(lse).all()))
+
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("N", [1, 130, 640])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_fp8_small(fa, d, N, causal):
+    e = _fp8_case(fa, 2, 2, N, d, causal, rot=True, per_tensor=False, seed=300 + N + d)
+    assert e["finite"]
+    assert e["lse_dq"] <= 1e-3, e
+    assert e["rmse_dq"] <= FP8_O_RMSE, e
+    assert e["rmse_exact"] <= FP8_O_RMSE, e
+
+
+@pytest.mark.parametrize("N", gen.FP8_N)
+def test_fwd_fp8_config_sampled(fa, N):
+    # the FP8 workload: B = 16384/N, H = 16, d = 128, non-causal, outliers
+    B = gen.TOTAL_TOKENS // N
+    rows = gen.sample_rows(N, 32, N)
+    e = _fp8_case(fa, B, 16, N, 128, False, rot=True, per_tensor=False, seed=3, rows=rows)
+    assert e["finite"]
+    assert e["lse_dq"] <= 1e-3, e
+    assert e["rmse_exact"] <= FP8_O_RMSE, e
+
+
+def test_block_hadamard_beats_per_tensor(fa):
+    B, H, N, d = 2, 4, 1024, 128
+    rows = gen.sample_rows(N, 96, 7)
+    res = {}
+    for name, rot, pt in (("per_tensor", False, True), ("block", False, False), ("block_hadamard", True, False)):
+        res[name] = _fp8_case(fa, B, H, N, d, False, rot=rot, per_tensor=pt, seed=3, rows=rows)
+    assert res["block_hadamard"]["rmse_exact"] < res["per_tensor"]["rmse_exact"], res
+    assert res["block"]["rmse_exact"] <= res["per_tensor"]["rmse_exact"] * 1.05, res
