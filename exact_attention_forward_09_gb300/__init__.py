@@ -17,11 +17,14 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["fwd", "fwd_fp8", "quant_fp8", "check_device_error", "lib", "FaError",
-           "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-           "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS"]
+__all__ = ["fwd", "fwd_fp8", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
+           "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+           "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
+           "QUANT_NOALLOC_MAX_BLOCKS"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_ERR_SCRATCH_LIMIT = 5
+QUANT_NOALLOC_MAX_BLOCKS = 65536
 FA_DTYPE_BF16, FA_DTYPE_FP16 = 0, 1
 FP8_BLOCK_ROWS = 128
 
@@ -49,6 +52,8 @@ def _lib():
         lib.fa_fwd_fp8.restype = i32
         lib.fa_quant_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp]
         lib.fa_quant_fp8.restype = i32
+        lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
+        lib.fa_quant_fp8_per_tensor_noalloc.restype = i32
         lib.fa_status_string.argtypes = [i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_check_device_error.argtypes = [vp]
@@ -159,6 +164,35 @@ def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: 
     _check(st, "fa_quant_fp8")
     del keep
     return x8, ds
+
+
+def quant_fp8_per_tensor_noalloc(x: torch.Tensor, signs=None, x8: torch.Tensor | None = None,
+                                 descale: torch.Tensor | None = None):
+    """Per-tensor FP8 quantisation through ``fa_quant_fp8_per_tensor_noalloc``:
+    the library uses its own static device scratch, so the call itself needs
+    no allocation (pass ``x8`` and ``descale`` to avoid torch allocating the
+    outputs too).  Same result as ``quant_fp8(x, signs, per_tensor=True)``.
+    Calls that overlap on the GPU share the scratch and race."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 \
+            or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 [B, H, N, d] CUDA tensor")
+    B, H, N, d = x.shape
+    nblk = (N + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS
+    if x8 is None:
+        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    if descale is None:
+        descale = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    keep = None
+    sp = None
+    if signs is not None:
+        keep = (ctypes.c_int8 * d)(*[int(s) for s in (signs.tolist() if hasattr(signs, "tolist") else signs)])
+        sp = ctypes.cast(keep, ctypes.c_void_p)
+    with torch.cuda.device(x.device):
+        st = _lib().fa_quant_fp8_per_tensor_noalloc(x.data_ptr(), x8.data_ptr(), descale.data_ptr(),
+                                                    B, H, N, d, sp, _stream(x))
+    _check(st, "fa_quant_fp8_per_tensor_noalloc")
+    del keep
+    return x8, descale
 
 
 def check_device_error(device=None):

@@ -233,6 +233,8 @@ const char* fa_status_string(fa_status status) {
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dimension or device (needs sm_103)";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel pipeline wait ran out of time";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "FA_ERR_SCRATCH_LIMIT: B*H*ceil(N/128) exceeds FA_QUANT_NOALLOC_MAX_BLOCKS (static scratch)";
   }
   return "FA_ERR_UNKNOWN";
 }

@@ -58,6 +58,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 // MODE 0: per-block scale.  MODE 1: per-tensor amax into *amax_ws (atomic).
 // MODE 2: per-tensor encode with the amax in *amax_ws.
+// MODE 3: per-block amax stored to amax_ws[bh * nblk + blk] (no atomics).
 template <int D, int MODE>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
                                                          float* __restrict__ descale, int N, int nblk,
@@ -135,6 +136,9 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
   if constexpr (MODE == 1) {
     if (threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(amax_ws), __float_as_int(amax));
     return;
+  } else if constexpr (MODE == 3) {
+    if (threadIdx.x == 0) amax_ws[(size_t)bh * nblk + blk] = amax;
+    return;
   } else {
     const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
     for (int r = warp; r < nrows; r += 8) {
@@ -182,6 +186,48 @@ static cudaError_t launch_quant_d(const QuantLaunch& L) {
   quant_e4m3_kernel<D, 2><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
                                                        L.amax_ws);
   return cudaGetLastError();
+}
+
+// Maximum of n partial maxima -> *out (one CTA).
+__global__ void __launch_bounds__(1024) reduce_max_kernel(const float* __restrict__ part, int n,
+                                                          float* __restrict__ out) {
+  __shared__ float red[32];
+  float a = 0.0f;
+  for (int i = threadIdx.x; i < n; i += 1024) a = fmaxf(a, part[i]);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    a = red[threadIdx.x];
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+    if (threadIdx.x == 0) *out = a;
+  }
+}
+
+template <int D>
+static cudaError_t launch_quant_partials_d(const QuantLaunch& L, float* partials, float* amax_out) {
+  const dim3 grid(L.nblk, L.BH, 1);
+  quant_e4m3_kernel<D, 3><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
+                                                       partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  reduce_max_kernel<<<1, 1024, 0, L.stream>>>(partials, L.BH * L.nblk, amax_out);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quant_e4m3_kernel<D, 2><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
+                                                       amax_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partials, float* amax_out) {
+  switch (L.d) {
+    case 64: return launch_quant_partials_d<64>(L, partials, amax_out);
+    case 128: return launch_quant_partials_d<128>(L, partials, amax_out);
+    case 256: return launch_quant_partials_d<256>(L, partials, amax_out);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_quant(const QuantLaunch& L) {

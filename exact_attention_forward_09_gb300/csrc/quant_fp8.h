@@ -26,4 +26,9 @@ struct QuantLaunch {
 
 cudaError_t launch_quant(const QuantLaunch& L);
 
+// Per-tensor mode with caller-provided scratch: per-block maxima go to
+// partials[BH * nblk], their maximum to *amax_out, then the encode pass runs.
+// Every partial is written before it is read, so nothing needs clearing.
+cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partials, float* amax_out);
+
 }  // namespace fa

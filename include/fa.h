@@ -48,7 +48,8 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, non-finite scale, bad dtype */
     FA_ERR_UNSUPPORTED = 2,   /* head dimension or device not supported                            */
     FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or kernel launch failed                 */
-    FA_ERR_TIMEOUT = 4        /* a kernel's pipeline wait ran out of time (see fa_check_device_error) */
+    FA_ERR_TIMEOUT = 4,       /* a kernel's pipeline wait ran out of time (see fa_check_device_error) */
+    FA_ERR_SCRATCH_LIMIT = 5  /* problem larger than the library's static scratch (no-allocation entry point) */
 } fa_status;
 
 typedef enum {
@@ -126,6 +127,36 @@ fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
                        int64_t B, int64_t H, int64_t N, int64_t d,
                        const int8_t* hadamard_signs, int per_tensor, float* workspace,
                        cudaStream_t stream);
+
+/*
+ * fa_quant_fp8_per_tensor_noalloc -- the per-tensor mode of fa_quant_fp8
+ * (per_tensor = 1) for callers that cannot allocate device memory.  The
+ * pages have no counterpart; it exists for the library's users.
+ *
+ * fa_quant_fp8 needs one float of device scratch from the caller in
+ * per-tensor mode.  Callers that cannot allocate -- code running under a
+ * framework that owns every device buffer, plug-ins whose host forbids
+ * cudaMalloc (which may also synchronise the device), runtimes with a fixed
+ * memory budget -- use this entry point instead: it takes the same inputs
+ * and outputs but keeps its scratch in a device array compiled into the
+ * library (about 256 KiB, held by every GPU that loads the library until
+ * the process exits).  It calls no allocator.
+ *   x, x8, descale, B, H, N, d, hadamard_signs: as for fa_quant_fp8; the
+ *   output equals fa_quant_fp8 with per_tensor = 1 bit for bit.
+ *   Limit: B * H * ceil(N / 128) <= FA_QUANT_NOALLOC_MAX_BLOCKS, else
+ *   FA_ERR_SCRATCH_LIMIT and nothing is launched.
+ *   The first call on each device looks up the scratch array's device
+ *   address (with that device current); make that first call before any
+ *   stream capture.
+ *   All calls share the one scratch array and it keeps the last call's
+ *   contents (each call writes every entry it reads, so nothing needs
+ *   clearing): calls that overlap on the GPU -- other streams, other host
+ *   threads on the same device -- race and can produce wrong scales.
+ */
+#define FA_QUANT_NOALLOC_MAX_BLOCKS 65536
+fa_status fa_quant_fp8_per_tensor_noalloc(const float* x, void* x8, float* descale,
+                                          int64_t B, int64_t H, int64_t N, int64_t d,
+                                          const int8_t* hadamard_signs, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status status);
