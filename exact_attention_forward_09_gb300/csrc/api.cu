@@ -96,8 +96,10 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  // index ranges used by the kernels: grid.x = B*H, grid.y = ceil(N / 256)
-  if (B * H > 0x7fffffffLL || N > (int64_t)65535 * 256 || B * H * N > ((int64_t)1 << 40)) return FA_ERR_UNSUPPORTED;
+  // index ranges used by the kernels: a 1-D grid of B*H*ceil(N/256) blocks
+  // (at most B*H*ceil(N/128) for one Q tile per block) and int row indices
+  if (N > 0x7fffffffLL - 256 || B * H > 0x7fffffffLL || B * H * ((N + 127) / 128) > 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 

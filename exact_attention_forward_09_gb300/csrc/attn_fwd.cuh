@@ -152,9 +152,21 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
   const int N = prm.N;
-  const int group = (CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.y);  // heaviest first when causal
+  // 1-D grid.  Non-causal: the Q-tile groups of one head are adjacent, so
+  // their K/V tiles are re-read from L2.  Causal: group-major with the
+  // heaviest groups (most key tiles) first across all heads, so the tail of
+  // the grid holds the shortest blocks (longest-processing-time-first).
+  const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
+  int bh, group;
+  if constexpr (CAUSAL) {
+    const int BHn = (int)(gridDim.x / n_groups);
+    group = n_groups - 1 - (int)(blockIdx.x / BHn);
+    bh = (int)(blockIdx.x % BHn);
+  } else {
+    bh = (int)(blockIdx.x / n_groups);
+    group = (int)(blockIdx.x % n_groups);
+  }
   const int q_base = group * (C::NQT * kBM);
   const int nkv = (N + kBN - 1) / kBN;
 
@@ -466,15 +478,32 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           s[c] = masked ? mask_val : s[c];
         }
       }
+      // row max (min for a negative scale) as eight independent chains
       float mx;
-      if (!neg) {
-        mx = s[0];
+      {
+        float r8[8];
 #pragma unroll
-        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      } else {
-        mx = s[0];
+        for (int i = 0; i < 8; ++i) r8[i] = s[i];
+        if (!neg) {
 #pragma unroll
-        for (int c = 1; c < kBN; ++c) mx = fminf(mx, s[c]);
+          for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r8[i] = fmaxf(r8[i], s[c + i]);
+#pragma unroll
+          for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) r8[i] = fmaxf(r8[i], r8[i + w]);
+        } else {
+#pragma unroll
+          for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r8[i] = fminf(r8[i], s[c + i]);
+#pragma unroll
+          for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) r8[i] = fminf(r8[i], r8[i + w]);
+        }
+        mx = r8[0];
       }
       const float mx2 = mx * cj;
       float alpha = 1.0f;
@@ -509,45 +538,56 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s*cj - m), row sum, pack and write back over S
+      // P = 2^(s*cj - m) and the row sum (eight chains), packed and written
+      // back over S in halves so the first store overlaps the second half.
+      // Masked tiles (causal diagonal, ragged tail) zero the masked p
+      // explicitly; every other tile takes the branch-free loop.
       const float nm = -m_run;
-      float lsum = 0.0f;
-      if (need_mask) {
+      float ls[8];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const float p = ex2(fmaf(s[c], cj, nm));
-          s[c] = (s[c] == mask_val) ? 0.0f : p;
-          lsum += s[c];
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] = ex2(fmaf(s[c], cj, nm));
-          lsum += s[c];
-        }
-      }
-      l_run += lsum;
-      {
-        uint32_t u[32];
+      for (int i = 0; i < 8; ++i) ls[i] = 0.0f;
+      auto p_at = [&](int c, bool masked_tile) -> float {
+        const float p = ex2(fmaf(s[c], cj, nm));
+        return (masked_tile && s[c] == mask_val) ? 0.0f : p;
+      };
+      auto emit = [&](bool masked_tile) {
         if constexpr (ELEM == kE4M3) {
+          uint32_t u[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            u[i] = pack_e4m3x4(s[4 * i] * pv_fac, s[4 * i + 1] * pv_fac, s[4 * i + 2] * pv_fac,
-                               s[4 * i + 3] * pv_fac);
+          for (int i = 0; i < 32; ++i) {
+            float p4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              p4[e] = p_at(4 * i + e, masked_tile);
+              ls[(4 * i + e) & 7] += p4[e];
+            }
+            u[i] = pack_e4m3x4(p4[0] * pv_fac, p4[1] * pv_fac, p4[2] * pv_fac, p4[3] * pv_fac);
+          }
           tmem_st32(s_addr, u);
         } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            uint32_t u[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float a = s[h * 64 + 2 * i], b = s[h * 64 + 2 * i + 1];
+              const int c = h * 64 + 2 * i;
+              const float a = p_at(c, masked_tile), b = p_at(c + 1, masked_tile);
+              ls[(2 * i) & 7] += a;
+              ls[(2 * i + 1) & 7] += b;
               u[i] = (ELEM == kBF16) ? pack_bf16x2(a, b) : pack_f16x2(a, b);
             }
             tmem_st32(s_addr + h * 32, u);
           }
         }
-        tmem_wait_st();
-      }
+      };
+      if (need_mask) emit(true);
+      else emit(false);
+#pragma unroll
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) ls[i] += ls[i + w];
+      l_run += ls[0];
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[buf]);
     }
@@ -618,7 +658,7 @@ cudaError_t launch_attn(const AttnLaunch& L) {
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   const int groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  dim3 grid(L.BH, groups, 1);
+  dim3 grid((unsigned)(L.BH * groups), 1, 1);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.prm);
   return cudaGetLastError();
 }
