@@ -478,32 +478,27 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           s[c] = masked ? mask_val : s[c];
         }
       }
-      // row max (min for a negative scale) as eight independent chains
+      // row max (min for a negative scale): eight chains of 3-input max
       float mx;
       {
         float r8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) r8[i] = s[i];
         if (!neg) {
 #pragma unroll
-          for (int c = 8; c < kBN; c += 8)
+          for (int i = 0; i < 8; ++i) r8[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r8[i] = fmaxf(r8[i], s[c + i]);
+          for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-          for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) r8[i] = fmaxf(r8[i], r8[i + w]);
+            for (int i = 0; i < 8; ++i) r8[i] = max3f(r8[i], s[c + i], s[c + 8 + i]);
+          mx = max3f(max3f(r8[0], r8[1], r8[2]), max3f(r8[3], r8[4], r8[5]), fmaxf(r8[6], r8[7]));
         } else {
 #pragma unroll
-          for (int c = 8; c < kBN; c += 8)
+          for (int i = 0; i < 8; ++i) r8[i] = fminf(s[i], s[8 + i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r8[i] = fminf(r8[i], s[c + i]);
+          for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-          for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) r8[i] = fminf(r8[i], r8[i + w]);
+            for (int i = 0; i < 8; ++i) r8[i] = min3f(r8[i], s[c + i], s[c + 8 + i]);
+          mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
         }
-        mx = r8[0];
       }
       const float mx2 = mx * cj;
       float alpha = 1.0f;
@@ -538,55 +533,58 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s*cj - m) and the row sum (eight chains), packed and written
-      // back over S in halves so the first store overlaps the second half.
-      // Masked tiles (causal diagonal, ragged tail) zero the masked p
-      // explicitly; every other tile takes the branch-free loop.
-      const float nm = -m_run;
-      float ls[8];
+      // P = 2^(s*cj - m) and the row sum (four packed pairs of chains),
+      // packed and written back over S a quarter at a time, so the stores
+      // overlap the rest and few registers are live at once.  Masked tiles
+      // (causal diagonal, ragged tail) zero the masked p explicitly; every
+      // other tile takes the select-free loop.
+      const float2 cj2 = make_float2(cj, cj);
+      const float2 nm2 = make_float2(-m_run, -m_run);
+      float2 acc[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.0f;
-      auto p_at = [&](int c, bool masked_tile) -> float {
-        const float p = ex2(fmaf(s[c], cj, nm));
-        return (masked_tile && s[c] == mask_val) ? 0.0f : p;
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+      auto p_pair = [&](int c, bool masked_tile) -> float2 {
+        const float2 x = fma2(make_float2(s[c], s[c + 1]), cj2, nm2);
+        float2 p = make_float2(ex2(x.x), ex2(x.y));
+        if (masked_tile) {
+          p.x = (s[c] == mask_val) ? 0.0f : p.x;
+          p.y = (s[c + 1] == mask_val) ? 0.0f : p.y;
+        }
+        return p;
       };
       auto emit = [&](bool masked_tile) {
-        if constexpr (ELEM == kE4M3) {
-          uint32_t u[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float p4[4];
+        for (int q = 0; q < 4; ++q) {
+          if constexpr (ELEM == kE4M3) {
+            uint32_t u[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              p4[e] = p_at(4 * i + e, masked_tile);
-              ls[(4 * i + e) & 7] += p4[e];
+            for (int i = 0; i < 8; ++i) {
+              const int c = q * 32 + 4 * i;
+              const float2 a = p_pair(c, masked_tile), b = p_pair(c + 2, masked_tile);
+              acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
+              acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
+              u[i] = pack_e4m3x4(a.x * pv_fac, a.y * pv_fac, b.x * pv_fac, b.y * pv_fac);
             }
-            u[i] = pack_e4m3x4(p4[0] * pv_fac, p4[1] * pv_fac, p4[2] * pv_fac, p4[3] * pv_fac);
-          }
-          tmem_st32(s_addr, u);
-        } else {
+            tmem_st8(s_addr + q * 8, u);
+          } else {
+            uint32_t u[16];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t u[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c = h * 64 + 2 * i;
-              const float a = p_at(c, masked_tile), b = p_at(c + 1, masked_tile);
-              ls[(2 * i) & 7] += a;
-              ls[(2 * i + 1) & 7] += b;
-              u[i] = (ELEM == kBF16) ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+            for (int i = 0; i < 16; ++i) {
+              const int c = q * 32 + 2 * i;
+              const float2 a = p_pair(c, masked_tile);
+              acc[i & 3] = add2(acc[i & 3], a);
+              u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
             }
-            tmem_st32(s_addr + h * 32, u);
+            tmem_st16(s_addr + q * 16, u);
           }
         }
       };
       if (need_mask) emit(true);
       else emit(false);
-#pragma unroll
-      for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) ls[i] += ls[i + w];
-      l_run += ls[0];
+      {
+        const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+        l_run += t.x + t.y;
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[buf]);
