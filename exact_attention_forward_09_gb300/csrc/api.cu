@@ -148,6 +148,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   L.prm.nblk = (int)((N + 127) / 128);
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   L.BH = (int)(B * H);
+  L.prm.BH = L.BH;
   L.stream = stream;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
 }
@@ -182,6 +183,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
   L.prm.nblk = (int)((N + 127) / 128);
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   L.BH = (int)(B * H);
+  L.prm.BH = L.BH;
   L.stream = stream;
   return dispatch<fa::kE4M3>(L, d, causal);
 }

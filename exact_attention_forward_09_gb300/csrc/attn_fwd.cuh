@@ -41,6 +41,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace fa {
@@ -81,7 +83,18 @@ struct AttnCfg {
   static constexpr int SOFTMAX_WARPS = 4 * NQT;
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
   static constexpr int LOAD_WARP = SOFTMAX_WARPS + 1;
-  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // Two Q tiles: a third, control warpgroup (MMA warp, load warp, two idle
+  // warps) so that registers can move between whole warpgroups: launched
+  // at LAUNCH_REGS, the control warpgroup drops to CTRL_REGS and the softmax
+  // warpgroups rise to SOFTMAX_REGS (their sum stays within the launch
+  // total).  One Q tile: 6 warps, no reallocation needed.
+  static constexpr bool REALLOC = (NQT == 2);
+  static constexpr int THREADS = REALLOC ? 32 * (SOFTMAX_WARPS + 4) : 32 * (SOFTMAX_WARPS + 2);
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int CTRL_REGS = 72;
+  static constexpr int SOFTMAX_REGS = 216;
+  static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
+                "register split exceeds the launch budget");
   // lazy-rescale threshold (log2 units): P <= 2^TAU.  FP8 P must stay far
   // below the E4M3 maximum, so FP8 rescales whenever the max moves.
   static constexpr float TAU = (ELEM == kE4M3) ? 0.0f : 8.0f;
@@ -106,6 +119,7 @@ struct AttnParams {
   const float* v_ds;
   int* err;             // device error word
   int N;
+  int BH;               // batch x heads
   int nblk;             // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
 };
@@ -114,6 +128,7 @@ struct AttnParams {
 template <int NS>
 struct Bars {
   uint64_t q_full;
+  uint64_t q_empty;
   uint64_t full[NS];
   uint64_t empty[NS];
   uint64_t s_full[2];
@@ -121,6 +136,11 @@ struct Bars {
   uint64_t o_ready[2];
   uint64_t o_full[2];
   uint64_t drain;
+  uint64_t clc_bar;        // response of the work-stealing request
+  uint64_t unit_full[2];   // queue of next-unit ids (load warp -> others)
+  uint64_t unit_empty[2];
+  alignas(16) uint32_t clc_resp[4];
+  int unit_q[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -153,36 +173,50 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = prm.N;
-  // 1-D grid.  Non-causal: the Q-tile groups of one head are adjacent, so
-  // their K/V tiles are re-read from L2.  Causal: group-major with the
-  // heaviest groups (most key tiles) first across all heads, so the tail of
-  // the grid holds the shortest blocks (longest-processing-time-first).
-  const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  int bh, group;
-  if constexpr (CAUSAL) {
-    const int BHn = (int)(gridDim.x / n_groups);
-    group = n_groups - 1 - (int)(blockIdx.x / BHn);
-    bh = (int)(blockIdx.x % BHn);
-  } else {
-    bh = (int)(blockIdx.x / n_groups);
-    group = (int)(blockIdx.x % n_groups);
-  }
-  const int q_base = group * (C::NQT * kBM);
   const int nkv = (N + kBN - 1) / kBN;
+  const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
+  const int U = prm.BH * n_groups;  // work units: (head, group of NQT Q tiles)
+  const int G = (int)gridDim.x;
 
-  // per-tile activity and key-tile counts
-  int Jt[2];
-  bool active[2];
+  // Work units are launched one CTA each, in this order: non-causal,
+  // head-major (the Q-tile groups of a head are adjacent, their K/V re-read
+  // from L2); causal, group-major with the heaviest groups (most key tiles)
+  // first (longest-processing-time-first).  A CTA that is about to finish
+  // its unit takes over the next not-yet-started CTA's unit through cluster
+  // launch control, so units flow to whichever SM frees up first and the
+  // next unit's loads overlap the current unit's tail.  The load warp makes
+  // the request and passes the unit id to the other roles through a
+  // two-slot queue in shared memory.
+  (void)G;
+  struct Unit {
+    int bh, q_base, J;
+    int Jt[2];
+    bool active[2];
+  };
+  auto decode = [&](int u) -> Unit {
+    Unit w;
+    int group;
+    if constexpr (CAUSAL) {
+      group = n_groups - 1 - u / prm.BH;
+      w.bh = u % prm.BH;
+    } else {
+      w.bh = u / n_groups;
+      group = u % n_groups;
+    }
+    w.q_base = group * (C::NQT * kBM);
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int q0 = q_base + t * kBM;
-    active[t] = (t < C::NQT) && (q0 < N);
-    Jt[t] = active[t] ? kv_tiles_for<CAUSAL>(q0, nkv) : 0;
-  }
-  const int J = Jt[0] > Jt[1] ? Jt[0] : Jt[1];
+    for (int t = 0; t < 2; ++t) {
+      const int q0 = w.q_base + t * kBM;
+      w.active[t] = (t < C::NQT) && (q0 < N);
+      w.Jt[t] = w.active[t] ? kv_tiles_for<CAUSAL>(q0, nkv) : 0;
+    }
+    w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
+    return w;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
@@ -194,6 +228,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       mbar_init(&bars->o_full[t], 1);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->clc_bar, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->unit_full[q], 1);
+      mbar_init(&bars->unit_empty[q], 1 + C::SOFTMAX_WARPS);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -206,6 +245,19 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // The id of this CTA's unit number r >= 1 from the queue (-1: no more),
+  // then release the slot.  `arrive` is done by one lane per warp.
+  auto next_unit = [&](int r, bool arrive) -> int {
+    const int slot = r & 1;
+    if (!mbar_wait(&bars->unit_full[slot], (uint32_t)(((r - 1) >> 1) & 1), abort_flag, prm.err)) return -2;
+    const int v = *reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    if (arrive) mbar_arrive(&bars->unit_empty[slot]);
+    return v;
+  };
+
+  if (warp >= C::SOFTMAX_WARPS) {
+    // control warpgroup: give registers to the softmax warpgroups
+    if constexpr (C::REALLOC) regs_dec<C::CTRL_REGS>();
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ load --
     if (lane == 0) {
@@ -214,56 +266,86 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
-      uint32_t qbytes = 0;
-      for (int t = 0; t < C::NQT; ++t) qbytes += active[t] ? (uint32_t)(kBM * C::ROW_BYTES) : 0u;
-      mbar_arrive_expect_tx(&bars->q_full, qbytes);
-      for (int t = 0; t < C::NQT; ++t) {
-        if (!active[t]) continue;
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d_hint(smem + C::OFF_Q + (t * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, &bars->q_full,
-                           ch * C::CH_ELEMS, q_base + t * kBM, bh, pol_q);
-      }
-      int pos = 0;
+      int pos = 0;     // ring position (continues across units)
+      int k = 0;       // units loaded by this CTA
+      int n_req = 0;   // work-stealing requests made
+      bool more = true;
       bool ok = true;
-      // one K or V tile (SPT ring slots) into the ring
-      auto load_tile = [&](bool is_v, int j) {
-        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-        for (int sp = 0; sp < C::SPT && ok; ++sp, ++pos) {
-          const int slot = pos % C::NS;
-          const uint32_t ph = (uint32_t)((pos / C::NS) & 1);
-          if (!mbar_wait(&bars->empty[slot], ph ^ 1u, abort_flag, prm.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
-          for (int ch = 0; ch < C::SLOT_CH; ++ch)
-            tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,
-                             &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, bh, pol_kv);
+      int u = (int)blockIdx.x;
+      for (int r = 0; ok && u >= 0; ++r) {
+        const Unit w = decode(u);
+        // the Q buffer is free once the previous unit's last Q K^T finished
+        if (k > 0 && !mbar_wait(&bars->q_empty, (uint32_t)((k - 1) & 1), abort_flag, prm.err)) { ok = false; break; }
+        uint32_t qbytes = 0;
+        for (int t = 0; t < C::NQT; ++t) qbytes += w.active[t] ? (uint32_t)(kBM * C::ROW_BYTES) : 0u;
+        mbar_arrive_expect_tx(&bars->q_full, qbytes);
+        for (int t = 0; t < C::NQT; ++t) {
+          if (!w.active[t]) continue;
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d_hint(smem + C::OFF_Q + (t * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, &bars->q_full,
+                             ch * C::CH_ELEMS, w.q_base + t * kBM, w.bh, pol_q);
         }
-      };
-      if constexpr (C::NQT == 2) {
-        for (int j = 0; j < J && ok; ++j) {
-          load_tile(false, j);
-          load_tile(true, j);
+        // one K or V tile (SPT ring slots) into the ring
+        auto load_tile = [&](bool is_v, int j) {
+          const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+          for (int sp = 0; sp < C::SPT && ok; ++sp, ++pos) {
+            const int slot = pos % C::NS;
+            const uint32_t ph = (uint32_t)((pos / C::NS) & 1);
+            if (!mbar_wait(&bars->empty[slot], ph ^ 1u, abort_flag, prm.err)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
+            for (int ch = 0; ch < C::SLOT_CH; ++ch)
+              tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,
+                               &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, w.bh, pol_kv);
+          }
+        };
+        if constexpr (C::NQT == 2) {
+          for (int j = 0; j < w.J && ok; ++j) {
+            load_tile(false, j);
+            load_tile(true, j);
+          }
+        } else {
+          for (int j = 0; j < w.J && j < 2 && ok; ++j) load_tile(false, j);
+          for (int j = 0; j < w.J && ok; ++j) {
+            load_tile(true, j);
+            if (j + 2 < w.J) load_tile(false, j + 2);
+          }
         }
-      } else {
-        for (int j = 0; j < J && j < 2 && ok; ++j) load_tile(false, j);
-        for (int j = 0; j < J && ok; ++j) {
-          load_tile(true, j);
-          if (j + 2 < J) load_tile(false, j + 2);
+        ++k;
+        if (!ok) break;
+        // every load of this unit is issued: claim the next unit
+        int nu = -1;
+        if (more) {
+          mbar_arrive_expect_tx(&bars->clc_bar, 16);
+          clc_try_cancel(bars->clc_resp, &bars->clc_bar);
+          if (!mbar_wait(&bars->clc_bar, (uint32_t)(n_req & 1), abort_flag, prm.err)) { ok = false; break; }
+          ++n_req;
+          nu = clc_query_x(bars->clc_resp);
+          if (nu < 0 || nu >= U) { nu = -1; more = false; }
         }
+        // publish it as unit r+1 (slot reused once the others read unit r-1)
+        const int nr = r + 1, slot = nr & 1;
+        if (nr >= 3 && !mbar_wait(&bars->unit_empty[slot], (uint32_t)(((nr - 3) >> 1) & 1), abort_flag, prm.err)) {
+          ok = false;
+          break;
+        }
+        *reinterpret_cast<volatile int*>(&bars->unit_q[slot]) = nu;
+        mbar_arrive(&bars->unit_full[slot]);
+        u = nu;
       }
       // Never leave with copies in flight: wait (bounded) for the last fill
-      // of every slot that was used.
+      // of every slot that was used, and for the last Q tile.
       const int used = pos < C::NS ? pos : C::NS;
-      for (int k = 0; k < used; ++k) {
-        const int p_last = pos - 1 - k;
+      for (int i = 0; i < used; ++i) {
+        const int p_last = pos - 1 - i;
         const int slot = p_last % C::NS;
         const uint32_t ph = (uint32_t)((p_last / C::NS) & 1);
         uint64_t t0 = globaltimer();
         while (!mbar_try_wait(&bars->full[slot], ph) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
         }
       }
-      {
+      if (k > 0) {
         uint64_t t0 = globaltimer();
-        while (qbytes && !mbar_try_wait(&bars->q_full, 0) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
+        while (!mbar_try_wait(&bars->q_full, (uint32_t)((k - 1) & 1)) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
         }
       }
     }
@@ -273,8 +355,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     if (lane == 0) {
       const uint32_t q_s = smem_u32(smem + C::OFF_Q);
       const uint32_t ring_s = smem_u32(smem + C::OFF_RING);
-      int pos = 0;  // ring position of the next item to consume
-      bool ok = (J > 0) ? mbar_wait(&bars->q_full, 0, abort_flag, prm.err) : true;
+      int pos = 0;          // ring position of the next item to consume
+      int k = 0;            // units processed
+      int pc[2] = {0, 0};   // two Q tiles: P handshakes consumed per tile
+      int g = 0;            // one Q tile: S/P iterations so far (buffer = g & 1)
+      bool ok = true;
 
       // wait for a whole tile (SPT slots) at the current ring position
       auto wait_tile = [&](int p) -> bool {
@@ -322,82 +407,101 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
       };
 
-      if constexpr (C::NQT == 2) {
-        // prologue: S_t(0) for both tiles
-        if (ok && J > 0) {
+      int u = (int)blockIdx.x;
+      for (int r = 0; ok && u >= 0; ++r) {
+        const Unit w = decode(u);
+        ok = mbar_wait(&bars->q_full, (uint32_t)(k & 1), abort_flag, prm.err);
+        if (!ok) break;
+        tc_fence_after();
+        // the Q buffer is released after this unit's last Q K^T
+        int qk_left = w.Jt[0] + w.Jt[1];
+        auto qk_issued = [&]() {
+          if (--qk_left == 0) mma_commit(&bars->q_empty);
+        };
+        if constexpr (C::NQT == 2) {
+          // prologue: S_t(0) for both tiles
           ok = wait_tile(pos);
-          if (ok) {
-            for (int t = 0; t < 2; ++t)
-              if (Jt[t] > 0) {
-                issue_qk(t, t, pos);
-                mma_commit(&bars->s_full[t]);
-              }
-            release_tile(pos);
-          }
-          pos += C::SPT;
-        }
-        for (int j = 0; j < J && ok; ++j) {
-          const int pv_pos = pos;            // V_j
-          const int k_pos = pos + C::SPT;    // K_{j+1}
-          bool v_ready = false, k_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= Jt[t]) continue;
-            if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
-            ok = mbar_wait(&bars->p_full[t], (uint32_t)(j & 1), abort_flag, prm.err);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, t, pv_pos, j > 0);
-            if (j + 1 < Jt[t]) {
-              if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
-              issue_qk(t, t, k_pos);
+          if (!ok) break;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (w.Jt[t] > 0) {
+              issue_qk(t, t, pos);
               mma_commit(&bars->s_full[t]);
-            } else {
-              mma_commit(&bars->o_full[t]);
+              qk_issued();
+            }
+          release_tile(pos);
+          pos += C::SPT;
+          for (int j = 0; j < w.J && ok; ++j) {
+            const int pv_pos = pos;            // V_j
+            const int k_pos = pos + C::SPT;    // K_{j+1}
+            bool v_ready = false, k_ready = false;
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (j >= w.Jt[t]) continue;
+              if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
+              ok = mbar_wait(&bars->p_full[t], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
+              ++pc[t];
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, t, pv_pos, j > 0);
+              if (j + 1 < w.Jt[t]) {
+                if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
+                issue_qk(t, t, k_pos);
+                mma_commit(&bars->s_full[t]);
+                qk_issued();
+              } else {
+                mma_commit(&bars->o_full[t]);
+              }
+            }
+            if (!ok) break;
+            release_tile(pv_pos);
+            pos += C::SPT;
+            if (j + 1 < w.J) {
+              release_tile(k_pos);
+              pos += C::SPT;
             }
           }
-          if (!ok) break;
-          release_tile(pv_pos);
-          pos += C::SPT;
-          if (j + 1 < J) {
-            release_tile(k_pos);
-            pos += C::SPT;
-          }
-        }
-      } else {
-        // one Q tile, S double-buffered: S(0), S(1), then PV(j), S(j+2)
-        const int Jn = Jt[0];
-        int k_pos[2] = {0, 0};
-        for (int j = 0; j < 2 && j < Jn && ok; ++j) {
-          ok = wait_tile(pos);
-          if (!ok) break;
-          issue_qk(0, j, pos);
-          mma_commit(&bars->s_full[j]);
-          release_tile(pos);
-          k_pos[j] = pos;
-          pos += C::SPT;
-        }
-        for (int j = 0; j < Jn && ok; ++j) {
-          const int b = j & 1;
-          ok = wait_tile(pos);  // V_j
-          if (!ok) break;
-          ok = mbar_wait(&bars->p_full[b], (uint32_t)((j >> 1) & 1), abort_flag, prm.err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(0, b, pos, j > 0);
-          mma_commit(&bars->o_ready[b]);
-          release_tile(pos);
-          pos += C::SPT;
-          if (j + 2 < Jn) {
-            ok = wait_tile(pos);  // K_{j+2}
+        } else {
+          // one Q tile, S double-buffered: S(0), S(1), then PV(j), S(j+2);
+          // buffers alternate on the running iteration count g
+          const int Jn = w.Jt[0];
+          for (int j = 0; j < 2 && j < Jn && ok; ++j) {
+            ok = wait_tile(pos);
             if (!ok) break;
-            issue_qk(0, b, pos);
-            mma_commit(&bars->s_full[b]);
+            issue_qk(0, (g + j) & 1, pos);
+            mma_commit(&bars->s_full[(g + j) & 1]);
+            qk_issued();
             release_tile(pos);
             pos += C::SPT;
           }
+          for (int j = 0; j < Jn && ok; ++j) {
+            const int gj = g + j;
+            const int b = gj & 1;
+            ok = wait_tile(pos);  // V_j
+            if (!ok) break;
+            ok = mbar_wait(&bars->p_full[b], (uint32_t)((gj >> 1) & 1), abort_flag, prm.err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, b, pos, j > 0);
+            mma_commit(&bars->o_ready[b]);
+            release_tile(pos);
+            pos += C::SPT;
+            if (j + 2 < Jn) {
+              ok = wait_tile(pos);  // K_{j+2}
+              if (!ok) break;
+              issue_qk(0, b, pos);
+              mma_commit(&bars->s_full[b]);
+              qk_issued();
+              release_tile(pos);
+              pos += C::SPT;
+            }
+          }
+          if (ok) mma_commit(&bars->o_full[0]);
+          g += Jn;
         }
-        if (ok && Jn > 0) mma_commit(&bars->o_full[0]);
-        (void)k_pos;
+        ++k;
+        if (!ok) break;
+        u = next_unit(r + 1, true);
+        if (u == -2) ok = false;
       }
       // drain: every MMA issued by this thread has completed before TMEM is freed
       mma_commit(&bars->drain);
@@ -406,219 +510,243 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       }
     }
     __syncwarp();
+  }
+  // (any further warps of the control warpgroup have no role)
   } else {
     // --------------------------------------------------------- softmax --
+    if constexpr (C::REALLOC) regs_inc<C::SOFTMAX_REGS>();
     const int t = warp / 4;                 // Q tile of this warpgroup
     const int wq = warp % 4;                // TMEM lane quarter
-    const int r = wq * 32 + lane;           // row within the tile
-    const int q0 = q_base + t * kBM;
-    const int row = q0 + r;
+    const int r_in = wq * 32 + lane;        // row within the tile
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-    const int Jn = Jt[t];
     const bool neg = prm.scale_log2 < 0.0f;
-
-    float m_run = -INFINITY;  // reference maximum, log2 units
-    float l_run = 0.0f;
-    float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
-    int o_seen[2] = {0, 0};   // one-Q-tile mode: o_ready phases consumed per buffer
+    const float mask_val = neg ? INFINITY : -INFINITY;
+    int sc = 0;               // two Q tiles: S handshakes consumed (this tile)
+    int g = 0;                // one Q tile: running iteration count
+    int oc = 0;               // units finished by this tile (o_full phases)
+    int o_seen[2] = {0, 0};   // one Q tile: o_ready completions consumed per buffer
     bool ok = true;
-    const int bh_blk = bh * prm.nblk;
-    float qds = 1.0f, vmax = 1.0f;
-    if (ELEM == kE4M3 && Jn > 0) {
-      qds = prm.q_ds[bh_blk + q0 / kBM];
-      vmax = 0.0f;
-      for (int b = 0; b < prm.nblk; ++b) vmax = fmaxf(vmax, prm.v_ds[bh_blk + b]);
-      if (!(vmax > 0.0f)) vmax = 1.0f;
-      v_mult = vmax / C::P8_SCALE;
-    }
 
-    for (int j = 0; j < Jn && ok; ++j) {
-      const int buf = (C::NQT == 2) ? t : (j & 1);
-      const uint32_t ph = (C::NQT == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], ph, abort_flag, prm.err));
-      if (!ok) break;
-      tc_fence_after();
-      if constexpr (C::NQT == 1) {
-        // PV(j-2) completed before S(j) (issue order), so its o_ready phase
-        // is already done: consume it to keep the phase count in step.
-        if (j >= 2 && o_seen[buf] < ((j - 2) >> 1) + 1) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bars->o_ready[buf], (uint32_t)(o_seen[buf] & 1), abort_flag, prm.err));
-          o_seen[buf]++;
-          if (!ok) break;
-        }
-      }
-      const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
-      float s[kBN];
-      {
-        uint32_t u[32];
-#pragma unroll
-        for (int c4 = 0; c4 < kBN / 32; ++c4) {
-          tmem_ld32(s_addr + c4 * 32, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
-        }
-        tmem_wait_ld();
-      }
-      // scale of this tile (log2 units)
-      float cj = prm.scale_log2;
-      float pv_fac = 1.0f;
+    int un = (int)blockIdx.x;
+    for (int rr = 0; ok && un >= 0; ++rr) {
+      const Unit w = decode(un);
+      do {  // one unit (skipped when this tile lies beyond N)
+      if (!(t == 0 ? w.active[0] : w.active[1])) break;
+      const int bh = w.bh;
+      const int q0 = w.q_base + t * kBM;
+      const int row = q0 + r_in;
+      const int Jn = (t == 0) ? w.Jt[0] : w.Jt[1];
+
+      float m_run = -INFINITY;  // reference maximum, log2 units
+      float l_run = 0.0f;
+      float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
+      const int bh_blk = bh * prm.nblk;
+      float qds = 1.0f, vmax = 1.0f;
       if constexpr (ELEM == kE4M3) {
-        cj *= qds * prm.k_ds[bh_blk + j];
-        pv_fac = C::P8_SCALE * (prm.v_ds[bh_blk + j] / vmax);
+        qds = prm.q_ds[bh_blk + q0 / kBM];
+        vmax = 0.0f;
+        for (int b = 0; b < prm.nblk; ++b) vmax = fmaxf(vmax, prm.v_ds[bh_blk + b]);
+        if (!(vmax > 0.0f)) vmax = 1.0f;
+        v_mult = vmax / C::P8_SCALE;
       }
-      const int col0 = j * kBN;
-      const bool need_mask = (col0 + kBN > N) || (CAUSAL && col0 + kBN - 1 > q0);
-      const float mask_val = neg ? INFINITY : -INFINITY;
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int col = col0 + c;
-          const bool masked = (col >= N) || (CAUSAL && col > row);
-          s[c] = masked ? mask_val : s[c];
+      // one Q tile: consume o_ready completions up to (and including) the PV
+      // of global iteration x on buffer x & 1 (they complete in order)
+      auto consume_o = [&](int x) -> bool {
+        const int b = x & 1;
+        while (2 * o_seen[b] + b <= x) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&bars->o_ready[b], (uint32_t)(o_seen[b] & 1), abort_flag, prm.err)))
+            return false;
+          ++o_seen[b];
         }
-      }
-      // row max (min for a negative scale): eight chains of 3-input max
-      float mx;
-      {
-        float r8[8];
-        if (!neg) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) r8[i] = fmaxf(s[i], s[8 + i]);
-#pragma unroll
-          for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) r8[i] = max3f(r8[i], s[c + i], s[c + 8 + i]);
-          mx = max3f(max3f(r8[0], r8[1], r8[2]), max3f(r8[3], r8[4], r8[5]), fmaxf(r8[6], r8[7]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) r8[i] = fminf(s[i], s[8 + i]);
-#pragma unroll
-          for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) r8[i] = min3f(r8[i], s[c + i], s[c + 8 + i]);
-          mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
-        }
-      }
-      const float mx2 = mx * cj;
-      float alpha = 1.0f;
-      const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY);
-      if (move) {
-        alpha = ex2(m_run - mx2);  // 0 on the first tile
-        m_run = mx2;
-      }
-      l_run *= alpha;
-      // rescale O when any row of the warp moved (never on the first tile)
-      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        return true;
+      };
+
+      for (int j = 0; j < Jn && ok; ++j) {
+        const int gj = g + j;
+        const int buf = (C::NQT == 2) ? t : (gj & 1);
+        const uint32_t ph = (C::NQT == 2) ? (uint32_t)(sc & 1) : (uint32_t)((gj >> 1) & 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], ph, abort_flag, prm.err));
+        ++sc;
+        if (!ok) break;
+        tc_fence_after();
         if constexpr (C::NQT == 1) {
-          // O holds PV(j-1): wait for it
-          const int pb = (j - 1) & 1;
-          if (o_seen[pb] < ((j - 1) >> 1) + 1) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->o_ready[pb], (uint32_t)(o_seen[pb] & 1), abort_flag, prm.err));
-            o_seen[pb]++;
-            if (!ok) break;
-          }
-          tc_fence_after();
+          // PV(gj-2) was issued before S(gj), so it has completed: consume
+          // its o_ready phase to keep at most one pending per buffer
+          if (gj >= 2 && !consume_o(gj - 2)) { ok = false; break; }
         }
-        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
+        float s[kBN];
+        {
           uint32_t u[32];
-          tmem_ld32(o_addr + c0, u);
-          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(o_addr + c0, u);
+          for (int c4 = 0; c4 < kBN / 32; ++c4) {
+            tmem_ld32(s_addr + c4 * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
+          }
+          tmem_wait_ld();
+        }
+        // scale of this tile (log2 units)
+        float cj = prm.scale_log2;
+        float pv_fac = 1.0f;
+        if constexpr (ELEM == kE4M3) {
+          cj *= qds * prm.k_ds[bh_blk + j];
+          pv_fac = C::P8_SCALE * (prm.v_ds[bh_blk + j] / vmax);
+        }
+        const int col0 = j * kBN;
+        const bool need_mask = (col0 + kBN > N) || (CAUSAL && col0 + kBN - 1 > q0);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const int col = col0 + c;
+            const bool masked = (col >= N) || (CAUSAL && col > row);
+            s[c] = masked ? mask_val : s[c];
+          }
+        }
+        // row max (min for a negative scale): eight chains of 3-input max
+        float mx;
+        {
+          float r8[8];
+          if (!neg) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r8[i] = fmaxf(s[i], s[8 + i]);
+#pragma unroll
+            for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) r8[i] = max3f(r8[i], s[c + i], s[c + 8 + i]);
+            mx = max3f(max3f(r8[0], r8[1], r8[2]), max3f(r8[3], r8[4], r8[5]), fmaxf(r8[6], r8[7]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r8[i] = fminf(s[i], s[8 + i]);
+#pragma unroll
+            for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) r8[i] = min3f(r8[i], s[c + i], s[c + 8 + i]);
+            mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
+          }
+        }
+        const float mx2 = mx * cj;
+        float alpha = 1.0f;
+        const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY);
+        if (move) {
+          alpha = ex2(m_run - mx2);  // 0 on the first tile
+          m_run = mx2;
+        }
+        l_run *= alpha;
+        // rescale O when any row of the warp moved (never on the first tile)
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          if constexpr (C::NQT == 1) {
+            // O holds PV(gj-1): wait for it
+            if (!consume_o(gj - 1)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t u[32];
+            tmem_ld32(o_addr + c0, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(o_addr + c0, u);
+          }
+          tmem_wait_st();
+        }
+        // P = 2^(s*cj - m) and the row sum (four packed pairs of chains),
+        // packed and written back over S a quarter at a time, so the stores
+        // overlap the rest and few registers are live at once.  Masked tiles
+        // (causal diagonal, ragged tail) zero the masked p explicitly; every
+        // other tile takes the select-free loop.
+        const float2 cj2 = make_float2(cj, cj);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 acc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        auto p_pair = [&](int c, bool masked_tile) -> float2 {
+          const float2 x = fma2(make_float2(s[c], s[c + 1]), cj2, nm2);
+          float2 p = make_float2(ex2(x.x), ex2(x.y));
+          if (masked_tile) {
+            p.x = (s[c] == mask_val) ? 0.0f : p.x;
+            p.y = (s[c + 1] == mask_val) ? 0.0f : p.y;
+          }
+          return p;
+        };
+        auto emit = [&](bool masked_tile) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if constexpr (ELEM == kE4M3) {
+              uint32_t u[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int c = q * 32 + 4 * i;
+                const float2 a = p_pair(c, masked_tile), b = p_pair(c + 2, masked_tile);
+                acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
+                acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
+                u[i] = pack_e4m3x4(a.x * pv_fac, a.y * pv_fac, b.x * pv_fac, b.y * pv_fac);
+              }
+              tmem_st8(s_addr + q * 8, u);
+            } else {
+              uint32_t u[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int c = q * 32 + 2 * i;
+                const float2 a = p_pair(c, masked_tile);
+                acc[i & 3] = add2(acc[i & 3], a);
+                u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
+              }
+              tmem_st16(s_addr + q * 16, u);
+            }
+          }
+        };
+        if (need_mask) emit(true);
+        else emit(false);
+        {
+          const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+          l_run += t.x + t.y;
         }
         tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[buf]);
       }
-      // P = 2^(s*cj - m) and the row sum (four packed pairs of chains),
-      // packed and written back over S a quarter at a time, so the stores
-      // overlap the rest and few registers are live at once.  Masked tiles
-      // (causal diagonal, ragged tail) zero the masked p explicitly; every
-      // other tile takes the select-free loop.
-      const float2 cj2 = make_float2(cj, cj);
-      const float2 nm2 = make_float2(-m_run, -m_run);
-      float2 acc[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      auto p_pair = [&](int c, bool masked_tile) -> float2 {
-        const float2 x = fma2(make_float2(s[c], s[c + 1]), cj2, nm2);
-        float2 p = make_float2(ex2(x.x), ex2(x.y));
-        if (masked_tile) {
-          p.x = (s[c] == mask_val) ? 0.0f : p.x;
-          p.y = (s[c + 1] == mask_val) ? 0.0f : p.y;
-        }
-        return p;
-      };
-      auto emit = [&](bool masked_tile) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if constexpr (ELEM == kE4M3) {
-            uint32_t u[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int c = q * 32 + 4 * i;
-              const float2 a = p_pair(c, masked_tile), b = p_pair(c + 2, masked_tile);
-              acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
-              acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
-              u[i] = pack_e4m3x4(a.x * pv_fac, a.y * pv_fac, b.x * pv_fac, b.y * pv_fac);
-            }
-            tmem_st8(s_addr + q * 8, u);
-          } else {
-            uint32_t u[16];
+
+      // ---------------------------------------------------------- epilogue --
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], (uint32_t)(oc & 1), abort_flag, prm.err));
+        ++oc;
+        if (ok) {
+          tc_fence_after();
+          const float inv_l = (l_run > 0.0f) ? (1.0f / l_run) : 0.0f;
+          const float f = inv_l * v_mult;
+          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+          const bool store = row < N;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + (size_t)(store ? row : 0)) * D * 2;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t u[32];
+            tmem_ld32(o_addr + c0, u);
+            tmem_wait_ld();
+            uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int c = q * 32 + 2 * i;
-              const float2 a = p_pair(c, masked_tile);
-              acc[i & 3] = add2(acc[i & 3], a);
-              u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
+              const float a = __uint_as_float(u[2 * i]) * f, b = __uint_as_float(u[2 * i + 1]) * f;
+              pk[i] = (ELEM == kFP16) ? pack_f16x2(a, b) : pack_bf16x2(a, b);
             }
-            tmem_st16(s_addr + q * 16, u);
-          }
-        }
-      };
-      if (need_mask) emit(true);
-      else emit(false);
-      {
-        const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-        l_run += t.x + t.y;
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[buf]);
-    }
-
-    // ---------------------------------------------------------- epilogue --
-    if (ok && Jn > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], 0, abort_flag, prm.err));
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = (l_run > 0.0f) ? (1.0f / l_run) : 0.0f;
-        const float f = inv_l * v_mult;
-        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
-        const bool store = row < N;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + (size_t)(store ? row : 0)) * D * 2;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t u[32];
-          tmem_ld32(o_addr + c0, u);
-          tmem_wait_ld();
-          uint32_t w[16];
+            if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = __uint_as_float(u[2 * i]) * f, b = __uint_as_float(u[2 * i + 1]) * f;
-            w[i] = (ELEM == kFP16) ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
+          if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
         }
-        if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
       }
+      g += Jn;
+      } while (0);
+      if (!ok) break;
+      const int nxt = next_unit(rr + 1, lane == 0);
+      un = __shfl_sync(0xffffffffu, nxt, 0);
+      if (un == -2) ok = false;
     }
   }
 
@@ -639,6 +767,7 @@ struct AttnLaunch {
   CUtensorMap q, k, v;
   AttnParams prm;
   int BH;
+  long long max_ctas;   // 0: one CTA per SM
   cudaStream_t stream;
 };
 
@@ -655,9 +784,44 @@ cudaError_t launch_attn(const AttnLaunch& L) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  const int groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  dim3 grid((unsigned)(L.BH * groups), 1, 1);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.prm);
+  // persistent grid: one CTA per SM (shared memory admits no second one)
+  static int sm_count[64] = {};
+  if (dev >= 0 && dev < 64 && sm_count[dev] == 0) {
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 148;
+  const long long groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
+  const long long units = (long long)L.BH * groups;
+  (void)sms;
+  if constexpr (C::REALLOC) {
+    // the register split must fit what the kernel is launched with, or the
+    // growing warpgroups would wait for registers that never come
+    static int regs_ok[64] = {};
+    if (dev >= 0 && dev < 64 && regs_ok[dev] == 0) {
+      cudaFuncAttributes fa_attr;
+      e = cudaFuncGetAttributes(&fa_attr, kern);
+      if (e != cudaSuccess) return e;
+      regs_ok[dev] = (fa_attr.numRegs * C::THREADS >= 128 * C::CTRL_REGS + C::SOFTMAX_WARPS * 32 * C::SOFTMAX_REGS) ? 1 : -1;
+    }
+    if (dev < 0 || dev >= 64 || regs_ok[dev] != 1) return cudaErrorInvalidConfiguration;
+  }
+  // one CTA per unit, launched as 1x1x1 clusters so that running CTAs can
+  // take over the units of CTAs that have not started (cluster launch control)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)units, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, L.q, L.k, L.v, L.prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

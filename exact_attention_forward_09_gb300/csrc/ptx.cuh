@@ -115,6 +115,45 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ------------------------------------------------- register reallocation --
+// Executed by all threads of a warpgroup: shrink / grow its per-thread
+// register budget (multiples of 8 in [24, 256]).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------- cluster launch control --
+// Ask the hardware to cancel one not-yet-started CTA of this grid; the
+// 16-byte response lands in shared memory and is counted on `bar`.
+__device__ __forceinline__ void clc_try_cancel(void* resp_smem, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          smem_u32(resp_smem)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Decode a response: the cancelled CTA's blockIdx.x, or -1 if none was
+// cancelled (no CTA left to start).
+__device__ __forceinline__ int clc_query_x(const void* resp_smem) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_u32(resp_smem))
+      : "memory");
+  return ok ? (int)x : -1;
+}
+
 // ------------------------------------------------------------------ tcgen05 --
 // TMEM allocation: executed by one whole warp.  Writes the TMEM base address
 // to *dst_smem.
