@@ -659,7 +659,14 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         // (causal diagonal, ragged tail) zero the masked p explicitly; every
         // other tile takes the select-free loop.
         const float2 cj2 = make_float2(cj, cj);
-        const float2 nm2 = make_float2(-m_run, -m_run);
+        // FP8: the V-block factor p~ = p * pv_fac is folded into the exponent
+        // (2^(x - m + log2 pv_fac)); the row sum is rescaled once per tile
+        float lpv = 0.0f, inv_pv = 1.0f;
+        if constexpr (ELEM == kE4M3) {
+          lpv = lg2(pv_fac);
+          inv_pv = 1.0f / pv_fac;
+        }
+        const float2 nm2 = make_float2(lpv - m_run, lpv - m_run);
         float2 acc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
                 const float2 a = p_pair(c, masked_tile), b = p_pair(c + 2, masked_tile);
                 acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
                 acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
-                u[i] = pack_e4m3x4(a.x * pv_fac, a.y * pv_fac, b.x * pv_fac, b.y * pv_fac);
+                u[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
               }
               tmem_st8(s_addr + q * 8, u);
             } else {
@@ -703,7 +710,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         else emit(false);
         {
           const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-          l_run += t.x + t.y;
+          l_run += (ELEM == kE4M3) ? (t.x + t.y) * inv_pv : (t.x + t.y);
         }
         tmem_wait_st();
         tc_fence_before();
