@@ -58,6 +58,8 @@ def _lib():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_check_device_error.restype = i32
+        lib.fa_debug_inject.argtypes = [i32]
+        lib.fa_debug_inject.restype = i32
         lib.fa_version.argtypes = []
         lib.fa_version.restype = i32
         _LIB = lib

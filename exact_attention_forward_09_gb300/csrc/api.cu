@@ -4,6 +4,7 @@
 // library's error word (a __device__ int per device).
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -34,6 +35,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_inject{0};  // one-shot failure injection for the next attention launch
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fa_status device_setup(int* dev_out, int** err_out) {
@@ -149,6 +151,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   L.BH = (int)(B * H);
   L.prm.BH = L.BH;
+  L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
   L.stream = stream;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
 }
@@ -184,6 +187,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   L.BH = (int)(B * H);
   L.prm.BH = L.BH;
+  L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
   L.stream = stream;
   return dispatch<fa::kE4M3>(L, d, causal);
 }
@@ -256,6 +260,12 @@ fa_status fa_check_device_error(cudaStream_t stream) {
     if (cudaMemcpyToSymbol(g_fa_device_error, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
     return FA_ERR_TIMEOUT;
   }
+  return FA_OK;
+}
+
+fa_status fa_debug_inject(int flags) {
+  if (flags != 0 && flags != 1) return FA_ERR_INVALID_ARG;
+  g_inject.store(flags);
   return FA_OK;
 }
 

@@ -122,6 +122,7 @@ struct AttnParams {
   int BH;               // batch x heads
   int nblk;             // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
+  int drop_pos;         // test hook: ring position CTA 0 never fills (-1: none)
 };
 
 // Barriers in shared memory.
@@ -292,6 +293,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             const int slot = pos % C::NS;
             const uint32_t ph = (uint32_t)((pos / C::NS) & 1);
             if (!mbar_wait(&bars->empty[slot], ph ^ 1u, abort_flag, prm.err)) { ok = false; break; }
+            // failure-injection hook (tests only): this slot is never filled,
+            // so the MMA warp's wait on it runs out and the kernel aborts
+            if (pos == prm.drop_pos && blockIdx.x == 0) continue;
             mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
             for (int ch = 0; ch < C::SLOT_CH; ++ch)
               tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,

@@ -1,0 +1,47 @@
+"""Failure detection on the GPU without a GPU fault: a pipeline wait that can
+never complete (the test hook fa_debug_inject leaves one K/V ring slot of
+one CTA unfilled) must end the kernel within its time limit, report
+FA_ERR_TIMEOUT through fa_check_device_error, and leave the CUDA context
+usable for the next, correct call."""
+import math
+import time
+
+import pytest
+import torch
+
+from gpu_util import assert_bf16_parity, errors, make_qkv, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_09_gb300 as fa
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+    return fa
+
+
+def test_pipeline_timeout_is_reported_and_context_survives(fa):
+    host, (q, k, v) = make_qkv(1, 2, 1024, 128, 31)
+    lib = fa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert lib.fa_debug_inject(1) == fa.FA_OK
+    t0 = time.time()
+    fa.fwd(q, k, v, causal=False)
+    st = lib.fa_check_device_error(stream)
+    elapsed = time.time() - t0
+    assert st == fa.FA_ERR_TIMEOUT, lib.fa_status_string(st)
+    assert elapsed < 30.0
+    # the error word is cleared by the check, the hook by the launch
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    o, lse = fa.fwd(q, k, v, causal=False)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    o_ref, l_ref = oracle_rows(host, False, 1.0 / math.sqrt(128))
+    assert_bf16_parity(errors(o, lse, o_ref, l_ref), "after the injected timeout")
+
+
+def test_inject_rejects_bad_flags(fa):
+    assert fa.lib().fa_debug_inject(7) == fa.FA_ERR_INVALID_ARG
+    assert fa.lib().fa_debug_inject(0) == fa.FA_OK
