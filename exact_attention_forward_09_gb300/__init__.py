@@ -17,7 +17,7 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["fwd", "fwd_fp8", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
+__all__ = ["fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
            "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
            "QUANT_NOALLOC_MAX_BLOCKS"]
@@ -50,6 +50,11 @@ def _lib():
         lib.fa_fwd.restype = i32
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, vp, vp, vp, vp]
         lib.fa_fwd_fp8.restype = i32
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32, vp]
+        lib.fa_fwd_gqa.restype = i32
+        lib.fa_fwd_fp8_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, vp, vp, vp,
+                                       vp]
+        lib.fa_fwd_fp8_gqa.restype = i32
         lib.fa_quant_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp]
         lib.fa_quant_fp8.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
@@ -109,6 +114,69 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         st = _lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                            B, H, N, d, int(bool(causal)), float(scale), dt, _stream(q))
     _check(st, "fa_fwd")
+    return out, lse
+
+
+def _check_gqa(q, k, v, allowed):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+        if t.dtype not in allowed:
+            raise ValueError(f"{name} has dtype {t.dtype}; expected one of {allowed}")
+    B, Hq, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or q.dtype != k.dtype or k.dtype != v.dtype:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's batch, head dimension and dtype")
+    if k.shape[1] == 0 or Hq % k.shape[1] != 0:
+        raise ValueError("the number of query heads must be a multiple of the number of key/value heads")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+
+
+def fwd_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+            scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Grouped/multi-query attention with Nq != Nk allowed (``fa_fwd_gqa``):
+    q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d]; causal masks are bottom-right
+    aligned.  Returns (O [B, Hq, Nq, d], LSE [B, Hq, Nq])."""
+    _check_gqa(q, k, v, (torch.bfloat16, torch.float16))
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    dt = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    with torch.cuda.device(q.device):
+        st = _lib().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), dt, _stream(q))
+    _check(st, "fa_fwd_gqa")
+    return out, lse
+
+
+def fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,
+                scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """FP8 E4M3 version of ``fwd_gqa`` (``fa_fwd_fp8_gqa``); descales are
+    [B, Hq, ceil(Nq/128)] for Q and [B, Hkv, ceil(Nk/128)] for K and V."""
+    _check_gqa(q8, k8, v8, (torch.uint8, torch.float8_e4m3fn))
+    B, Hq, Nq, d = q8.shape
+    Hkv, Nk = k8.shape[1], k8.shape[2]
+    nq, nk = (Nq + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS, (Nk + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS
+    for name, t, shape in (("q_descale", q_descale, (B, Hq, nq)), ("k_descale", k_descale, (B, Hkv, nk)),
+                           ("v_descale", v_descale, (B, Hkv, nk))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q8.device:
+            raise ValueError(f"{name} must be a contiguous fp32 {list(shape)} tensor on {q8.device}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        st = _lib().fa_fwd_fp8_gqa(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), q_descale.data_ptr(),
+                                   k_descale.data_ptr(), v_descale.data_ptr(), _stream(q8))
+    _check(st, "fa_fwd_fp8_gqa")
     return out, lse
 
 

@@ -89,18 +89,20 @@ fa_status encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
 }
 
 fa_status check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int64_t B,
-                       int64_t H, int64_t N, int64_t d, float scale, bool* empty) {
-  if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
+                       int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, float scale, bool* empty) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  *empty = (B == 0 || H == 0 || N == 0);
+  *empty = (B == 0 || Hq == 0 || Nq == 0);
   if (*empty) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0 || Nk == 0) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  // index ranges used by the kernels: a 1-D grid of B*H*ceil(N/256) blocks
-  // (at most B*H*ceil(N/128) for one Q tile per block) and int row indices
-  if (N > 0x7fffffffLL - 256 || B * H > 0x7fffffffLL || B * H * ((N + 127) / 128) > 0x7fffffffLL)
+  // index ranges used by the kernels: a 1-D grid of B*Hq*ceil(Nq/256) blocks
+  // (at most B*Hq*ceil(Nq/128) for one Q tile per block) and int row indices
+  const int64_t lim = 0x7fffffffLL - 256;
+  if (Nq > lim || Nk > lim || B * Hq > 0x7fffffffLL || B * Hq * ((Nq + 127) / 128) > 0x7fffffffLL)
     return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -125,12 +127,13 @@ fa_status dispatch(const fa::AttnLaunch& L, int64_t d, int causal) {
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t N,
-                 int64_t d, int causal, float scale, int dtype, cudaStream_t stream) {
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t Hq,
+                     int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, int dtype,
+                     cudaStream_t stream) {
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   bool empty = false;
-  fa_status st = check_common(q, k, v, o, lse, B, H, N, d, scale, &empty);
+  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, &empty);
   if (st != FA_OK || empty) return st;
   int dev = 0;
   int* err = nullptr;
@@ -140,28 +143,38 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   std::memset(&L, 0, sizeof(L));
   const CUtensorMapDataType dt =
       dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((st = encode_map(&L.q, q, dt, 2, B * H, N, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.k, k, dt, 2, B * H, N, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.v, v, dt, 2, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.q, q, dt, 2, B * Hq, Nq, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.o = o;
   L.prm.lse = lse;
   L.prm.err = err;
-  L.prm.N = (int)N;
-  L.prm.nblk = (int)((N + 127) / 128);
+  L.prm.N = (int)Nq;
+  L.prm.Nk = (int)Nk;
+  L.prm.Hq = (int)Hq;
+  L.prm.Hkv = (int)Hkv;
+  L.prm.nblk = (int)((Nq + 127) / 128);
+  L.prm.nblk_k = (int)((Nk + 127) / 128);
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
-  L.BH = (int)(B * H);
+  L.BH = (int)(B * Hq);
   L.prm.BH = L.BH;
   L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
   L.stream = stream;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
 }
 
-fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int64_t B, int64_t H,
-                     int64_t N, int64_t d, int causal, float scale, const float* q_descale, const float* k_descale,
-                     const float* v_descale, cudaStream_t stream) {
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t N,
+                 int64_t d, int causal, float scale, int dtype, cudaStream_t stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, N, d, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, float* lse, int64_t B, int64_t Hq,
+                         int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                         const float* q_descale, const float* k_descale, const float* v_descale,
+                         cudaStream_t stream) {
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   bool empty = false;
-  fa_status st = check_common(q8, k8, v8, o, lse, B, H, N, d, scale, &empty);
+  fa_status st = check_common(q8, k8, v8, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, &empty);
   if (st != FA_OK || empty) return st;
   if (d == 64) return FA_ERR_UNSUPPORTED;  // FP8 rows must span the 128-byte swizzle
   if (!q_descale || !k_descale || !v_descale) return FA_ERR_INVALID_ARG;
@@ -173,23 +186,34 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
 
   fa::AttnLaunch L;
   std::memset(&L, 0, sizeof(L));
-  if ((st = encode_map(&L.q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.k, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.v, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * H, N, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hq, Nq, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.o = o;
   L.prm.lse = lse;
   L.prm.q_ds = q_descale;
   L.prm.k_ds = k_descale;
   L.prm.v_ds = v_descale;
   L.prm.err = err;
-  L.prm.N = (int)N;
-  L.prm.nblk = (int)((N + 127) / 128);
+  L.prm.N = (int)Nq;
+  L.prm.Nk = (int)Nk;
+  L.prm.Hq = (int)Hq;
+  L.prm.Hkv = (int)Hkv;
+  L.prm.nblk = (int)((Nq + 127) / 128);
+  L.prm.nblk_k = (int)((Nk + 127) / 128);
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
-  L.BH = (int)(B * H);
+  L.BH = (int)(B * Hq);
   L.prm.BH = L.BH;
   L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
   L.stream = stream;
   return dispatch<fa::kE4M3>(L, d, causal);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int64_t B, int64_t H,
+                     int64_t N, int64_t d, int causal, float scale, const float* q_descale, const float* k_descale,
+                     const float* v_descale, cudaStream_t stream) {
+  return fa_fwd_fp8_gqa(q8, k8, v8, o, lse, B, H, H, N, N, d, causal, scale, q_descale, k_descale, v_descale,
+                        stream);
 }
 
 fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,

@@ -118,9 +118,12 @@ struct AttnParams {
   const float* k_ds;
   const float* v_ds;
   int* err;             // device error word
-  int N;
-  int BH;               // batch x heads
-  int nblk;             // ceil(N / 128)
+  int N;                // query rows per head (Nq)
+  int Nk;               // keys per head
+  int BH;               // batch x query heads
+  int Hq, Hkv;          // query heads, key/value heads (Hq % Hkv == 0)
+  int nblk;             // ceil(Nq / 128): Q descale blocks per head
+  int nblk_k;           // ceil(Nk / 128): K/V descale blocks per head
   float scale_log2;     // scale * log2(e)
   int drop_pos;         // test hook: ring position CTA 0 never fills (-1: none)
 };
@@ -141,17 +144,21 @@ struct Bars {
   uint64_t unit_full[2];   // queue of next-unit ids (load warp -> others)
   uint64_t unit_empty[2];
   alignas(16) uint32_t clc_resp[4];
-  int unit_q[2];
+  alignas(16) int4 unit_q[2];  // decoded units: {bh (-1: none), kvh, q_base, Jt0 | Jt1 << 16}
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Number of key tiles a Q tile starting at row q0 visits.
+// Number of key tiles a Q tile starting at row q0 visits.  Causal masks are
+// aligned at the bottom right: key j is visible to query i iff
+// j <= i + off with off = Nk - Nq (off = 0 for equal lengths).
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_for(int q0, int nkv) {
+__device__ __forceinline__ int kv_tiles_for(int q0, int nkv, int off) {
   if constexpr (CAUSAL) {
-    int last = q0 / kBN + (kBM / kBN) - 1;  // diagonal tile (kBM == kBN)
-    return last + 1 < nkv ? last + 1 : nkv;
+    const int last_key = q0 + kBM - 1 + off;  // last key any row of the tile sees
+    if (last_key < 0) return 0;
+    const int tiles = last_key / kBN + 1;
+    return tiles < nkv ? tiles : nkv;
   } else {
     return nkv;
   }
@@ -173,8 +180,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = prm.N;
-  const int nkv = (N + kBN - 1) / kBN;
+  const int N = prm.N;                     // query rows
+  const int Nk = prm.Nk;                   // keys
+  const int koff = Nk - N;                 // causal diagonal offset
+  const int nkv = (Nk + kBN - 1) / kBN;
+  const int qgroup = prm.Hq / prm.Hkv;     // query heads per key/value head
   const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
   const int U = prm.BH * n_groups;  // work units: (head, group of NQT Q tiles)
   const int G = (int)gridDim.x;
@@ -190,7 +200,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   // two-slot queue in shared memory.
   (void)G;
   struct Unit {
-    int bh, q_base, J;
+    int bh, kvh, q_base, J;
     int Jt[2];
     bool active[2];
   };
@@ -209,9 +219,10 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       const int q0 = w.q_base + t * kBM;
       w.active[t] = (t < C::NQT) && (q0 < N);
-      w.Jt[t] = w.active[t] ? kv_tiles_for<CAUSAL>(q0, nkv) : 0;
+      w.Jt[t] = w.active[t] ? kv_tiles_for<CAUSAL>(q0, nkv, koff) : 0;
     }
     w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
+    w.kvh = (w.bh / prm.Hq) * prm.Hkv + (w.bh % prm.Hq) / qgroup;
     return w;
   };
 
@@ -246,14 +257,43 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // The id of this CTA's unit number r >= 1 from the queue (-1: no more),
-  // then release the slot.  `arrive` is done by one lane per warp.
-  auto next_unit = [&](int r, bool arrive) -> int {
+  // Unit number r of this CTA from the queue (the load warp decodes each
+  // unit once and publishes it; bh < 0 means no more units), then release
+  // the slot.  `arrive` is done by one lane per warp.
+  auto fetch_unit = [&](int r, bool arrive, bool& okr) -> Unit {
+    Unit w;
     const int slot = r & 1;
-    if (!mbar_wait(&bars->unit_full[slot], (uint32_t)(((r - 1) >> 1) & 1), abort_flag, prm.err)) return -2;
-    const int v = *reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    okr = mbar_wait(&bars->unit_full[slot], (uint32_t)((r >> 1) & 1), abort_flag, prm.err);
+    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    const int4 v = make_int4(qv[0], qv[1], qv[2], qv[3]);
     if (arrive) mbar_arrive(&bars->unit_empty[slot]);
-    return v;
+    w.bh = okr ? v.x : -1;
+    w.kvh = v.y;
+    w.q_base = v.z;
+    w.Jt[0] = v.w & 0xffff;
+    w.Jt[1] = (v.w >> 16) & 0xffff;
+    w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
+    w.active[0] = true;
+    w.active[1] = (C::NQT == 2) && (w.q_base + kBM < N);
+    return w;
+  };
+  // the load warp's side: publish unit r (u < 0: no more units)
+  auto publish_unit = [&](int r, int u) -> bool {
+    const int slot = r & 1;
+    if (r >= 2 && !mbar_wait(&bars->unit_empty[slot], (uint32_t)(((r - 2) >> 1) & 1), abort_flag, prm.err))
+      return false;
+    int4 v = make_int4(-1, 0, 0, 0);
+    if (u >= 0) {
+      const Unit w = decode(u);
+      v = make_int4(w.bh, w.kvh, w.q_base, w.Jt[0] | (w.Jt[1] << 16));
+    }
+    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    qv[0] = v.x;
+    qv[1] = v.y;
+    qv[2] = v.z;
+    qv[3] = v.w;
+    mbar_arrive(&bars->unit_full[slot]);
+    return true;
   };
 
   if (warp >= C::SOFTMAX_WARPS) {
@@ -273,15 +313,17 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       bool more = true;
       bool ok = true;
       int u = (int)blockIdx.x;
+      ok = publish_unit(0, u);
       for (int r = 0; ok && u >= 0; ++r) {
         const Unit w = decode(u);
+        if (w.J > 0) {  // (a unit whose rows see no key needs no loads)
         // the Q buffer is free once the previous unit's last Q K^T finished
         if (k > 0 && !mbar_wait(&bars->q_empty, (uint32_t)((k - 1) & 1), abort_flag, prm.err)) { ok = false; break; }
         uint32_t qbytes = 0;
-        for (int t = 0; t < C::NQT; ++t) qbytes += w.active[t] ? (uint32_t)(kBM * C::ROW_BYTES) : 0u;
+        for (int t = 0; t < C::NQT; ++t) qbytes += w.Jt[t] > 0 ? (uint32_t)(kBM * C::ROW_BYTES) : 0u;
         mbar_arrive_expect_tx(&bars->q_full, qbytes);
         for (int t = 0; t < C::NQT; ++t) {
-          if (!w.active[t]) continue;
+          if (w.Jt[t] == 0) continue;
           for (int ch = 0; ch < C::NCH; ++ch)
             tma_load_3d_hint(smem + C::OFF_Q + (t * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, &bars->q_full,
                              ch * C::CH_ELEMS, w.q_base + t * kBM, w.bh, pol_q);
@@ -299,7 +341,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
             for (int ch = 0; ch < C::SLOT_CH; ++ch)
               tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,
-                               &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, w.bh, pol_kv);
+                               &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, w.kvh, pol_kv);
           }
         };
         if constexpr (C::NQT == 2) {
@@ -315,6 +357,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           }
         }
         ++k;
+        }
         if (!ok) break;
         // every load of this unit is issued: claim the next unit
         int nu = -1;
@@ -326,14 +369,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           nu = clc_query_x(bars->clc_resp);
           if (nu < 0 || nu >= U) { nu = -1; more = false; }
         }
-        // publish it as unit r+1 (slot reused once the others read unit r-1)
-        const int nr = r + 1, slot = nr & 1;
-        if (nr >= 3 && !mbar_wait(&bars->unit_empty[slot], (uint32_t)(((nr - 3) >> 1) & 1), abort_flag, prm.err)) {
+        // publish it as unit r+1 (its slot is reused once the others read unit r-1)
+        if (!publish_unit(r + 1, nu)) {
           ok = false;
           break;
         }
-        *reinterpret_cast<volatile int*>(&bars->unit_q[slot]) = nu;
-        mbar_arrive(&bars->unit_full[slot]);
         u = nu;
       }
       // Never leave with copies in flight: wait (bounded) for the last fill
@@ -411,9 +451,10 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
       };
 
-      int u = (int)blockIdx.x;
-      for (int r = 0; ok && u >= 0; ++r) {
-        const Unit w = decode(u);
+      for (int r = 0; ok; ++r) {
+        const Unit w = fetch_unit(r, true, ok);
+        if (!ok || w.bh < 0) break;
+        if (w.J > 0) {  // (a unit whose rows see no key needs no MMA)
         ok = mbar_wait(&bars->q_full, (uint32_t)(k & 1), abort_flag, prm.err);
         if (!ok) break;
         tc_fence_after();
@@ -503,9 +544,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           g += Jn;
         }
         ++k;
-        if (!ok) break;
-        u = next_unit(r + 1, true);
-        if (u == -2) ok = false;
+        }
       }
       // drain: every MMA issued by this thread has completed before TMEM is freed
       mma_commit(&bars->drain);
@@ -531,25 +570,40 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     int o_seen[2] = {0, 0};   // one Q tile: o_ready completions consumed per buffer
     bool ok = true;
 
-    int un = (int)blockIdx.x;
-    for (int rr = 0; ok && un >= 0; ++rr) {
-      const Unit w = decode(un);
+    for (int rr = 0; ok; ++rr) {
+      bool okr = true;
+      const Unit w = fetch_unit(rr, lane == 0, okr);
+      if (!__all_sync(0xffffffffu, okr)) { ok = false; break; }
+      if (w.bh < 0) break;
       do {  // one unit (skipped when this tile lies beyond N)
       if (!(t == 0 ? w.active[0] : w.active[1])) break;
       const int bh = w.bh;
       const int q0 = w.q_base + t * kBM;
       const int row = q0 + r_in;
       const int Jn = (t == 0) ? w.Jt[0] : w.Jt[1];
+      if (Jn == 0) {
+        // no row of this tile sees a key (causal, Nq > Nk): O = 0, LSE = -inf
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + row) * D * 2);
+#pragma unroll 1
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+          prm.lse[(size_t)bh * N + row] = -INFINITY;
+        }
+        break;
+      }
 
+      // last key this row sees (keys beyond it are masked)
+      const int last_col = CAUSAL ? min(Nk - 1, row + koff) : Nk - 1;
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.0f;
       float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
-      const int bh_blk = bh * prm.nblk;
+      const int bh_blk = bh * prm.nblk;          // Q descale blocks of this head
+      const int kv_blk = w.kvh * prm.nblk_k;     // K/V descale blocks
       float qds = 1.0f, vmax = 1.0f;
       if constexpr (ELEM == kE4M3) {
         qds = prm.q_ds[bh_blk + q0 / kBM];
         vmax = 0.0f;
-        for (int b = 0; b < prm.nblk; ++b) vmax = fmaxf(vmax, prm.v_ds[bh_blk + b]);
+        for (int b = 0; b < prm.nblk_k; ++b) vmax = fmaxf(vmax, prm.v_ds[kv_blk + b]);
         if (!(vmax > 0.0f)) vmax = 1.0f;
         v_mult = vmax / C::P8_SCALE;
       }
@@ -595,17 +649,16 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         float cj = prm.scale_log2;
         float pv_fac = 1.0f;
         if constexpr (ELEM == kE4M3) {
-          cj *= qds * prm.k_ds[bh_blk + j];
-          pv_fac = C::P8_SCALE * (prm.v_ds[bh_blk + j] / vmax);
+          cj *= qds * prm.k_ds[kv_blk + j];
+          pv_fac = C::P8_SCALE * (prm.v_ds[kv_blk + j] / vmax);
         }
         const int col0 = j * kBN;
-        const bool need_mask = (col0 + kBN > N) || (CAUSAL && col0 + kBN - 1 > q0);
+        const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > q0 + koff);
         if (need_mask) {
+          const int lim = last_col - col0;
 #pragma unroll
           for (int c = 0; c < kBN; ++c) {
-            const int col = col0 + c;
-            const bool masked = (col >= N) || (CAUSAL && col > row);
-            s[c] = masked ? mask_val : s[c];
+            s[c] = (c > lim) ? mask_val : s[c];
           }
         }
         // row max (min for a negative scale): eight chains of 3-input max
@@ -632,7 +685,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
         const float mx2 = mx * cj;
         float alpha = 1.0f;
-        const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY);
+        // (a row that has seen no key yet keeps m = -inf until it does)
+        const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY && mx2 != -INFINITY);
         if (move) {
           alpha = ex2(m_run - mx2);  // 0 on the first tile
           m_run = mx2;
@@ -698,15 +752,18 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
               }
               tmem_st8(s_addr + q * 8, u);
             } else {
-              uint32_t u[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int c = q * 32 + 2 * i;
-                const float2 a = p_pair(c, masked_tile);
-                acc[i & 3] = add2(acc[i & 3], a);
-                u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
+              for (int h = 0; h < 2; ++h) {
+                uint32_t u[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const int c = q * 32 + h * 16 + 2 * i;
+                  const float2 a = p_pair(c, masked_tile);
+                  acc[i & 3] = add2(acc[i & 3], a);
+                  u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
+                }
+                tmem_st8(s_addr + q * 16 + h * 8, u);
               }
-              tmem_st16(s_addr + q * 16, u);
             }
           }
         };
@@ -754,10 +811,6 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       }
       g += Jn;
       } while (0);
-      if (!ok) break;
-      const int nxt = next_unit(rr + 1, lane == 0);
-      un = __shfl_sync(0xffffffffu, nxt, 0);
-      if (un == -2) ok = false;
     }
   }
 

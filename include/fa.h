@@ -102,6 +102,36 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
                      cudaStream_t stream);
 
 /*
+ * fa_fwd_gqa -- fa_fwd for grouped-query / multi-query attention and for
+ * different query and key lengths ("FlashAttention-3: async pipelines on
+ * Hopper", section "how GQA/MQA changes the kernel's task count": several
+ * query heads share one K/V head through the head index, K/V are never
+ * copied in HBM).
+ *   q    [B, Hq, Nq, d];  k, v [B, Hkv, Nk, d];  o [B, Hq, Nq, d];  lse [B, Hq, Nq]
+ *   Hq must be a multiple of Hkv (>= 1); query head h reads K/V head
+ *   h / (Hq / Hkv).  Nk >= 1 when Nq >= 1.
+ *   causal: key j is visible to query i iff j <= i + (Nk - Nq) (the mask is
+ *   aligned at the bottom right; for Nq == Nk this is j <= i).  A query row
+ *   that sees no key (causal with Nq > Nk) gets O = 0 and LSE = -inf.
+ * fa_fwd(q, k, v, o, lse, B, H, N, d, ...) equals
+ * fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, N, d, ...).
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                     int causal, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * fa_fwd_fp8_gqa -- fa_fwd_fp8 with the head and length conventions of
+ * fa_fwd_gqa: q8 [B, Hq, Nq, d], q_descale [B, Hq, ceil(Nq/128)];
+ * k8, v8 [B, Hkv, Nk, d], k_descale, v_descale [B, Hkv, ceil(Nk/128)].
+ */
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                         int causal, float scale,
+                         const float* q_descale, const float* k_descale, const float* v_descale,
+                         cudaStream_t stream);
+
+/*
  * fa_quant_fp8 -- quantise fp32 [B, H, N, d] to E4M3 with one scale per
  * 128-row block (per_tensor = 0) or one scale for the whole tensor
  * (per_tensor = 1, the baseline), optionally after the incoherent-processing

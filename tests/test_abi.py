@@ -73,6 +73,12 @@ def test_host_argument_checks(fa_lib):
     assert fa_lib.fa_fwd_fp8(p, p, p, p, p, 1, 1, 1, 128, 0, 0.1, None, p, p, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_fwd_fp8(None, None, None, None, None, 0, 1, 1, 128, 0, 0.1, None, None, None,
                              None) == fa.FA_OK
+    # grouped-query entry point: Hq must be a multiple of Hkv, Nk >= 1
+    assert fa_lib.fa_fwd_gqa(p, p, p, p, p, 1, 6, 4, 8, 8, 64, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_gqa(p, p, p, p, p, 1, 4, 0, 8, 8, 64, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_gqa(p, p, p, p, p, 1, 4, 2, 8, 0, 64, 1, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_gqa(None, None, None, None, None, 1, 4, 2, 0, 9, 64, 1, 0.1, 0, None) == fa.FA_OK
+    assert fa_lib.fa_fwd_fp8_gqa(p, p, p, p, p, 1, 4, 2, 8, 8, 64, 0, 0.1, p, p, p, None) == fa.FA_ERR_UNSUPPORTED
     # quantiser
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 100, None, 0, None, None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 1, None, None) == fa.FA_ERR_INVALID_ARG
