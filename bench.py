@@ -17,6 +17,7 @@ Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -132,26 +133,50 @@ def run_ours(args, rank, world, device):
     B, H, N, d = args.B, args.H, args.N, args.d
     causal = args.causal
     scale = 1.0 / math.sqrt(d)
-    dtype = torch.bfloat16
+    fp8 = args.fp8
+    dtype = torch.float32 if fp8 else torch.bfloat16
     g = torch.Generator(device=device)
     g.manual_seed(1 + rank)
     q = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
     k = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
     v = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
-    o = torch.empty_like(q)
+    o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
     lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
     flush = torch.empty(512 * 1024 * 1024 // 4, device=device, dtype=torch.float32)
     stream = torch.cuda.current_stream(device)
     flops = gen.flops(B, H, N, d, causal)
+    signs = gen.hadamard_signs(d, 4)
+    if fp8:
+        nb = (N + 127) // 128
+        q8, k8, v8 = (torch.empty((B, H, N, d), device=device, dtype=torch.uint8) for _ in range(3))
+        qs, ks, vs = (torch.empty((B, H, nb), device=device, dtype=torch.float32) for _ in range(3))
+    launches_per_step = 4 if fp8 else 1
 
-    def step():
-        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+    # one step = the whole hot path on one batch: FP8 quantises Q and K
+    # (block scales + Hadamard) and V (block scales), then runs attention;
+    # `mid` marks the start of the attention launch (the dominant kernel)
+    def step(qi, ki, vi, mid=None):
+        if fp8:
+            lib = fa.lib()
+            sp = torch.cuda.current_stream(device).cuda_stream
+            keep = (ctypes.c_int8 * d)(*[int(x) for x in signs])
+            for x, c, ds, rot in ((qi, q8, qs, True), (ki, k8, ks, True), (vi, v8, vs, False)):
+                st = lib.fa_quant_fp8(x.data_ptr(), c.data_ptr(), ds.data_ptr(), B, H, N, d,
+                                      ctypes.cast(keep, ctypes.c_void_p) if rot else None, 0, None, sp)
+                assert st == 0
+            if mid is not None:
+                mid.record(stream)
+            fa.fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, scale=scale, out=o, lse=lse)
+        else:
+            if mid is not None:
+                mid.record(stream)
+            fa.fwd(qi, ki, vi, causal=causal, scale=scale, out=o, lse=lse)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        step(q, k, v)
     fa.check_device_error(device)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     sampler = ClockSampler(device.index if device.index is not None else 0)
     _barrier(world)
     torch.cuda.synchronize(device)
@@ -159,15 +184,15 @@ def run_ours(args, rank, world, device):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+        step(q, k, v, mid=ev[i][1])
+        ev[i][2].record(stream)
     torch.cuda.synchronize(device)
     _barrier(world)
     clocks = sampler.stop()
     fa.check_device_error(device)
-    times_ms = [a.elapsed_time(b) for a, b in ev]
+    times_ms = [a.elapsed_time(c) for a, _, c in ev]
     total_ms = _max_over_ranks(sum(times_ms), world, device)
-    launch_ms = sum(times_ms) / len(times_ms)
+    launch_ms = sum(b.elapsed_time(c) for _, b, c in ev) / len(ev)   # the attention launch alone
 
     # end to end through the public API: pinned host inputs -> device, kernel,
     # result back to pinned host memory, every step
@@ -182,7 +207,7 @@ def run_ours(args, rank, world, device):
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
-        fa.fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse)
+        step(qd, kd, vd)
         oh.copy_(o, non_blocking=True)
         lh.copy_(lse, non_blocking=True)
 
@@ -205,6 +230,7 @@ def run_ours(args, rank, world, device):
         extra = run_extra(args, device)
 
     return dict(times_ms=times_ms, total_ms=total_ms, launch_ms=launch_ms, flops=flops, clocks=clocks,
+                launches_per_step=launches_per_step,
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, extra=extra)
 
 
@@ -280,6 +306,12 @@ def run_extra(args, device):
     return out
 
 
+def whole_job_tflops(flops_per_rank_step: float, world: int, total_ms_max: float, steps: int) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_rank_step`
+    (independent problems); the job takes the slowest rank's time."""
+    return flops_per_rank_step * world * steps / (total_ms_max * 1e-3) / 1e12
+
+
 def _barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -353,7 +385,9 @@ def run_reference(args, rank, world):
 
 
 def _config(args):
-    return {"workload": f"{args.workload}: B={args.B} H={args.H} N={args.N} d={args.d} bf16 "
+    kind = ("fp32 inputs quantised to e4m3 in the step (Q, K: block scales + Hadamard; V: block scales), "
+            "then FP8 attention" if getattr(args, "fp8", False) else "bf16")
+    return {"workload": f"{args.workload}: B={args.B} H={args.H} N={args.N} d={args.d} {kind} "
                         f"{'causal' if args.causal else 'non-causal'} scale=1/sqrt(d)",
             "B": args.B, "H": args.H, "N": args.N, "d": args.d, "causal": bool(args.causal),
             "l2": "flushed before every timed step (512 MB write, outside the timed events)",
@@ -366,13 +400,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mid", choices=["mid", "sweep4k", "sweep16k", "long"])
+    ap.add_argument("--workload", default="mid", choices=["mid", "sweep4k", "sweep16k", "long", "fp8_4k", "fp8_16k"])
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     shapes = {"mid": (4, 16, 2048, 128), "sweep4k": (4, 16, 4096, 128), "sweep16k": (1, 16, 16384, 128),
-              "long": (1, 16, 65536, 128)}
+              "long": (1, 16, 65536, 128), "fp8_4k": (4, 16, 4096, 128), "fp8_16k": (1, 16, 16384, 128)}
+    args.fp8 = args.workload.startswith("fp8")
     args.B, args.H, args.N, args.d = shapes[args.workload]
     if args.workload == "long":
         args.causal = True
@@ -396,27 +431,34 @@ def main():
 
     if rank == 0:
         peaks, peak_src = load_peaks()
-        tflops = res["flops"] * world / (res["total_ms"] * 1e-3 / args.steps) / 1e12
+        tflops = whole_job_tflops(res["flops"], world, res["total_ms"], args.steps)
         achieved = res["flops"] / (res["launch_ms"] * 1e-3) / 1e12
         e2e_tflops = res["flops"] * world / (res["e2e_ms"] * 1e-3) / 1e12
         cpu_tf, cpu_s, cpu_sample, cpu_threads = time_oracle(args.B, args.H, args.N, args.d, args.causal,
                                                               args.cpu_budget)
         traffic = load_traffic(args.workload + ("_causal" if args.causal else ""))
+        if args.fp8:
+            peak = peaks["bf16_tflops"] * 2.0
+            peak_source = f"{peak_src} bf16 burst (cuBLAS GEMM) x 2, the nominal dense fp8:bf16 ratio"
+            kernel = f"attn_fwd_kernel<e4m3,{args.d},{'causal' if args.causal else 'non-causal'}>"
+        else:
+            peak = peaks["bf16_tflops"]
+            peak_source = f"{peak_src} bf16 burst (cuBLAS GEMM)"
+            kernel = f"attn_fwd_kernel<bf16,{args.d},{'causal' if args.causal else 'non-causal'}>"
         line = {
             "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": res["total_ms"] / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16", "data": "synthetic",
             "config": _config(args),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16 burst (cuBLAS GEMM)",
-                         "kernel": "attn_fwd_kernel<bf16,128,non-causal>",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_source, "kernel": kernel,
                          "algorithmic_flops_per_launch": res["flops"]},
             "cpu_baseline": {"value": cpu_tf, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
                              "sample": cpu_sample, "seconds": round(cpu_s, 2)},
             "e2e": {"value": e2e_tflops, "unit": "TFLOPS", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"]},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * res["launches_per_step"],
             "clocks": res["clocks"],
             "extra": res["extra"],
         }

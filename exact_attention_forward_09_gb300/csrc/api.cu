@@ -249,6 +249,7 @@ fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int6
   L.x8 = static_cast<uint8_t*>(x8);
   L.descale = descale;
   L.amax_ws = workspace;
+  L.err = err;
   L.BH = (int)(B * H);
   L.N = (int)N;
   L.d = (int)d;

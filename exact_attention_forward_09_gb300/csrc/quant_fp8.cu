@@ -5,7 +5,9 @@
 // "how incoherent processing flattens outliers"; E4M3 maximum 448 from the
 // wmrh.cn FlashAttention V3 article, sec. 3.3).
 //
-// One CTA per (head, 128-row block), one warp per row at a time.  Each lane
+// One CTA per (head, 128-row block).  The block's rows are contiguous in
+// memory, so one bulk copy (cp.async.bulk, completion on an mbarrier) brings
+// the whole block into shared memory; then one warp per row at a time.  Each lane
 // holds d/32 consecutive elements; the Walsh-Hadamard butterfly runs inside
 // the lane for strides below d/32 and across lanes (shuffle) above, stride
 // 1, 2, 4, ... in fp32, so every element sees the same sequence of fp32
@@ -16,6 +18,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
 #include "quant_fp8.h"
 
 namespace fa {
@@ -63,11 +66,13 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
                                                          float* __restrict__ descale, int N, int nblk,
                                                          SignBits sg, int rot, float rinv,
-                                                         float* __restrict__ amax_ws) {
+                                                         float* __restrict__ amax_ws, int* err) {
   constexpr int E = D / 32;
   constexpr int ROWS = 128;
-  extern __shared__ __align__(16) float ys[];  // [ROWS][D] (MODE 0 only)
+  extern __shared__ __align__(128) float ys[];  // [ROWS][D]: the block, rotated in place
   __shared__ float red[8];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int failed;
   const int blk = blockIdx.x;
   const int bh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,17 +80,40 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
   const int nrows = min(ROWS, N - r0);
   const size_t base = ((size_t)bh * N + r0) * D;
 
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    failed = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)(nrows * D * sizeof(float));
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load(ys, x + base, bytes, &bar);
+    // bounded wait for the block
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bar, 0)) {
+      if (globaltimer() - t0 > FA_WAIT_LIMIT_NS) {
+        failed = 1;
+        if (err) atomicExch(err, FA_DEVERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (failed) return;
+
   float amax = 0.0f;
   for (int r = warp; r < nrows; r += 8) {
     float v[E];
-    const float* src = x + base + (size_t)r * D + lane * E;
+    float* yrow = ys + r * D + lane * E;
     if constexpr (E == 2) {
-      const float2 t = *reinterpret_cast<const float2*>(src);
+      const float2 t = *reinterpret_cast<const float2*>(yrow);
       v[0] = t.x; v[1] = t.y;
     } else {
 #pragma unroll
       for (int q = 0; q < E / 4; ++q) {
-        const float4 t = reinterpret_cast<const float4*>(src)[q];
+        const float4 t = reinterpret_cast<const float4*>(yrow)[q];
         v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
     }
@@ -93,8 +121,10 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
     if constexpr (MODE == 0) {
+      if (rot) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) ys[r * D + lane * E + e] = v[e];
+        for (int e = 0; e < E; ++e) yrow[e] = v[e];
+      }
     } else if constexpr (MODE == 2) {
       // per-tensor encode: scale known up front
       const float am = *amax_ws;
@@ -159,33 +189,41 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
   }
 }
 
+// Dynamic shared memory of one block (128 rows x D fp32), set once per
+// device for each instance.
+template <int D, int MODE>
+static cudaError_t prep_quant() {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(quant_e4m3_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(128u * D * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <int D, int MODE>
+static cudaError_t launch_mode(const QuantLaunch& L, float* ws) {
+  cudaError_t e = prep_quant<D, MODE>();
+  if (e != cudaSuccess) return e;
+  const dim3 grid(L.nblk, L.BH, 1);
+  quant_e4m3_kernel<D, MODE><<<grid, 256, 128u * D * sizeof(float), L.stream>>>(
+      L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv, ws, L.err);
+  return cudaGetLastError();
+}
+
 template <int D>
 static cudaError_t launch_quant_d(const QuantLaunch& L) {
-  const dim3 grid(L.nblk, L.BH, 1);
-  const size_t smem = 128u * D * sizeof(float);
-  if (!L.per_tensor) {
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-      e = cudaFuncSetAttribute(quant_e4m3_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
-    quant_e4m3_kernel<D, 0><<<grid, 256, smem, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot,
-                                                             L.rinv, nullptr);
-    return cudaGetLastError();
-  }
+  if (!L.per_tensor) return launch_mode<D, 0>(L, nullptr);
   cudaError_t e = cudaMemsetAsync(L.amax_ws, 0, sizeof(float), L.stream);
   if (e != cudaSuccess) return e;
-  quant_e4m3_kernel<D, 1><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
-                                                       L.amax_ws);
-  e = cudaGetLastError();
+  e = launch_mode<D, 1>(L, L.amax_ws);
   if (e != cudaSuccess) return e;
-  quant_e4m3_kernel<D, 2><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
-                                                       L.amax_ws);
-  return cudaGetLastError();
+  return launch_mode<D, 2>(L, L.amax_ws);
 }
 
 // Maximum of n partial maxima -> *out (one CTA).
@@ -208,17 +246,12 @@ __global__ void __launch_bounds__(1024) reduce_max_kernel(const float* __restric
 
 template <int D>
 static cudaError_t launch_quant_partials_d(const QuantLaunch& L, float* partials, float* amax_out) {
-  const dim3 grid(L.nblk, L.BH, 1);
-  quant_e4m3_kernel<D, 3><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
-                                                       partials);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_mode<D, 3>(L, partials);
   if (e != cudaSuccess) return e;
   reduce_max_kernel<<<1, 1024, 0, L.stream>>>(partials, L.BH * L.nblk, amax_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quant_e4m3_kernel<D, 2><<<grid, 256, 0, L.stream>>>(L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv,
-                                                       amax_out);
-  return cudaGetLastError();
+  return launch_mode<D, 2>(L, amax_out);
 }
 
 cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partials, float* amax_out) {

@@ -16,6 +16,7 @@ struct QuantLaunch {
   uint8_t* x8;      // [BH, N, d] E4M3 codes
   float* descale;   // [BH, nblk]
   float* amax_ws;   // per-tensor mode: one float of scratch
+  int* err;         // device error word (may be null)
   int BH, N, d, nblk;
   int per_tensor;
   int rot;
