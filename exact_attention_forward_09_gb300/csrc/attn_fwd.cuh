@@ -419,8 +419,22 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         for (int sp = 0; sp < C::SPT; ++sp) mma_commit(&bars->empty[(p + sp) % C::NS]);
       };
       // S_buf = Q_t K^T for the K tile at ring position p
+      // Descriptors are built once and advanced per K step by adding the
+      // step's byte offset >> 4 to the start-address field (bits 0..13; all
+      // shared addresses are below 256 KB, so the field cannot overflow):
+      // the issuing thread then spends a single add per operand per MMA.
+      const uint64_t q_desc0 = smem_desc(q_s, 16, 1024, 2);                 // Q tiles, K-major
+      const uint64_t ring_k_desc0 = smem_desc(ring_s, 16, 1024, 2);         // K slots, K-major
+      const uint64_t ring_v_desc0 = smem_desc(ring_s, C::CHUNK_BYTES, 1024, 2);  // V slots, MN-major
+      auto slot_of = [&](int p) -> uint32_t { return (uint32_t)(p % C::NS); };
+      // S_buf = Q_t K^T for the K tile at ring position p
       auto issue_qk = [&](int t, int buf, int p) {
         const uint32_t d_tmem = tmem + C::S_COL0 + buf * kBN;
+        const uint64_t a0 = q_desc0 + (uint64_t)((t * C::NCH * C::CHUNK_BYTES) >> 4);
+        uint64_t b0[C::SPT];
+#pragma unroll
+        for (int sp = 0; sp < C::SPT; ++sp)
+          b0[sp] = ring_k_desc0 + (uint64_t)((slot_of(p + sp) * C::SLOT_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
           const int byte_k = ks * 32;                         // byte offset along the row
@@ -428,10 +442,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           const int in_ch = byte_k % 128;
           const int sp = ch / C::SLOT_CH;                     // which slot of the tile
           const int ch_in_slot = ch % C::SLOT_CH;
-          const uint32_t a = q_s + (t * C::NCH + ch) * C::CHUNK_BYTES + in_ch;
-          const uint32_t b = ring_s + ((p + sp) % C::NS) * C::SLOT_BYTES + ch_in_slot * C::CHUNK_BYTES + in_ch;
-          mma_ss<C::MMA_KIND>(d_tmem, smem_desc(a, 16, 1024, 2), smem_desc(b, 16, 1024, 2), C::IDESC_QK,
-                              ks > 0 ? 1u : 0u);
+          const uint64_t a = a0 + (uint64_t)((ch * C::CHUNK_BYTES + in_ch) >> 4);
+          const uint64_t b = b0[sp] + (uint64_t)((ch_in_slot * C::CHUNK_BYTES + in_ch) >> 4);
+          mma_ss<C::MMA_KIND>(d_tmem, a, b, C::IDESC_QK, ks > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_buf V for the V tile at ring position p
@@ -440,13 +453,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
 #pragma unroll
         for (int sp = 0; sp < C::SPT; ++sp) {
           const uint32_t d_tmem = tmem + C::O_COL0 + t * D + sp * C::SLOT_D;
-          const uint32_t vbase = ring_s + ((p + sp) % C::NS) * C::SLOT_BYTES;
+          const uint64_t v0 = ring_v_desc0 + (uint64_t)((slot_of(p + sp) * C::SLOT_BYTES) >> 4);
 #pragma unroll
           for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
             // keys ks*KSTEP .. +KSTEP-1 are KSTEP/8 groups of 8 rows (1024 B each)
-            const uint32_t b = vbase + ks * (C::KSTEP / 8) * 1024;
-            mma_ts<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, smem_desc(b, C::CHUNK_BYTES, 1024, 2), C::IDESC_PV,
-                                (acc || ks > 0) ? 1u : 0u);
+            const uint64_t b = v0 + (uint64_t)((ks * (C::KSTEP / 8) * 1024) >> 4);
+            mma_ts<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
           }
         }
       };
