@@ -87,12 +87,14 @@ struct AttnCfg {
   // warps) so that registers can move between whole warpgroups: launched
   // at LAUNCH_REGS, the control warpgroup drops to CTRL_REGS and the softmax
   // warpgroups rise to SOFTMAX_REGS (their sum stays within the launch
-  // total).  One Q tile: 6 warps, no reallocation needed.
+  // total).  One Q tile: 6 warps, no reallocation needed.  The 16-bit
+  // kernels' warp-wide MMA loop needs more than 72 registers (it spills at
+  // 72); the FP8 softmax is the tighter side and keeps 216.
   static constexpr bool REALLOC = (NQT == 2);
   static constexpr int THREADS = REALLOC ? 32 * (SOFTMAX_WARPS + 4) : 32 * (SOFTMAX_WARPS + 2);
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = 72;
-  static constexpr int SOFTMAX_REGS = 216;
+  static constexpr int CTRL_REGS = (ELEM == kE4M3) ? 72 : 88;
+  static constexpr int SOFTMAX_REGS = (ELEM == kE4M3) ? 216 : 208;
   static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   // lazy-rescale threshold (log2 units): P <= 2^TAU.  FP8 P must stay far
@@ -396,7 +398,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------- MMA --
-    if (lane == 0) {
+    // The whole warp runs the issuing loop in step, so that its counters,
+    // ring positions and descriptors are warp-uniform; each tcgen05.mma and
+    // commit is issued by one elected lane.  A single diverged lane running
+    // the same loop spends nearly a 128x128x16 step's tensor time on issuing
+    // each MMA, so every wait and commit beside them starves the pipe.
+    {
       const uint32_t q_s = smem_u32(smem + C::OFF_Q);
       const uint32_t ring_s = smem_u32(smem + C::OFF_RING);
       int pos = 0;          // ring position of the next item to consume
@@ -404,19 +411,23 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       int pc[2] = {0, 0};   // two Q tiles: P handshakes consumed per tile
       int g = 0;            // one Q tile: S/P iterations so far (buffer = g & 1)
       bool ok = true;
+      // every lane waits; the outcome is made uniform across the warp
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity, volatile int* af, int* ew) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, af, ew));
+      };
 
       // wait for a whole tile (SPT slots) at the current ring position
       auto wait_tile = [&](int p) -> bool {
         for (int sp = 0; sp < C::SPT; ++sp) {
           const int slot = (p + sp) % C::NS;
-          if (!mbar_wait(&bars->full[slot], (uint32_t)(((p + sp) / C::NS) & 1), abort_flag, prm.err))
+          if (!warp_wait(&bars->full[slot], (uint32_t)(((p + sp) / C::NS) & 1), abort_flag, prm.err))
             return false;
         }
         tc_fence_after();
         return true;
       };
       auto release_tile = [&](int p) {
-        for (int sp = 0; sp < C::SPT; ++sp) mma_commit(&bars->empty[(p + sp) % C::NS]);
+        for (int sp = 0; sp < C::SPT; ++sp) mma_commit_elect(&bars->empty[(p + sp) % C::NS]);
       };
       // S_buf = Q_t K^T for the K tile at ring position p
       // Descriptors are built once and advanced per K step by adding the
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           const int ch_in_slot = ch % C::SLOT_CH;
           const uint64_t a = a0 + (uint64_t)((ch * C::CHUNK_BYTES + in_ch) >> 4);
           const uint64_t b = b0[sp] + (uint64_t)((ch_in_slot * C::CHUNK_BYTES + in_ch) >> 4);
-          mma_ss<C::MMA_KIND>(d_tmem, a, b, C::IDESC_QK, ks > 0 ? 1u : 0u);
+          mma_ss_elect<C::MMA_KIND>(d_tmem, a, b, C::IDESC_QK, ks > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_buf V for the V tile at ring position p
@@ -458,22 +469,23 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
             // keys ks*KSTEP .. +KSTEP-1 are KSTEP/8 groups of 8 rows (1024 B each)
             const uint64_t b = v0 + (uint64_t)((ks * (C::KSTEP / 8) * 1024) >> 4);
-            mma_ts<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+            mma_ts_elect<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
           }
         }
       };
 
       for (int r = 0; ok; ++r) {
-        const Unit w = fetch_unit(r, true, ok);
+        const Unit w = fetch_unit(r, lane == 0, ok);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok || w.bh < 0) break;
         if (w.J > 0) {  // (a unit whose rows see no key needs no MMA)
-        ok = mbar_wait(&bars->q_full, (uint32_t)(k & 1), abort_flag, prm.err);
+        ok = warp_wait(&bars->q_full, (uint32_t)(k & 1), abort_flag, prm.err);
         if (!ok) break;
         tc_fence_after();
         // the Q buffer is released after this unit's last Q K^T
         int qk_left = w.Jt[0] + w.Jt[1];
         auto qk_issued = [&]() {
-          if (--qk_left == 0) mma_commit(&bars->q_empty);
+          if (--qk_left == 0) mma_commit_elect(&bars->q_empty);
         };
         if constexpr (C::NQT == 2) {
           // prologue: S_t(0) for both tiles
@@ -483,7 +495,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           for (int t = 0; t < 2; ++t)
             if (w.Jt[t] > 0) {
               issue_qk(t, t, pos);
-              mma_commit(&bars->s_full[t]);
+              mma_commit_elect(&bars->s_full[t]);
               qk_issued();
             }
           release_tile(pos);
@@ -495,7 +507,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             for (int t = 0; t < 2 && ok; ++t) {
               if (j >= w.Jt[t]) continue;
               if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
-              ok = mbar_wait(&bars->p_full[t], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
+              ok = warp_wait(&bars->p_full[t], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
               ++pc[t];
               if (!ok) break;
               tc_fence_after();
@@ -503,10 +515,10 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
               if (j + 1 < w.Jt[t]) {
                 if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
                 issue_qk(t, t, k_pos);
-                mma_commit(&bars->s_full[t]);
+                mma_commit_elect(&bars->s_full[t]);
                 qk_issued();
               } else {
-                mma_commit(&bars->o_full[t]);
+                mma_commit_elect(&bars->o_full[t]);
               }
             }
             if (!ok) break;
@@ -525,7 +537,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             ok = wait_tile(pos);
             if (!ok) break;
             issue_qk(0, (g + j) & 1, pos);
-            mma_commit(&bars->s_full[(g + j) & 1]);
+            mma_commit_elect(&bars->s_full[(g + j) & 1]);
             qk_issued();
             release_tile(pos);
             pos += C::SPT;
@@ -535,31 +547,31 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             const int b = gj & 1;
             ok = wait_tile(pos);  // V_j
             if (!ok) break;
-            ok = mbar_wait(&bars->p_full[b], (uint32_t)((gj >> 1) & 1), abort_flag, prm.err);
+            ok = warp_wait(&bars->p_full[b], (uint32_t)((gj >> 1) & 1), abort_flag, prm.err);
             if (!ok) break;
             tc_fence_after();
             issue_pv(0, b, pos, j > 0);
-            mma_commit(&bars->o_ready[b]);
+            mma_commit_elect(&bars->o_ready[b]);
             release_tile(pos);
             pos += C::SPT;
             if (j + 2 < Jn) {
               ok = wait_tile(pos);  // K_{j+2}
               if (!ok) break;
               issue_qk(0, b, pos);
-              mma_commit(&bars->s_full[b]);
+              mma_commit_elect(&bars->s_full[b]);
               qk_issued();
               release_tile(pos);
               pos += C::SPT;
             }
           }
-          if (ok) mma_commit(&bars->o_full[0]);
+          if (ok) mma_commit_elect(&bars->o_full[0]);
           g += Jn;
         }
         ++k;
         }
       }
       // drain: every MMA issued by this thread has completed before TMEM is freed
-      mma_commit(&bars->drain);
+      mma_commit_elect(&bars->drain);
       uint64_t t0 = globaltimer();
       while (!mbar_try_wait(&bars->drain, 0) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
       }
