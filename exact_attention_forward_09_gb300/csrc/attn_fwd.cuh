@@ -18,8 +18,9 @@
 //                  full/empty mbarriers ("FlashAttention-3: async pipelines
 //                  on Hopper", section "first overlap: producer and consumer
 //                  in parallel": stage = j mod s, two states per stage).
-//   * MMA warp     one thread issues every tcgen05.mma: S = Q K^T into TMEM,
-//                  then O += P V with P read from TMEM; it also allocates TMEM.
+//   * MMA warp     runs in step; one elected lane issues every tcgen05.mma:
+//                  S = Q K^T into TMEM, then O += P V with P read from TMEM;
+//                  it also allocates TMEM.
 //   * softmax      one warpgroup per Q tile, one thread per query row: reads
 //                  S from TMEM, masks, takes the row max, rescales O in TMEM
 //                  when the max moved by more than TAU (exact: o, l, m stay
@@ -97,11 +98,12 @@ struct AttnCfg {
   static constexpr int SOFTMAX_REGS = (ELEM == kE4M3) ? 216 : 208;
   static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
-  // lazy-rescale threshold (log2 units): P <= 2^TAU.  FP8 P must stay far
-  // below the E4M3 maximum, so FP8 rescales whenever the max moves.
-  static constexpr float TAU = (ELEM == kE4M3) ? 0.0f : 8.0f;
-  // FP8: P is stored as p * 2^8 * (s_Vj / max_j s_Vj) <= 256 < 448
-  static constexpr float P8_SCALE = 256.0f;
+  // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max
+  static constexpr float TAU = (ELEM == kE4M3) ? 2.0f : 8.0f;
+  // FP8: P is stored as p * 2^6 * (s_Vj / max_j s_Vj) <= 2^6 * 2^TAU = 256,
+  // inside the E4M3 range (448)
+  static constexpr float P8_SCALE = 64.0f;
+  static_assert(ELEM != kE4M3 || P8_SCALE * (1 << (int)TAU) <= 256.0f, "FP8 P would leave the E4M3 range");
   static constexpr uint32_t A_FMT = (ELEM == kBF16) ? 1u : 0u;  // bf16=1, f16=0, e4m3=0
   static constexpr uint32_t IDESC_QK = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN);
   static constexpr uint32_t IDESC_PV = instr_desc(A_FMT, A_FMT, 0, 1, 128, SLOT_D);
