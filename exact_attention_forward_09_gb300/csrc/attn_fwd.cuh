@@ -76,6 +76,7 @@ struct AttnCfg {
   static constexpr int KSTEP = 32 / ES;                        // MMA K per instruction (32 bytes)
   static constexpr int KSTEPS_QK = D / KSTEP;
   static constexpr int KSTEPS_PV = kBN / KSTEP;
+  static_assert(KSTEPS_PV % 2 == 0, "P is handed over in two halves of the key tile");
   static constexpr int P_COLS = kBN * ES / 4;                  // TMEM columns of P per row
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0;                        // S/P buffers at 0 and 128
@@ -89,13 +90,14 @@ struct AttnCfg {
   // at LAUNCH_REGS, the control warpgroup drops to CTRL_REGS and the softmax
   // warpgroups rise to SOFTMAX_REGS (their sum stays within the launch
   // total).  One Q tile: 6 warps, no reallocation needed.  The 16-bit
-  // kernels' warp-wide MMA loop needs more than 72 registers (it spills at
-  // 72); the FP8 softmax is the tighter side and keeps 216.
+  // kernels' warp-wide MMA loop spills below ~100 registers and their
+  // softmax fits in 200 (measured fastest of 72/216, 88/208, 104/200); the
+  // FP8 softmax is the tighter side and keeps 216.
   static constexpr bool REALLOC = (NQT == 2);
   static constexpr int THREADS = REALLOC ? 32 * (SOFTMAX_WARPS + 4) : 32 * (SOFTMAX_WARPS + 2);
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = (ELEM == kE4M3) ? 72 : 88;
-  static constexpr int SOFTMAX_REGS = (ELEM == kE4M3) ? 216 : 208;
+  static constexpr int CTRL_REGS = (ELEM == kE4M3) ? 72 : 104;
+  static constexpr int SOFTMAX_REGS = (ELEM == kE4M3) ? 216 : 200;
   static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max
@@ -140,7 +142,7 @@ struct Bars {
   uint64_t full[NS];
   uint64_t empty[NS];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2][2];  // [S/P buffer][half of the key tile]
   uint64_t o_ready[2];
   uint64_t o_full[2];
   uint64_t drain;
@@ -239,7 +241,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t][0], 128);
+      mbar_init(&bars->p_full[t][1], 128);
       mbar_init(&bars->o_ready[t], 1);
       mbar_init(&bars->o_full[t], 1);
     }
@@ -460,15 +463,15 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           mma_ss_elect<C::MMA_KIND>(d_tmem, a, b, C::IDESC_QK, ks > 0 ? 1u : 0u);
         }
       };
-      // O_t (+)= P_buf V for the V tile at ring position p
-      auto issue_pv = [&](int t, int buf, int p, bool acc) {
+      // O_t (+)= P_buf V for half h of the keys of the V tile at ring position p
+      auto issue_pv = [&](int t, int buf, int p, bool acc, int h) {
         const uint32_t p_tmem = tmem + C::S_COL0 + buf * kBN;
 #pragma unroll
         for (int sp = 0; sp < C::SPT; ++sp) {
           const uint32_t d_tmem = tmem + C::O_COL0 + t * D + sp * C::SLOT_D;
           const uint64_t v0 = ring_v_desc0 + (uint64_t)((slot_of(p + sp) * C::SLOT_BYTES) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
+          for (int ks = h * (C::KSTEPS_PV / 2); ks < (h + 1) * (C::KSTEPS_PV / 2); ++ks) {
             // keys ks*KSTEP .. +KSTEP-1 are KSTEP/8 groups of 8 rows (1024 B each)
             const uint64_t b = v0 + (uint64_t)((ks * (C::KSTEP / 8) * 1024) >> 4);
             mma_ts_elect<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
@@ -509,11 +512,17 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             for (int t = 0; t < 2 && ok; ++t) {
               if (j >= w.Jt[t]) continue;
               if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
-              ok = warp_wait(&bars->p_full[t], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
+              // P arrives in two halves of the key tile: the first half's
+              // MMAs run while the softmax still writes the second
+#pragma unroll
+              for (int h = 0; h < 2 && ok; ++h) {
+                ok = warp_wait(&bars->p_full[t][h], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, t, pv_pos, j > 0, h);
+              }
               ++pc[t];
               if (!ok) break;
-              tc_fence_after();
-              issue_pv(t, t, pv_pos, j > 0);
               if (j + 1 < w.Jt[t]) {
                 if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
                 issue_qk(t, t, k_pos);
@@ -549,10 +558,14 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             const int b = gj & 1;
             ok = wait_tile(pos);  // V_j
             if (!ok) break;
-            ok = warp_wait(&bars->p_full[b], (uint32_t)((gj >> 1) & 1), abort_flag, prm.err);
+#pragma unroll
+            for (int h = 0; h < 2 && ok; ++h) {
+              ok = warp_wait(&bars->p_full[b][h], (uint32_t)((gj >> 1) & 1), abort_flag, prm.err);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(0, b, pos, j > 0, h);
+            }
             if (!ok) break;
-            tc_fence_after();
-            issue_pv(0, b, pos, j > 0);
             mma_commit_elect(&bars->o_ready[b]);
             release_tile(pos);
             pos += C::SPT;
@@ -766,6 +779,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         auto emit = [&](bool masked_tile) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            if (q == 2) {
+              // keys 0..63 of P are in TMEM: let their MMAs start
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(&bars->p_full[buf][0]);
+            }
             if constexpr (ELEM == kE4M3) {
               uint32_t u[8];
 #pragma unroll
@@ -801,7 +820,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[buf]);
+        mbar_arrive(&bars->p_full[buf][1]);
       }
 
       // ---------------------------------------------------------- epilogue --
