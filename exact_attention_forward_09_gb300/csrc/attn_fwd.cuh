@@ -641,10 +641,31 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       float qds = 1.0f, vmax = 1.0f;
       if constexpr (ELEM == kE4M3) {
         qds = prm.q_ds[bh_blk + q0 / kBM];
+        // max of the head's V-block descales: lanes take strided blocks
         vmax = 0.0f;
-        for (int b = 0; b < prm.nblk_k; ++b) vmax = fmaxf(vmax, prm.v_ds[kv_blk + b]);
+        for (int b = lane; b < prm.nblk_k; b += 32) vmax = fmaxf(vmax, prm.v_ds[kv_blk + b]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
         if (!(vmax > 0.0f)) vmax = 1.0f;
         v_mult = vmax / C::P8_SCALE;
+      }
+      // FP8 per-tile factors, prepared one tile ahead so that neither the
+      // descale loads nor the log / reciprocal sit between S and P: the
+      // loads for tile j+1 are issued when S(j) arrives, the factors are
+      // formed after P(j) has been handed over.
+      //   f_k:   q-block descale x k-block descale (multiplies the scale)
+      //   f_lpv: log2 of P~'s V-block factor 2^6 * s_Vj / max s_V
+      //   f_inv: that factor's reciprocal (undoes it in the row sum)
+      float f_k = 1.0f, f_lpv = 0.0f, f_inv = 1.0f;
+      float kd_next = 1.0f, vd_next = 1.0f;
+      auto fp8_factors = [&](float kd, float vd) {
+        f_k = qds * kd;
+        const float pv = C::P8_SCALE * (vd / vmax);
+        f_lpv = lg2(pv);
+        f_inv = 1.0f / pv;
+      };
+      if constexpr (ELEM == kE4M3) {
+        if (Jn > 0) fp8_factors(prm.k_ds[kv_blk], prm.v_ds[kv_blk]);
       }
       // one Q tile: consume o_ready completions up to (and including) the PV
       // of global iteration x on buffer x & 1 (they complete in order)
@@ -686,10 +707,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         }
         // scale of this tile (log2 units)
         float cj = prm.scale_log2;
-        float pv_fac = 1.0f;
         if constexpr (ELEM == kE4M3) {
-          cj *= qds * prm.k_ds[kv_blk + j];
-          pv_fac = C::P8_SCALE * (prm.v_ds[kv_blk + j] / vmax);
+          cj *= f_k;
+          if (j + 1 < Jn) {
+            kd_next = prm.k_ds[kv_blk + j + 1];
+            vd_next = prm.v_ds[kv_blk + j + 1];
+          }
         }
         const int col0 = j * kBN;
         const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > q0 + koff);
@@ -756,13 +779,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         // (causal diagonal, ragged tail) zero the masked p explicitly; every
         // other tile takes the select-free loop.
         const float2 cj2 = make_float2(cj, cj);
-        // FP8: the V-block factor p~ = p * pv_fac is folded into the exponent
-        // (2^(x - m + log2 pv_fac)); the row sum is rescaled once per tile
-        float lpv = 0.0f, inv_pv = 1.0f;
-        if constexpr (ELEM == kE4M3) {
-          lpv = lg2(pv_fac);
-          inv_pv = 1.0f / pv_fac;
-        }
+        // FP8: the V-block factor of p~ is folded into the exponent
+        // (2^(x - m + f_lpv)); the row sum is rescaled once per tile (f_inv)
+        const float lpv = f_lpv, inv_pv = f_inv;
         const float2 nm2 = make_float2(lpv - m_run, lpv - m_run);
         float2 acc[4];
 #pragma unroll
@@ -821,6 +840,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[buf][1]);
+        if constexpr (ELEM == kE4M3) {
+          if (j + 1 < Jn) fp8_factors(kd_next, vd_next);
+        }
       }
 
       // ---------------------------------------------------------- epilogue --
