@@ -147,6 +147,7 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   if ((st = encode_map(&L.k, k, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   if ((st = encode_map(&L.v, v, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.o = o;
+  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   L.prm.lse = lse;
   L.prm.err = err;
   L.prm.N = (int)Nq;
@@ -190,6 +191,7 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
   if ((st = encode_map(&L.k, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
   if ((st = encode_map(&L.v, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.o = o;
+  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   L.prm.lse = lse;
   L.prm.q_ds = q_descale;
   L.prm.k_ds = k_descale;

@@ -132,6 +132,7 @@ struct AttnParams {
   int nblk_k;           // ceil(Nk / 128): K/V descale blocks per head
   float scale_log2;     // scale * log2(e)
   int drop_pos;         // test hook: ring position CTA 0 never fills (-1: none)
+  int o_vec32;          // 1: o is 32-byte aligned (rows are stored 32 bytes at a time)
 };
 
 // Barriers in shared memory.
@@ -868,9 +869,16 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
               pk[i] = (ELEM == kFP16) ? pack_f16x2(a, b) : pack_bf16x2(a, b);
             }
             if (store) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+              // each lane writes its own row: whole 32-byte sectors when the
+              // output allows it (the C ABI only promises 16-byte alignment)
+              if (prm.o_vec32) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                for (int i = 0; i < 2; ++i) st_global_v8(orow + c0 * 2 + 32 * i, pk + 8 * i);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
             }
           }
           if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;

@@ -377,6 +377,14 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work;
 // each half rounds exactly like the scalar operation).
+// 32 contiguous bytes to global memory in one store (address 32-byte aligned):
+// a warp writing 32 rows then fills whole 32-byte sectors per instruction.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   uint64_t A, B, Cc, D;
   asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));

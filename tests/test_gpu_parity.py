@@ -170,3 +170,22 @@ def test_back_to_back_shapes(fa):
         causal = bool(rng.integers(0, 2))
         err = _run(fa, 1, 2, N, d, causal, seed=2000 + it)
         assert_bf16_parity(err, f"iter {it}: N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_output_alignment_16_not_32(fa, d):
+    # The C ABI promises O 16-byte alignment only; rows are stored 32 bytes
+    # at a time when O is 32-byte aligned and 16 bytes at a time otherwise.
+    # Both must write the same bytes.
+    B, H, N = 1, 3, 300
+    host, (q, k, v) = make_qkv(B, H, N, d, 4242, torch.bfloat16)
+    o_ref, l_ref = fa.fwd(q, k, v, causal=True)
+    n = B * H * N * d
+    buf = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device=q.device)
+    o_off = buf[8:8 + n].view(B, H, N, d)            # 16 bytes past a 256-byte boundary
+    assert o_off.data_ptr() % 16 == 0 and o_off.data_ptr() % 32 != 0
+    o2, l2 = fa.fwd(q, k, v, causal=True, out=o_off)
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    assert torch.equal(o2, o_ref) and torch.equal(l2, l_ref)
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all(), "wrote outside O"
