@@ -510,7 +510,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             const int pv_pos = pos;            // V_j
             const int k_pos = pos + C::SPT;    // K_{j+1}
             bool v_ready = false, k_ready = false;
-            for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok) break;
               if (j >= w.Jt[t]) continue;
               if (!v_ready) { ok = wait_tile(pv_pos); v_ready = true; if (!ok) break; }
               // P arrives in two halves of the key tile: the first half's
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     int sc = 0;               // two Q tiles: S handshakes consumed (this tile)
     int g = 0;                // one Q tile: running iteration count
     int oc = 0;               // units finished by this tile (o_full phases)
-    int o_seen[2] = {0, 0};   // one Q tile: o_ready completions consumed per buffer
+    int pv_seen = 0;          // one Q tile: PV completions consumed (global iteration order)
     bool ok = true;
 
     for (int rr = 0; ok; ++rr) {
@@ -671,12 +673,13 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       // one Q tile: consume o_ready completions up to (and including) the PV
       // of global iteration x on buffer x & 1 (they complete in order)
       auto consume_o = [&](int x) -> bool {
-        const int b = x & 1;
-        while (2 * o_seen[b] + b <= x) {
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait(&bars->o_ready[b], (uint32_t)(o_seen[b] & 1), abort_flag, prm.err)))
+        while (pv_seen <= x) {
+          // PV(pv_seen) ran on buffer pv_seen & 1, as that buffer's
+          // (pv_seen >> 1)-th completion (one counter, no indexed array)
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_ready[pv_seen & 1], (uint32_t)((pv_seen >> 1) & 1),
+                                                 abort_flag, prm.err)))
             return false;
-          ++o_seen[b];
+          ++pv_seen;
         }
         return true;
       };
