@@ -62,6 +62,17 @@ def hadamard_signs(d: int, seed: int = 4) -> np.ndarray:
     return np.where(rng.random(d) < 0.5, -1, 1).astype(np.int8)
 
 
+def rope_tables(N: int, d: int, base: float = 10000.0, offset: int = 0):
+    """Rotary-embedding angle tables, inputs of the quantiser: (cos, sin),
+    fp32 [N, d/2], for positions offset..offset+N-1 and frequencies
+    base^(-2i/d), i < d/2 (the usual choice; the pages fix none).  The
+    angles are formed in fp64 and rounded once."""
+    pos = np.arange(offset, offset + N, dtype=np.float64)[:, None]
+    freq = base ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)[None, :]
+    ang = pos * freq
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
 def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
     """Sorted distinct query rows: always 0, 127, 128, N-1 (when they exist),
     the rest uniform without replacement."""

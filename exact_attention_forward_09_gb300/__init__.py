@@ -20,12 +20,14 @@ from .build import LIB as _LIB_PATH
 __all__ = ["fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
            "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
+           "FA_ROPE_INTERLEAVED", "FA_ROPE_HALF",
            "QUANT_NOALLOC_MAX_BLOCKS"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 FA_ERR_SCRATCH_LIMIT = 5
 QUANT_NOALLOC_MAX_BLOCKS = 65536
 FA_DTYPE_BF16, FA_DTYPE_FP16 = 0, 1
+FA_ROPE_INTERLEAVED, FA_ROPE_HALF = 1, 2
 FP8_BLOCK_ROWS = 128
 
 
@@ -57,6 +59,8 @@ def _lib():
         lib.fa_fwd_fp8_gqa.restype = i32
         lib.fa_quant_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp]
         lib.fa_quant_fp8.restype = i32
+        lib.fa_quant_fp8_rope.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, i32, vp, i32, vp, vp]
+        lib.fa_quant_fp8_rope.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
         lib.fa_quant_fp8_per_tensor_noalloc.restype = i32
         lib.fa_status_string.argtypes = [i32]
@@ -207,10 +211,14 @@ def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_descale: tor
     return out, lse
 
 
-def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: torch.Tensor | None = None):
+def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: torch.Tensor | None = None,
+              rope=None):
     """fp32 [B, H, N, d] -> (E4M3 codes uint8 [B, H, N, d], descale fp32
     [B, H, ceil(N/128)]) via ``fa_quant_fp8``.  ``signs``: d entries of +-1
-    (host sequence / numpy / CPU tensor) for the Hadamard rotation, or None."""
+    (host sequence / numpy / CPU tensor) for the Hadamard rotation, or None.
+    ``rope``: None, or (cos, sin, layout) with cos / sin contiguous fp32 CUDA
+    tensors [N, d/2] and layout FA_ROPE_INTERLEAVED or FA_ROPE_HALF: the
+    rotary embedding is applied first, in the same pass (``fa_quant_fp8_rope``)."""
     if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 \
             or not x.is_contiguous():
         raise ValueError("x must be a contiguous fp32 [B, H, N, d] CUDA tensor")
@@ -229,9 +237,21 @@ def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: 
             workspace = torch.empty((1,), dtype=torch.float32, device=x.device)
         ws = workspace.data_ptr()
     with torch.cuda.device(x.device):
-        st = _lib().fa_quant_fp8(x.data_ptr(), x8.data_ptr(), ds.data_ptr(), B, H, N, d, sp,
-                                 int(bool(per_tensor)), ws, _stream(x))
-    _check(st, "fa_quant_fp8")
+        if rope is None:
+            st = _lib().fa_quant_fp8(x.data_ptr(), x8.data_ptr(), ds.data_ptr(), B, H, N, d, sp,
+                                     int(bool(per_tensor)), ws, _stream(x))
+            name = "fa_quant_fp8"
+        else:
+            cos, sin, layout = rope
+            for nm, t in (("cos", cos), ("sin", sin)):
+                if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 \
+                        or not t.is_contiguous() or tuple(t.shape) != (N, d // 2) or t.device != x.device:
+                    raise ValueError(f"rope {nm} must be a contiguous fp32 [N, d/2] tensor on x's device")
+            st = _lib().fa_quant_fp8_rope(x.data_ptr(), x8.data_ptr(), ds.data_ptr(), B, H, N, d,
+                                          cos.data_ptr(), sin.data_ptr(), int(layout), sp,
+                                          int(bool(per_tensor)), ws, _stream(x))
+            name = "fa_quant_fp8_rope"
+    _check(st, name)
     del keep
     return x8, ds
 

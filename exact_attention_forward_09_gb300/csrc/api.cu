@@ -218,12 +218,17 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
                         stream);
 }
 
-fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
-                       const int8_t* hadamard_signs, int per_tensor, float* workspace, cudaStream_t stream) {
+namespace {
+fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                     const float* rope_cos, const float* rope_sin, int rope_layout, const int8_t* hadamard_signs,
+                     int per_tensor, float* workspace, cudaStream_t stream) {
   if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (per_tensor != 0 && per_tensor != 1) return FA_ERR_INVALID_ARG;
+  if (rope_layout != 0 && rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (rope_layout != 0 && (!rope_cos || !rope_sin || ((uintptr_t)rope_cos & 3u) || ((uintptr_t)rope_sin & 3u)))
+    return FA_ERR_INVALID_ARG;
   if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x8) || ((uintptr_t)descale & 3u)) return FA_ERR_INVALID_ARG;
   if (per_tensor && (!workspace || ((uintptr_t)workspace & 3u))) return FA_ERR_INVALID_ARG;
@@ -257,8 +262,25 @@ fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int6
   L.d = (int)d;
   L.nblk = (int)((N + 127) / 128);
   L.per_tensor = per_tensor;
+  L.rope = rope_layout;
+  L.rope_cos = rope_cos;
+  L.rope_sin = rope_sin;
   L.stream = stream;
   return fa::launch_quant(L) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
+fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                       const int8_t* hadamard_signs, int per_tensor, float* workspace, cudaStream_t stream) {
+  return quant_impl(x, x8, descale, B, H, N, d, nullptr, nullptr, 0, hadamard_signs, per_tensor, workspace, stream);
+}
+
+fa_status fa_quant_fp8_rope(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                            const float* rope_cos, const float* rope_sin, int rope_layout,
+                            const int8_t* hadamard_signs, int per_tensor, float* workspace, cudaStream_t stream) {
+  if (rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
+  return quant_impl(x, x8, descale, B, H, N, d, rope_cos, rope_sin, rope_layout, hadamard_signs, per_tensor,
+                    workspace, stream);
 }
 
 const char* fa_status_string(fa_status status) {

@@ -5,6 +5,14 @@
 // "how incoherent processing flattens outliers"; E4M3 maximum 448 from the
 // wmrh.cn FlashAttention V3 article, sec. 3.3).
 //
+// Optionally each row first gets a rotary position embedding (the pages
+// let RoPE and the block-scale / Hadamard prep share one pass: same article,
+// sections "why block quantization beats a per-tensor scale" and "how
+// incoherent processing flattens outliers").  Pairs (a, b) of channels turn
+// by the row's angle: a' = a*cos - b*sin, b' = a*sin + b*cos, in fp32 with
+// each product rounded before the sum; the caller supplies the cos / sin
+// tables and picks the pairing, (2i, 2i+1) or (i, i + d/2).
+//
 // One CTA per (head, 128-row block).  The block's rows are contiguous in
 // memory, so one bulk copy (cp.async.bulk, completion on an mbarrier) brings
 // the whole block into shared memory; then one warp per row at a time.  Each lane
@@ -53,6 +61,36 @@ __device__ __forceinline__ void rotate_row(float (&v)[D / 32], int lane, const S
   }
 }
 
+// Rotary embedding of one row (lane holds channels lane*E .. lane*E+E-1);
+// c, s: this row's cos / sin tables (d/2 entries each).
+template <int D>
+__device__ __forceinline__ void rope_row(float (&v)[D / 32], int lane, const float* __restrict__ c,
+                                         const float* __restrict__ s, int mode) {
+  constexpr int E = D / 32;
+  if (mode == 1) {
+    // pairs (2i, 2i+1), both in this lane
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const int i = (lane * E + e) >> 1;
+      const float cs = c[i], sn = s[i];
+      const float a = v[e], b = v[e + 1];
+      v[e] = __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn));
+      v[e + 1] = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
+    }
+  } else if (mode == 2) {
+    // pairs (i, i + D/2): lane L < 16 holds i = L*E + e, lane L + 16 its partner
+    const bool first = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = (lane & 15) * E + e;
+      const float cs = c[i], sn = s[i];
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], 16);
+      const float a = first ? v[e] : o, b = first ? o : v[e];
+      v[e] = first ? __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)) : __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -66,7 +104,8 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
                                                          float* __restrict__ descale, int N, int nblk,
                                                          SignBits sg, int rot, float rinv,
-                                                         float* __restrict__ amax_ws, int* err) {
+                                                         const float* __restrict__ rcos, const float* __restrict__ rsin,
+                                                         int rope, float* __restrict__ amax_ws, int* err) {
   constexpr int E = D / 32;
   constexpr int ROWS = 128;
   extern __shared__ __align__(128) float ys[];  // [ROWS][D]: the block, rotated in place
@@ -117,11 +156,12 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
         v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
     }
+    if (rope) rope_row<D>(v, lane, rcos + (size_t)(r0 + r) * (D / 2), rsin + (size_t)(r0 + r) * (D / 2), rope);
     rotate_row<D>(v, lane, sg, rot != 0);
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
     if constexpr (MODE == 0) {
-      if (rot) {
+      if (rot || rope) {
 #pragma unroll
         for (int e = 0; e < E; ++e) yrow[e] = v[e];
       }
@@ -212,7 +252,7 @@ static cudaError_t launch_mode(const QuantLaunch& L, float* ws) {
   if (e != cudaSuccess) return e;
   const dim3 grid(L.nblk, L.BH, 1);
   quant_e4m3_kernel<D, MODE><<<grid, 256, 128u * D * sizeof(float), L.stream>>>(
-      L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv, ws, L.err);
+      L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv, L.rope_cos, L.rope_sin, L.rope, ws, L.err);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,12 @@ struct QuantLaunch {
   int rot;
   float rinv;       // 1/sqrt(d) as fp32 when rotating, else 1
   SignBits signs;
+  // rotary position embedding applied to each row before the rotation:
+  // 0 off, 1 pairs (2i, 2i+1), 2 pairs (i, i + d/2); angle tables
+  // [N, d/2] fp32 (row n uses row n of each table)
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope;
   cudaStream_t stream;
 };
 

@@ -159,6 +159,35 @@ fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
                        cudaStream_t stream);
 
 /*
+ * fa_quant_fp8_rope -- fa_quant_fp8 with a rotary position embedding applied
+ * to every row first, in the same pass ("FlashAttention-3: async pipelines on
+ * Hopper", sections "why block quantization beats a per-tensor scale" and
+ * "how incoherent processing flattens outliers": the block scales and the
+ * Hadamard rotation can share one pass with a preceding RoPE).  The pages fix
+ * no RoPE convention, so the angles come from the caller and both usual
+ * channel pairings are offered:
+ *   FA_ROPE_INTERLEAVED  pairs (2i, 2i+1), i < d/2
+ *   FA_ROPE_HALF         pairs (i, i + d/2), i < d/2
+ * Pair (a, b) of row n becomes (a*c - b*s, a*s + b*c) with c = rope_cos[n][i],
+ * s = rope_sin[n][i], in fp32 with each product rounded before the sum; then
+ * the optional rotation and the quantisation proceed as in fa_quant_fp8.
+ *   rope_cos, rope_sin  [N, d/2] fp32 (device, read only, 4-byte aligned),
+ *                       shared by every (b, h): row n is position n of each
+ *                       sequence (offset positions by offsetting the tables)
+ *   rope_layout         FA_ROPE_INTERLEAVED or FA_ROPE_HALF
+ *   other arguments as for fa_quant_fp8.
+ * Errors: FA_ERR_INVALID_ARG for a null or misaligned table or an unknown
+ * layout, otherwise as fa_quant_fp8.
+ */
+#define FA_ROPE_INTERLEAVED 1
+#define FA_ROPE_HALF 2
+fa_status fa_quant_fp8_rope(const float* x, void* x8, float* descale,
+                            int64_t B, int64_t H, int64_t N, int64_t d,
+                            const float* rope_cos, const float* rope_sin, int rope_layout,
+                            const int8_t* hadamard_signs, int per_tensor, float* workspace,
+                            cudaStream_t stream);
+
+/*
  * fa_quant_fp8_per_tensor_noalloc -- the per-tensor mode of fa_quant_fp8
  * (per_tensor = 1) for callers that cannot allocate device memory.  The
  * pages have no counterpart; it exists for the library's users.

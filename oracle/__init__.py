@@ -25,6 +25,13 @@ Functions and the passages they follow:
   flattens outliers" of "FlashAttention-3: async pipelines on Hopper"; the
   constant 448 from the wmrh.cn article sec. 3.3).  fp32 arithmetic, as the
   code decision is taken in the kernel's precision.
+  With ``rope`` given, each row first gets a rotary position embedding in
+  the same fp32 arithmetic as the kernel (the pages let RoPE share that
+  pass, same two sections; they give no RoPE formula, so it is the usual
+  planar rotation of channel pairs by the caller's angles).
+* :func:`rope` -- the same rotary embedding in fp64, written as the
+  rotation it is (per pair: [[cos, -sin], [sin, cos]] applied to (a, b)),
+  for the attention-level checks.
 * :func:`e4m3_encode` / :func:`e4m3_decode` -- the E4M3 format.
 * :func:`hadamard_signs` is NOT here: random signs are inputs, drawn by
   ``attn_inputs``.
@@ -52,7 +59,7 @@ def _lib():
         lib.oracle_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                         i32, f64, vp, i64, i32]
         lib.oracle_attn_fwd.restype = i32
-        lib.oracle_quant_e4m3.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32]
+        lib.oracle_quant_e4m3.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp, i32]
         lib.oracle_quant_e4m3.restype = i32
         lib.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
         lib.oracle_e4m3_encode_array.restype = None
@@ -202,11 +209,39 @@ def fwht_f32(x, signs=None) -> np.ndarray:
     return out.reshape(x.shape)
 
 
-def quant_e4m3(x, signs=None, per_tensor: bool = False, block_rows: int = 128):
+ROPE_INTERLEAVED, ROPE_HALF = 1, 2   # channel pairs (2i, 2i+1) / (i, i + d/2)
+
+
+def rope(x, cos, sin, layout) -> np.ndarray:
+    """Rotary embedding of x [..., N, d] in fp64: for every row n and pair
+    index i < d/2, the channel pair (a, b) -- (2i, 2i+1) for ROPE_INTERLEAVED,
+    (i, i + d/2) for ROPE_HALF -- is multiplied by the 2x2 rotation
+    [[cos[n, i], -sin[n, i]], [sin[n, i], cos[n, i]]]."""
+    x = _np(x, np.float64)
+    cos = _np(cos, np.float64)
+    sin = _np(sin, np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    if layout == ROPE_INTERLEAVED:
+        ia, ib = np.arange(half) * 2, np.arange(half) * 2 + 1
+    elif layout == ROPE_HALF:
+        ia, ib = np.arange(half), np.arange(half) + half
+    else:
+        raise ValueError("unknown rope layout")
+    a, b = x[..., ia], x[..., ib]
+    out = np.empty_like(x)
+    out[..., ia] = cos * a - sin * b
+    out[..., ib] = sin * a + cos * b
+    return out
+
+
+def quant_e4m3(x, signs=None, per_tensor: bool = False, block_rows: int = 128, rope=None):
     """Quantise x [B, H, N, d] fp32 to E4M3 codes + descale [B, H, ceil(N/block_rows)].
 
     dequantised value = decode(code) * descale; with rotation on (signs given)
-    that approximates x diag(signs) H_d / sqrt(d).
+    that approximates x diag(signs) H_d / sqrt(d).  ``rope``: None or
+    (cos, sin, layout) with fp32 tables [N, d/2]: the rotary embedding is
+    applied to every row first, in fp32.
     """
     x = _np(x, np.float32)
     B, H, N, d = x.shape
@@ -217,9 +252,20 @@ def quant_e4m3(x, signs=None, per_tensor: bool = False, block_rows: int = 128):
     if signs is not None:
         sg = np.ascontiguousarray(np.asarray(signs, dtype=np.int8))
         assert sg.shape == (d,)
+    cos_ptr, sin_ptr, layout = None, None, 0
+    keep = None
+    if rope is not None:
+        tcos, tsin, layout = rope
+        tcos = np.ascontiguousarray(_np(tcos, np.float32))
+        tsin = np.ascontiguousarray(_np(tsin, np.float32))
+        assert tcos.shape == (N, d // 2) and tsin.shape == (N, d // 2)
+        keep = (tcos, tsin)
+        cos_ptr, sin_ptr = tcos.ctypes.data, tsin.ctypes.data
     rc = _lib().oracle_quant_e4m3(x.ctypes.data, codes.ctypes.data, descale.ctypes.data,
                                   B * H, N, d, block_rows,
-                                  sg.ctypes.data if sg is not None else None, int(bool(per_tensor)))
+                                  sg.ctypes.data if sg is not None else None, int(bool(per_tensor)),
+                                  cos_ptr, sin_ptr, int(layout))
+    del keep
     if rc != 0:
         raise RuntimeError("oracle_quant_e4m3 failed")
     return codes, descale

@@ -42,6 +42,14 @@
  *                    carried in the stored descale, codes are
  *                    round-to-nearest-even of (y / s) with saturation at 448.
  *
+ *                    With a rotary position embedding requested, each row is
+ *                    first turned pairwise by the caller's angles (the pages
+ *                    let RoPE share the quantisation pass, same sections; they
+ *                    give no RoPE formula, so it is the usual planar rotation
+ *                    of channel pairs (2i, 2i+1) or (i, i + d/2):
+ *                    a' = a cos - b sin, b' = a sin + b cos), in fp32 with each
+ *                    product rounded before the sum, like the kernel.
+ *
  *  oracle_e4m3_encode / oracle_e4m3_decode
  *                    The E4M3 format from its definition: 1 sign bit, 4
  *                    exponent bits (bias 7), 3 mantissa bits, subnormals at
@@ -206,6 +214,21 @@ void oracle_fwht_f32(const float* x, float* y, int64_t d, const int8_t* signs)
     }
 }
 
+/* Rotary embedding of one row: pairs (2i, 2i+1) (layout 1) or (i, i + d/2)
+ * (layout 2) turned by angle i of the row: c[i] = cos, s[i] = sin, fp32. */
+void oracle_rope_f32(const float* x, float* y, int64_t d, const float* c, const float* s, int layout)
+{
+    const int64_t half = d / 2;
+    for (int64_t i = 0; i < half; ++i) {
+        const int64_t ia = (layout == 1) ? 2 * i : i;
+        const int64_t ib = (layout == 1) ? 2 * i + 1 : i + half;
+        const float a = x[ia], b = x[ib];
+        const float ac = a * c[i], bs = b * s[i], as = a * s[i], bc = b * c[i];
+        y[ia] = ac - bs;
+        y[ib] = as + bc;
+    }
+}
+
 /*
  * x        [BH, N, d] fp32
  * codes    [BH, N, d] e4m3 codes
@@ -213,21 +236,35 @@ void oracle_fwht_f32(const float* x, float* y, int64_t d, const int8_t* signs)
  * signs    d entries of +-1 (rotation on), or NULL (rotation off); d must then
  *          be a power of two.
  * per_tensor: one scale over the whole tensor instead of one per block.
+ * rope_layout: 0 none, else 1 or 2 (see oracle_rope_f32), with rope_cos /
+ *          rope_sin [N, d/2]: row n of every (b,h) uses row n of the tables.
  */
 int oracle_quant_e4m3(const float* x, uint8_t* codes, float* descale,
                       int64_t BH, int64_t N, int64_t d, int64_t block_rows,
-                      const int8_t* signs, int per_tensor)
+                      const int8_t* signs, int per_tensor,
+                      const float* rope_cos, const float* rope_sin, int rope_layout)
 {
     if (BH < 0 || N < 0 || d <= 0 || block_rows <= 0) return -1;
     if (signs && (d & (d - 1)) != 0) return -1;
+    if (rope_layout && (rope_layout != 1 && rope_layout != 2)) return -1;
+    if (rope_layout && (!rope_cos || !rope_sin || (d & 1))) return -1;
     const int64_t nblk = (N + block_rows - 1) / block_rows;
     const int64_t n = BH * N * d;
     float* y = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
     if (!y) return -1;
+    float* t = (float*)malloc(sizeof(float) * (size_t)d);
+    if (!t) { free(y); return -1; }
     for (int64_t r = 0; r < BH * N; ++r) {
-        if (signs) oracle_fwht_f32(x + r * d, y + r * d, d, signs);
-        else memcpy(y + r * d, x + r * d, sizeof(float) * (size_t)d);
+        const float* xr = x + r * d;
+        if (rope_layout) {
+            const int64_t n = r % N;
+            oracle_rope_f32(xr, t, d, rope_cos + n * (d / 2), rope_sin + n * (d / 2), rope_layout);
+            xr = t;
+        }
+        if (signs) oracle_fwht_f32(xr, y + r * d, d, signs);
+        else memcpy(y + r * d, xr, sizeof(float) * (size_t)d);
     }
+    free(t);
     const float rinv = signs ? (float)(1.0 / sqrt((double)d)) : 1.0f;
 
     float gmax = 0.0f;

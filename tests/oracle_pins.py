@@ -19,7 +19,11 @@ Sources of truth used here:
   * the tiled online recurrence equals the two-pass result (wmrh.cn article,
     sec. 2.1: the tiled result is the same as the global one);
   * torch.float8_e4m3fn for the E4M3 codec, and 448 as its maximum (wmrh.cn
-    article, sec. 3.3).
+    article, sec. 3.3);
+  * for the rotary embedding (which the pages only place before the
+    quantisation pass): complex multiplication of each channel pair by
+    e^{i theta} (numpy complex arithmetic), the permutation relating the two
+    channel pairings, and the relative-position property of the scores.
 """
 from __future__ import annotations
 
@@ -255,6 +259,89 @@ def pin_quantiser(oracle):
                 assert oracle.e4m3_decode(codes & 0x7F).max() == 448.0
 
 
+def _rope_pairs(d, layout):
+    half = d // 2
+    if layout == 1:
+        return np.arange(half) * 2, np.arange(half) * 2 + 1
+    return np.arange(half), np.arange(half) + half
+
+
+def pin_rope_complex(oracle):
+    # a pair (a, b) read as a + ib, times e^{i theta}; a quarter turn maps
+    # (1, 0) to (0, 1)
+    one = np.zeros((1, 4))
+    one[0, 0] = 1.0
+    s90 = np.array([[1.0, 0.0]])
+    y = oracle.rope(one, np.cos(np.pi / 2 * s90), np.sin(np.pi / 2 * s90), 1)
+    assert np.allclose(y, [[0.0, 1.0, 0.0, 0.0]], atol=1e-15), y
+    for layout in (1, 2):
+        for d in (8, 64, 128):
+            x = gen.normal((2, 3, 17, d), 50 + d).astype(np.float64)
+            theta = gen.normal((17, d // 2), 51 + d).astype(np.float64) * 3.0
+            y = oracle.rope(x, np.cos(theta), np.sin(theta), layout)
+            ia, ib = _rope_pairs(d, layout)
+            z = (x[..., ia] + 1j * x[..., ib]) * np.exp(1j * theta)
+            assert np.allclose(y[..., ia], z.real, atol=1e-13) and np.allclose(y[..., ib], z.imag, atol=1e-13)
+
+
+def pin_rope_layouts(oracle):
+    # the half-split pairing is the interleaved one after moving channel i to
+    # 2i and channel i + d/2 to 2i + 1
+    d = 64
+    x = gen.normal((1, 2, 9, d), 60).astype(np.float64)
+    cos, sin = gen.rope_tables(9, d)
+    perm = np.empty(d, dtype=np.int64)
+    perm[0::2] = np.arange(d // 2)
+    perm[1::2] = np.arange(d // 2) + d // 2
+    inter = oracle.rope(x[..., perm], cos, sin, 1)
+    half = oracle.rope(x, cos, sin, 2)
+    assert np.allclose(half[..., perm], inter, atol=1e-14)
+
+
+def pin_rope_relative_position(oracle):
+    # with angles n * f_i, the score of positions (m, n) depends on m - n only
+    d = 128
+    q = gen.normal((1, 1, 1, d), 61).astype(np.float64)
+    k = gen.normal((1, 1, 1, d), 62).astype(np.float64)
+    freq = 10000.0 ** (-2.0 * np.arange(d // 2) / d)
+    for layout in (1, 2):
+        def at(x, pos):
+            ang = (np.array([[pos]], dtype=np.float64) * freq[None, :])
+            return oracle.rope(x, np.cos(ang), np.sin(ang), layout)[0, 0, 0]
+        for (m, n, t) in ((5, 3, 7), (100, 0, 900), (17, 40, 3)):
+            assert abs(at(q, m) @ at(k, n) - at(q, m + t) @ at(k, n + t)) <= 1e-11, (layout, m, n, t)
+
+
+def pin_rope_quantiser(oracle):
+    rows = _golden()["quant_block_rows"]["value"]
+    B, H, N, d = 1, 2, 200, 64
+    x = gen.outliers((B, H, N, d), 63)
+    signs = gen.hadamard_signs(d, 64)
+    # identity angles change nothing, bit for bit
+    ones = np.ones((N, d // 2), dtype=np.float32)
+    zeros = np.zeros((N, d // 2), dtype=np.float32)
+    for sg in (None, signs):
+        c0, s0 = oracle.quant_e4m3(x, signs=sg, block_rows=rows)
+        for layout in (1, 2):
+            c1, s1 = oracle.quant_e4m3(x, signs=sg, block_rows=rows, rope=(ones, zeros, layout))
+            assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
+    # real angles: dequantised values within half an E4M3 step of the fp64
+    # rotary embedding (and rotation) of x
+    cos, sin = gen.rope_tables(N, d, offset=3)
+    for layout in (1, 2):
+        for sg in (None, signs):
+            codes, ds = oracle.quant_e4m3(x, signs=sg, block_rows=rows, rope=(cos, sin, layout))
+            target = oracle.rope(x, cos, sin, layout)
+            if sg is not None:
+                target = oracle.rotate(target, sg)
+            deq = oracle.dequant_e4m3(codes, ds, block_rows=rows)
+            for r0 in range(0, N, rows):
+                tb = target[:, :, r0:r0 + rows]
+                s = ds[:, :, r0 // rows][..., None, None]
+                tol = np.maximum(np.abs(tb) * 2.0 ** -4, 2.0 ** -10 * s) * (1 + 1e-4) + 1e-5 * np.abs(tb).max()
+                assert np.all(np.abs(deq[:, :, r0:r0 + rows] - tb) <= tol), (layout, sg is None, r0)
+
+
 def pin_flop_convention(oracle):
     g = _golden()["matmul_flops_per_exp_d128"]["value"]
     B, H, N, d = 1, 1, 1024, 128
@@ -266,4 +353,5 @@ ALL_PINS = [
     pin_library_cross_check, pin_zero_query, pin_causal_row0, pin_special_cases,
     pin_rotation_invariance, pin_online_recurrence, pin_row_subset,
     pin_e4m3_decode, pin_e4m3_encode, pin_fwht, pin_quantiser, pin_flop_convention,
+    pin_rope_complex, pin_rope_layouts, pin_rope_relative_position, pin_rope_quantiser,
 ]

@@ -84,6 +84,17 @@ def test_host_argument_checks(fa_lib):
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 1, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 3, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8(None, None, None, 1, 0, 1, 128, None, 0, None, None) == fa.FA_OK
+    # quantiser with rotary embedding: a known layout and both tables are required
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 0, None, 0, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 3, None, 0, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, None, p, fa.FA_ROPE_HALF, None, 0, None,
+                                    None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p + 2, fa.FA_ROPE_INTERLEAVED, None, 0, None,
+                                    None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 100, p, p, fa.FA_ROPE_HALF, None, 0, None,
+                                    None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_quant_fp8_rope(None, None, None, 0, 1, 1, 128, None, None, fa.FA_ROPE_HALF, None, 0, None,
+                                    None) == fa.FA_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

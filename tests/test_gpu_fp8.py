@@ -114,3 +114,47 @@ def test_block_hadamard_beats_per_tensor(fa):
         res[name] = _fp8_case(fa, B, H, N, d, False, rot=rot, per_tensor=pt, seed=3, rows=rows)
     assert res["block_hadamard"]["rmse_exact"] < res["per_tensor"]["rmse_exact"], res
     assert res["block"]["rmse_exact"] <= res["per_tensor"]["rmse_exact"] * 1.05, res
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("rot", [False, True])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quant_rope_bit_exact(fa, d, layout, rot, per_tensor):
+    # rotary embedding fused into the quantisation pass: codes and descales
+    # equal the oracle's (same fp32 angle tables), for both channel pairings
+    N = 300                                              # ragged last block
+    x = gen.outliers((2, 3, N, d), 70 + d + layout)
+    cos, sin = gen.rope_tables(N, d, offset=5)
+    signs = gen.hadamard_signs(d, 4) if rot else None
+    codes_ref, ds_ref = oracle.quant_e4m3(x, signs=signs, per_tensor=per_tensor, rope=(cos, sin, layout))
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs, per_tensor=per_tensor,
+                             rope=(torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(), layout))
+    fa.check_device_error()
+    mism = int((codes.cpu().numpy() != codes_ref).sum())
+    assert mism == 0, f"{mism} E4M3 codes differ from the oracle quantiser"
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_fwd_fp8_with_rope(fa, layout):
+    # Q and K get the rotary embedding (and the Hadamard rotation) in the
+    # quantiser; the attention then matches the fp64 oracle on the embedded,
+    # unquantised inputs within the FP8 tolerance
+    B, H, N, d = 2, 4, 700, 128
+    q, k, v = gen.qkv_outliers((B, H, N, d), 71 + layout)
+    cos, sin = gen.rope_tables(N, d)
+    signs = gen.hadamard_signs(d, 4)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    rope = (dev(cos), dev(sin), layout)
+    qc, qs = fa.quant_fp8(dev(q), signs=signs, rope=rope)
+    kc, ks = fa.quant_fp8(dev(k), signs=signs, rope=rope)
+    vc, vs = fa.quant_fp8(dev(v))
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = fa.fwd_fp8(qc, kc, vc, qs, ks, vs, causal=causal, scale=scale)
+        fa.check_device_error()
+        o_ex, l_ex = oracle.attn_fwd(oracle.rope(q, cos, sin, layout), oracle.rope(k, cos, sin, layout), v,
+                                     causal=causal, scale=scale)
+        rmse = float(np.sqrt(((o.float().cpu().numpy() - o_ex) ** 2).mean()))
+        assert np.isfinite(rmse) and rmse <= FP8_O_RMSE, (causal, rmse)

@@ -29,6 +29,10 @@ MUTANTS = {
     "fwht_sign": ("y[c + h] = a - b;", "y[c + h] = b - a;"),
     "signs_ignored": ("(signs && signs[c] < 0) ? -x[c] : x[c]", "x[c]"),
     "rotation_norm_missing": ("(float)(1.0 / sqrt((double)d))", "1.0f"),
+    "rope_sign": ("y[ia] = ac - bs;", "y[ia] = ac + bs;"),
+    "rope_pairing": ("const int64_t ib = (layout == 1) ? 2 * i + 1 : i + half;",
+                     "const int64_t ib = (layout == 1) ? 2 * i + 1 : half - 1 - i;"),
+    "rope_position": ("const int64_t n = r % N;", "const int64_t n = r / N;"),
 }
 
 
