@@ -298,10 +298,18 @@ def run_extra(args, device):
         qfn = lambda: fa.quant_fp8(x[0], signs=signs)
         qms = _time_launches(qfn, 5, device, flush)
         qbytes = x[0].numel() * 5  # 4 B read + 1 B written per element
+        # the same quantisation with the rotary embedding fused in (angle
+        # tables [N, d/2] cos + sin, shared by every head: 4 B each per pair)
+        cos, sin = (torch.from_numpy(t).to(device) for t in gen.rope_tables(N, 128))
+        rfn = lambda: fa.quant_fp8(x[0], signs=signs, rope=(cos, sin, fa.FA_ROPE_HALF))
+        rms = _time_launches(rfn, 5, device, flush)
+        rbytes = qbytes + (cos.numel() + sin.numel()) * 4
         out[f"fp8_N{N}_d128"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
                                  "frac_of_fp8_peak": round(tf / fp8_peak, 3),
                                  "quant_ms_per_tensor": round(qms, 4),
-                                 "quant_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1)}
+                                 "quant_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1),
+                                 "quant_rope_ms_per_tensor": round(rms, 4),
+                                 "quant_rope_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1)}
     out["fp8_peak_note"] = "FP8 peak = measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"
     return out
 
