@@ -17,7 +17,7 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
+__all__ = ["fwd_splitkv", "splitkv_workspace_bytes", "fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
            "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
            "FA_ROPE_INTERLEAVED", "FA_ROPE_HALF",
@@ -59,6 +59,11 @@ def _lib():
         lib.fa_fwd_fp8_gqa.restype = i32
         lib.fa_quant_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp]
         lib.fa_quant_fp8.restype = i32
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32, i32, vp,
+                                       ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = i32
+        lib.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_splitkv_workspace_bytes.restype = i32
         lib.fa_quant_fp8_rope.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, i32, vp, i32, vp, vp]
         lib.fa_quant_fp8_rope.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
@@ -118,6 +123,44 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         st = _lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                            B, H, N, d, int(bool(causal)), float(scale), dt, _stream(q))
     _check(st, "fa_fwd")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    """Device workspace (bytes) ``fwd_splitkv`` needs on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(_lib().fa_splitkv_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, int(num_splits), ctypes.byref(n)),
+           "fa_splitkv_workspace_bytes")
+    return int(n.value)
+
+
+def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                scale: float | None = None, num_splits: int = 0, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Split-KV forward for decode-like shapes (``fa_fwd_splitkv``): q [B, Hq,
+    Nq, d], k/v [B, Hkv, Nk, d]; the query heads of a key/value group are
+    packed together and the keys split into ``num_splits`` runs (0: chosen
+    for the device).  Returns (O [B, Hq, Nq, d], LSE [B, Hq, Nq])."""
+    _check_gqa(q, k, v, (torch.bfloat16, torch.float16))
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    dt = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    with torch.cuda.device(q.device):
+        need = splitkv_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+        wp = workspace.data_ptr() if workspace is not None else None
+        wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        st = _lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), dt, int(num_splits),
+                                   wp, wb, _stream(q))
+    _check(st, "fa_fwd_splitkv")
     return out, lse
 
 

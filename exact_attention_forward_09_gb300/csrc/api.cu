@@ -14,6 +14,7 @@
 
 #include "fa.h"
 #include "attn_fwd.cuh"
+#include "splitkv.h"
 #include "quant_fp8.h"
 
 namespace fa {
@@ -123,9 +124,119 @@ fa_status dispatch(const fa::AttnLaunch& L, int64_t d, int causal) {
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Split-KV plan: the query heads of a key/value group are packed into one
+// head of g * Nq rows (contiguous in [B, Hq, Nq, d]), and each row's key
+// tiles are cut into S runs of T tiles, S chosen (when 0 is asked) to give
+// about two units per SM.  Workspace: partial O [S][B*Hkv][g*Nq][d] fp32,
+// then partial LSE [S][B*Hkv][g*Nq] fp32 (256-byte aligned start).
+struct SplitPlan {
+  int64_t BHp, Np;
+  int S, T;
+  size_t o_bytes, ws_bytes;
+};
+
+fa_status splitkv_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int num_splits,
+                       int sms, SplitPlan* p) {
+  p->BHp = B * Hkv;
+  p->Np = (Hq / Hkv) * Nq;
+  if (p->Np > 0x7fffffffLL - 256) return FA_ERR_UNSUPPORTED;
+  const int64_t rows_per_unit = d <= 128 ? 256 : 128;
+  const int64_t base = p->BHp * ((p->Np + rows_per_unit - 1) / rows_per_unit);
+  const int64_t nkv = (Nk + 127) / 128;
+  int64_t S = num_splits > 0 ? num_splits : (2 * (int64_t)sms + base - 1) / base;
+  if (S > nkv) S = nkv;
+  if (S > 1024) S = 1024;
+  if (S < 1) S = 1;
+  const int64_t T = (nkv + S - 1) / S;
+  S = (nkv + T - 1) / T;  // no empty run
+  if (base * S > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  p->S = (int)S;
+  p->T = (int)T;
+  p->o_bytes = S > 1 ? (((size_t)S * p->BHp * p->Np * d * 4 + 255) / 256) * 256 : 0;
+  p->ws_bytes = S > 1 ? p->o_bytes + (size_t)S * p->BHp * p->Np * 4 : 0;
+  return FA_OK;
+}
+
+int device_sm_count(int dev) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  return sms;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                                     int num_splits, size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nk < 0 || d < 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0 || Nk == 0) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  SplitPlan p;
+  const fa_status st = splitkv_plan(B, Hq, Hkv, Nq, Nk, d, num_splits, device_sm_count(dev), &p);
+  if (st == FA_OK) *bytes = p.ws_bytes;
+  return st;
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t Hq,
+                         int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, int dtype,
+                         int num_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  bool empty = false;
+  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, &empty);
+  if (st != FA_OK || empty) return st;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  SplitPlan p;
+  if ((st = splitkv_plan(B, Hq, Hkv, Nq, Nk, d, num_splits, device_sm_count(dev), &p)) != FA_OK) return st;
+  if (p.S > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < p.ws_bytes))
+    return FA_ERR_INVALID_ARG;
+
+  fa::AttnLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const CUtensorMapDataType dt =
+      dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // packed: head (b, kv head) with g * Nq rows; K/V heads map one to one
+  if ((st = encode_map(&L.q, q, dt, 2, p.BHp, p.Np, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k, dt, 2, p.BHp, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v, dt, 2, p.BHp, Nk, d)) != FA_OK) return st;
+  L.prm.o = o;
+  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  L.prm.lse = lse;
+  L.prm.err = err;
+  L.prm.N = (int)p.Np;
+  L.prm.Nk = (int)Nk;
+  L.prm.Hq = 1;
+  L.prm.Hkv = 1;
+  L.prm.nblk = (int)((p.Np + 127) / 128);
+  L.prm.nblk_k = (int)((Nk + 127) / 128);
+  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  L.BH = (int)p.BHp;
+  L.prm.BH = L.BH;
+  L.prm.drop_pos = -1;
+  L.prm.q_period = (int)Nq;
+  L.prm.splits = p.S;
+  L.prm.split_tiles = p.T;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = p.S > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.o_bytes) : nullptr;
+  L.prm.o_part = p.S > 1 ? o_part : nullptr;
+  L.prm.lse_part = lse_part;
+  L.stream = stream;
+  st = dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
+  if (st != FA_OK || p.S == 1) return st;
+  return fa::launch_splitkv_combine(o_part, lse_part, o, lse, p.S, (long long)(p.BHp * p.Np), (int)d,
+                                    dtype == FA_DTYPE_FP16, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
 
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t Hq,
                      int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, int dtype,
@@ -160,6 +271,9 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   L.BH = (int)(B * Hq);
   L.prm.BH = L.BH;
   L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
+  L.prm.q_period = (int)Nq;
+  L.prm.splits = 1;
+  L.prm.split_tiles = (int)((Nk + 127) / 128);
   L.stream = stream;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
 }
@@ -207,6 +321,9 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
   L.BH = (int)(B * Hq);
   L.prm.BH = L.BH;
   L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
+  L.prm.q_period = (int)Nq;
+  L.prm.splits = 1;
+  L.prm.split_tiles = (int)((Nk + 127) / 128);
   L.stream = stream;
   return dispatch<fa::kE4M3>(L, d, causal);
 }

@@ -133,6 +133,18 @@ struct AttnParams {
   float scale_log2;     // scale * log2(e)
   int drop_pos;         // test hook: ring position CTA 0 never fills (-1: none)
   int o_vec32;          // 1: o is 32-byte aligned (rows are stored 32 bytes at a time)
+  // Row r of a head sits at sequence position r % q_period (q_period = N,
+  // or Nq when the query heads of a key/value group are packed into one
+  // head of g * Nq rows); causal masks use that position.
+  int q_period;
+  // Split-KV: splits > 1 divides each row's key tiles into runs of
+  // split_tiles; a unit then covers one run and writes O normalised over its
+  // keys (fp32) to o_part[split][bh][row][d] and its LSE to
+  // lse_part[split][bh][row], for a separate combine.
+  int splits;
+  int split_tiles;
+  float* o_part;
+  float* lse_part;
 };
 
 // Barriers in shared memory.
@@ -151,7 +163,7 @@ struct Bars {
   uint64_t unit_full[2];   // queue of next-unit ids (load warp -> others)
   uint64_t unit_empty[2];
   alignas(16) uint32_t clc_resp[4];
-  alignas(16) int4 unit_q[2];  // decoded units: {bh (-1: none), kvh, q_base, Jt0 | Jt1 << 16}
+  alignas(16) int unit_q[2][8];  // decoded units: {bh (-1: none), kvh, q_base, Jt0 | Jt1 << 16, split, tb}
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -189,11 +201,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int N = prm.N;                     // query rows
   const int Nk = prm.Nk;                   // keys
-  const int koff = Nk - N;                 // causal diagonal offset
   const int nkv = (Nk + kBN - 1) / kBN;
   const int qgroup = prm.Hq / prm.Hkv;     // query heads per key/value head
   const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  const int U = prm.BH * n_groups;  // work units: (head, group of NQT Q tiles)
+  const int S = prm.splits;         // key splits (1: none)
+  const int U = prm.BH * n_groups * S;  // work units: (head, group of NQT Q tiles, key split)
   const int G = (int)gridDim.x;
 
   // Work units are launched one CTA each, in this order: non-causal,
@@ -210,23 +222,42 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     int bh, kvh, q_base, J;
     int Jt[2];
     bool active[2];
+    int split, tb;  // key split and its first key tile
   };
   auto decode = [&](int u) -> Unit {
     Unit w;
     int group;
+    w.split = u % S;
+    const int v = u / S;
     if constexpr (CAUSAL) {
-      group = n_groups - 1 - u / prm.BH;
-      w.bh = u % prm.BH;
+      group = n_groups - 1 - v / prm.BH;
+      w.bh = v % prm.BH;
     } else {
-      w.bh = u / n_groups;
-      group = u % n_groups;
+      w.bh = v / n_groups;
+      group = v % n_groups;
     }
     w.q_base = group * (C::NQT * kBM);
+    w.tb = w.split * prm.split_tiles;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int q0 = w.q_base + t * kBM;
       w.active[t] = (t < C::NQT) && (q0 < N);
-      w.Jt[t] = w.active[t] ? kv_tiles_for<CAUSAL>(q0, nkv, koff) : 0;
+      int tiles = 0;
+      if (w.active[t]) {
+        if constexpr (CAUSAL) {
+          // last key any row of the tile sees, from the largest position
+          // among its rows (rows of several packed heads: the last one)
+          const int q1 = min(q0 + kBM, N) - 1;
+          const int P = prm.q_period;
+          const int maxpos = (q1 / P != q0 / P) ? P - 1 : q1 % P;
+          tiles = kv_tiles_for<CAUSAL>(maxpos - (kBM - 1), nkv, Nk - P);
+        } else {
+          tiles = nkv;
+        }
+      }
+      // this split's run of key tiles
+      tiles -= w.tb;
+      w.Jt[t] = tiles < 0 ? 0 : (tiles > prm.split_tiles ? prm.split_tiles : tiles);
     }
     w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
     w.kvh = (w.bh / prm.Hq) * prm.Hkv + (w.bh % prm.Hq) / qgroup;
@@ -272,8 +303,10 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     Unit w;
     const int slot = r & 1;
     okr = mbar_wait(&bars->unit_full[slot], (uint32_t)((r >> 1) & 1), abort_flag, prm.err);
-    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot][0]);
     const int4 v = make_int4(qv[0], qv[1], qv[2], qv[3]);
+    w.split = qv[4];
+    w.tb = qv[5];
     if (arrive) mbar_arrive(&bars->unit_empty[slot]);
     w.bh = okr ? v.x : -1;
     w.kvh = v.y;
@@ -291,15 +324,20 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     if (r >= 2 && !mbar_wait(&bars->unit_empty[slot], (uint32_t)(((r - 2) >> 1) & 1), abort_flag, prm.err))
       return false;
     int4 v = make_int4(-1, 0, 0, 0);
+    int split = 0, tb = 0;
     if (u >= 0) {
       const Unit w = decode(u);
       v = make_int4(w.bh, w.kvh, w.q_base, w.Jt[0] | (w.Jt[1] << 16));
+      split = w.split;
+      tb = w.tb;
     }
-    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot]);
+    volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot][0]);
     qv[0] = v.x;
     qv[1] = v.y;
     qv[2] = v.z;
     qv[3] = v.w;
+    qv[4] = split;
+    qv[5] = tb;
     mbar_arrive(&bars->unit_full[slot]);
     return true;
   };
@@ -349,7 +387,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             mbar_arrive_expect_tx(&bars->full[slot], C::SLOT_BYTES);
             for (int ch = 0; ch < C::SLOT_CH; ++ch)
               tma_load_3d_hint(smem + C::OFF_RING + slot * C::SLOT_BYTES + ch * C::CHUNK_BYTES, map,
-                               &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, j * kBN, w.kvh, pol_kv);
+                               &bars->full[slot], (sp * C::SLOT_CH + ch) * C::CH_ELEMS, (w.tb + j) * kBN, w.kvh,
+                               pol_kv);
           }
         };
         if constexpr (C::NQT == 2) {
@@ -624,18 +663,31 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       const int row = q0 + r_in;
       const int Jn = (t == 0) ? w.Jt[0] : w.Jt[1];
       if (Jn == 0) {
-        // no row of this tile sees a key (causal, Nq > Nk): O = 0, LSE = -inf
+        // no row of this tile sees a key of this unit (causal, Nq > Nk, or a
+        // key split beyond the tile's last key): O = 0, LSE = -inf
         if (row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + row) * D * 2);
+          if (S > 1) {
+            const size_t pr = ((size_t)w.split * prm.BH + bh) * N + row;
+            float4* dst = reinterpret_cast<float4*>(prm.o_part + pr * D);
 #pragma unroll 1
-          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-          prm.lse[(size_t)bh * N + row] = -INFINITY;
+            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            prm.lse_part[pr] = -INFINITY;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + row) * D * 2);
+#pragma unroll 1
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            prm.lse[(size_t)bh * N + row] = -INFINITY;
+          }
         }
         break;
       }
 
       // last key this row sees (keys beyond it are masked)
-      const int last_col = CAUSAL ? min(Nk - 1, row + koff) : Nk - 1;
+      const int last_col = CAUSAL ? min(Nk - 1, row % prm.q_period + (Nk - prm.q_period)) : Nk - 1;
+      // the smallest last-visible key among the tile's rows (causal)
+      const int first_last = (min(q0 + kBM, N) - 1) / prm.q_period != q0 / prm.q_period
+                                 ? Nk - prm.q_period
+                                 : q0 % prm.q_period + (Nk - prm.q_period);
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.0f;
       float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
@@ -668,7 +720,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         f_inv = 1.0f / pv;
       };
       if constexpr (ELEM == kE4M3) {
-        if (Jn > 0) fp8_factors(prm.k_ds[kv_blk], prm.v_ds[kv_blk]);
+        if (Jn > 0) fp8_factors(prm.k_ds[kv_blk + w.tb], prm.v_ds[kv_blk + w.tb]);
       }
       // one Q tile: consume o_ready completions up to (and including) the PV
       // of global iteration x on buffer x & 1 (they complete in order)
@@ -714,12 +766,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         if constexpr (ELEM == kE4M3) {
           cj *= f_k;
           if (j + 1 < Jn) {
-            kd_next = prm.k_ds[kv_blk + j + 1];
-            vd_next = prm.v_ds[kv_blk + j + 1];
+            kd_next = prm.k_ds[kv_blk + w.tb + j + 1];
+            vd_next = prm.v_ds[kv_blk + w.tb + j + 1];
           }
         }
-        const int col0 = j * kBN;
-        const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > q0 + koff);
+        const int col0 = (w.tb + j) * kBN;
+        const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > first_last);
         if (need_mask) {
           const int lim = last_col - col0;
 #pragma unroll
@@ -859,6 +911,25 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           const float f = inv_l * v_mult;
           const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
           const bool store = row < N;
+          if (S > 1) {
+            // split-KV partial: O normalised over this split's keys, fp32,
+            // and the split's LSE (a row without visible keys: 0, -inf)
+            const size_t pr = ((size_t)w.split * prm.BH + bh) * N + (size_t)(store ? row : 0);
+            float* prow = prm.o_part + pr * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t u[32];
+              tmem_ld32(o_addr + c0, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+              if (store) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) st_global_v8(prow + c0 + 8 * i, u + 8 * i);
+              }
+            }
+            if (store) prm.lse_part[pr] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
+          } else {
           uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + (size_t)(store ? row : 0)) * D * 2;
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -885,6 +956,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             }
           }
           if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
+          }
         }
       }
       g += Jn;
@@ -934,7 +1006,7 @@ cudaError_t launch_attn(const AttnLaunch& L) {
   }
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 148;
   const long long groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  const long long units = (long long)L.BH * groups;
+  const long long units = (long long)L.BH * groups * (L.prm.splits > 1 ? L.prm.splits : 1);
   (void)sms;
   if constexpr (C::REALLOC) {
     // the register split must fit what the kernel is launched with, or the

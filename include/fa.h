@@ -36,6 +36,7 @@
 #ifndef FA_H
 #define FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -130,6 +131,46 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
                          int causal, float scale,
                          const float* q_descale, const float* k_descale, const float* v_descale,
                          cudaStream_t stream);
+
+/*
+ * fa_fwd_splitkv -- the forward pass of fa_fwd_gqa for decode-like shapes
+ * (few query rows against a long key/value sequence), where batch x heads x
+ * query tiles leave most SMs idle ("FlashAttention-3: async pipelines on
+ * Hopper", sections "why GQA/MQA changes the kernel's task count" and
+ * "prefill, decode and training gain differently": decode needs split-KV
+ * and GQA packing to produce enough parallelism).
+ *   Same inputs, outputs, layouts and masking as fa_fwd_gqa (q [B, Hq, Nq, d],
+ *   k/v [B, Hkv, Nk, d], bf16 or fp16; causal masks bottom-right aligned).
+ *   The Hq / Hkv query heads sharing a key/value head are processed as one
+ *   head of (Hq / Hkv) * Nq rows, so every key/value byte is read once per
+ *   group; each row's keys are split into num_splits runs processed in
+ *   parallel, whose partial results (O normalised per run, fp32, and the
+ *   run's LSE) go to `workspace` and are merged by LSE weights in a second
+ *   kernel on the same stream.  The merge is exact in real arithmetic.
+ *   num_splits   0: chosen for the current device (about two work units per
+ *                SM); else the requested count, capped at the number of
+ *                128-key tiles (runs are never empty).
+ *   workspace    DEVICE pointer, 256-byte aligned, owned by the caller, at
+ *                least the size fa_splitkv_workspace_bytes reports for the
+ *                same shape and num_splits on the same device (NULL allowed
+ *                when that size is 0: a single run writes O directly);
+ *                overwritten; calls sharing it must not overlap on the GPU.
+ * Errors: as fa_fwd_gqa, plus FA_ERR_INVALID_ARG for num_splits < 0 or a
+ * missing, misaligned or too small workspace.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                         int causal, float scale, int dtype, int num_splits,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_splitkv_workspace_bytes -- bytes of device workspace fa_fwd_splitkv
+ * needs for this shape and num_splits on the current device (0 when the
+ * keys are not split).  Writes *bytes; same argument checks as
+ * fa_fwd_splitkv (no pointers besides bytes).
+ */
+fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                                     int num_splits, size_t* bytes);
 
 /*
  * fa_quant_fp8 -- quantise fp32 [B, H, N, d] to E4M3 with one scale per

@@ -84,6 +84,18 @@ def test_host_argument_checks(fa_lib):
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 1, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8(p, p, p, 1, 1, 1, 128, None, 3, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8(None, None, None, 1, 0, 1, 128, None, 0, None, None) == fa.FA_OK
+    # split-KV: a negative split count or a bad dtype is refused, an empty problem is a no-op
+    assert fa_lib.fa_fwd_splitkv(p, p, p, p, p, 1, 4, 2, 1, 100, 128, 0, 0.1, 0, -1, None, 0,
+                                 None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_splitkv(p, p, p, p, p, 1, 4, 2, 1, 100, 128, 0, 0.1, 5, 0, None, 0,
+                                 None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_splitkv(None, None, None, None, None, 1, 4, 2, 0, 100, 128, 0, 0.1, 0, 0, None, 0,
+                                 None) == fa.FA_OK
+    nbytes = ctypes.c_size_t(7)
+    assert fa_lib.fa_splitkv_workspace_bytes(1, 4, 2, 1, 100, 96, 0, ctypes.byref(nbytes)) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_splitkv_workspace_bytes(1, 4, 3, 1, 100, 128, 0, ctypes.byref(nbytes)) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_splitkv_workspace_bytes(0, 4, 2, 1, 100, 128, 0, ctypes.byref(nbytes)) == fa.FA_OK
+    assert nbytes.value == 0
     # quantiser with rotary embedding: a known layout and both tables are required
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 0, None, 0, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 3, None, 0, None, None) == fa.FA_ERR_INVALID_ARG
