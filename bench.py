@@ -311,6 +311,28 @@ def run_extra(args, device):
                                  "quant_rope_ms_per_tensor": round(rms, 4),
                                  "quant_rope_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1)}
     out["fp8_peak_note"] = "FP8 peak = measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"
+
+    # decode-like: one query row per head against a long key/value cache,
+    # GQA 4 (split-KV with the group's query heads packed), against the
+    # unsplit grouped-query path on the same shape; HBM-bound, so the figure
+    # is the K/V bytes read per second
+    B, Hq, Hkv, Nk, d = 8, 32, 8, 32768, 128
+    q = torch.randn((B, Hq, 1, d), device=device, generator=g).to(torch.bfloat16)
+    k, v = (torch.randn((B, Hkv, Nk, d), device=device, generator=g).to(torch.bfloat16) for _ in range(2))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, 1), device=device, dtype=torch.float32)
+    need = fa.splitkv_workspace_bytes(B, Hq, Hkv, 1, Nk, d)
+    ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=device)
+    kv_bytes = 2 * B * Hkv * Nk * d * 2
+    dec = {}
+    for name, fn in (("splitkv", lambda: fa.fwd_splitkv(q, k, v, out=o, lse=lse, workspace=ws)),
+                     ("unsplit_gqa", lambda: fa.fwd_gqa(q, k, v, out=o, lse=lse))):
+        fn()
+        ms = _time_launches(fn, 5, device, flush)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        dec[name] = {"ms": round(ms, 4), "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
+    dec["workload"] = f"B={B} Hq={Hq} Hkv={Hkv} Nq=1 Nk={Nk} d={d} bf16, K/V {kv_bytes / 1e9:.2f} GB"
+    out["decode"] = dec
     return out
 
 

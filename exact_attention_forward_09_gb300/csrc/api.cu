@@ -18,7 +18,7 @@
 #include "quant_fp8.h"
 
 namespace fa {
-template <int ELEM, int D, bool CAUSAL>
+template <int ELEM, int D, bool CAUSAL, bool SPLIT>
 cudaError_t launch_attn(const AttnLaunch& L);
 }
 
@@ -108,16 +108,16 @@ fa_status check_common(const void* q, const void* k, const void* v, const void* 
   return FA_OK;
 }
 
-template <int ELEM>
+template <int ELEM, bool SPLIT = false>
 fa_status dispatch(const fa::AttnLaunch& L, int64_t d, int causal) {
   cudaError_t e = cudaErrorInvalidValue;
   if (d == 64) {
     if constexpr (ELEM == fa::kE4M3) return FA_ERR_UNSUPPORTED;
-    else e = causal ? fa::launch_attn<ELEM, 64, true>(L) : fa::launch_attn<ELEM, 64, false>(L);
+    else e = causal ? fa::launch_attn<ELEM, 64, true, SPLIT>(L) : fa::launch_attn<ELEM, 64, false, SPLIT>(L);
   } else if (d == 128) {
-    e = causal ? fa::launch_attn<ELEM, 128, true>(L) : fa::launch_attn<ELEM, 128, false>(L);
+    e = causal ? fa::launch_attn<ELEM, 128, true, SPLIT>(L) : fa::launch_attn<ELEM, 128, false, SPLIT>(L);
   } else if (d == 256) {
-    e = causal ? fa::launch_attn<ELEM, 256, true>(L) : fa::launch_attn<ELEM, 256, false>(L);
+    e = causal ? fa::launch_attn<ELEM, 256, true, SPLIT>(L) : fa::launch_attn<ELEM, 256, false, SPLIT>(L);
   } else {
     return FA_ERR_UNSUPPORTED;
   }
@@ -230,7 +230,8 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   L.prm.o_part = p.S > 1 ? o_part : nullptr;
   L.prm.lse_part = lse_part;
   L.stream = stream;
-  st = dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
+  // the split-KV instance (packed rows; partial results when S > 1)
+  st = dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16, true>(L, d, causal) : dispatch<fa::kFP16, true>(L, d, causal);
   if (st != FA_OK || p.S == 1) return st;
   return fa::launch_splitkv_combine(o_part, lse_part, o, lse, p.S, (long long)(p.BHp * p.Np), (int)d,
                                     dtype == FA_DTYPE_FP16, stream) == cudaSuccess

@@ -187,7 +187,11 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int nkv, int off) {
 //   two Q tiles : K0 V0 K1 V1 ...            (S(j+1) is issued after PV(j))
 //   one Q tile  : K0 K1 V0 K2 V1 K3 V2 ...   (S(j+2) is issued after PV(j))
 
-template <int ELEM, int D, bool CAUSAL>
+// SPLIT: the split-KV instance: rows may be packed (causal positions modulo
+// q_period) and, when prm.splits > 1, units cover runs of key tiles and
+// write fp32 partial results.  Without it every row is its own position and
+// a unit covers the whole key range.
+template <int ELEM, int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams prm) {
@@ -204,7 +208,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   const int nkv = (Nk + kBN - 1) / kBN;
   const int qgroup = prm.Hq / prm.Hkv;     // query heads per key/value head
   const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  const int S = prm.splits;         // key splits (1: none)
+  const int koff = Nk - N;                 // causal diagonal offset (unpacked rows)
+  const int S = SPLIT ? prm.splits : 1;  // key splits
   const int U = prm.BH * n_groups * S;  // work units: (head, group of NQT Q tiles, key split)
   const int G = (int)gridDim.x;
 
@@ -227,8 +232,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   auto decode = [&](int u) -> Unit {
     Unit w;
     int group;
-    w.split = u % S;
-    const int v = u / S;
+    w.split = SPLIT ? u % S : 0;
+    const int v = SPLIT ? u / S : u;
     if constexpr (CAUSAL) {
       group = n_groups - 1 - v / prm.BH;
       w.bh = v % prm.BH;
@@ -237,27 +242,32 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       group = v % n_groups;
     }
     w.q_base = group * (C::NQT * kBM);
-    w.tb = w.split * prm.split_tiles;
+    w.tb = SPLIT ? w.split * prm.split_tiles : 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int q0 = w.q_base + t * kBM;
       w.active[t] = (t < C::NQT) && (q0 < N);
       int tiles = 0;
       if (w.active[t]) {
-        if constexpr (CAUSAL) {
+        if constexpr (CAUSAL && SPLIT) {
           // last key any row of the tile sees, from the largest position
           // among its rows (rows of several packed heads: the last one)
           const int q1 = min(q0 + kBM, N) - 1;
           const int P = prm.q_period;
           const int maxpos = (q1 / P != q0 / P) ? P - 1 : q1 % P;
           tiles = kv_tiles_for<CAUSAL>(maxpos - (kBM - 1), nkv, Nk - P);
+        } else if constexpr (CAUSAL) {
+          tiles = kv_tiles_for<CAUSAL>(q0, nkv, koff);
         } else {
           tiles = nkv;
         }
       }
-      // this split's run of key tiles
-      tiles -= w.tb;
-      w.Jt[t] = tiles < 0 ? 0 : (tiles > prm.split_tiles ? prm.split_tiles : tiles);
+      if constexpr (SPLIT) {
+        // this split's run of key tiles
+        tiles -= w.tb;
+        tiles = tiles < 0 ? 0 : (tiles > prm.split_tiles ? prm.split_tiles : tiles);
+      }
+      w.Jt[t] = tiles;
     }
     w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
     w.kvh = (w.bh / prm.Hq) * prm.Hkv + (w.bh % prm.Hq) / qgroup;
@@ -305,8 +315,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     okr = mbar_wait(&bars->unit_full[slot], (uint32_t)((r >> 1) & 1), abort_flag, prm.err);
     volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot][0]);
     const int4 v = make_int4(qv[0], qv[1], qv[2], qv[3]);
-    w.split = qv[4];
-    w.tb = qv[5];
+    w.split = SPLIT ? qv[4] : 0;
+    w.tb = SPLIT ? qv[5] : 0;
     if (arrive) mbar_arrive(&bars->unit_empty[slot]);
     w.bh = okr ? v.x : -1;
     w.kvh = v.y;
@@ -666,7 +676,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         // no row of this tile sees a key of this unit (causal, Nq > Nk, or a
         // key split beyond the tile's last key): O = 0, LSE = -inf
         if (row < N) {
-          if (S > 1) {
+          if (SPLIT && S > 1) {
             const size_t pr = ((size_t)w.split * prm.BH + bh) * N + row;
             float4* dst = reinterpret_cast<float4*>(prm.o_part + pr * D);
 #pragma unroll 1
@@ -683,11 +693,16 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       }
 
       // last key this row sees (keys beyond it are masked)
-      const int last_col = CAUSAL ? min(Nk - 1, row % prm.q_period + (Nk - prm.q_period)) : Nk - 1;
-      // the smallest last-visible key among the tile's rows (causal)
-      const int first_last = (min(q0 + kBM, N) - 1) / prm.q_period != q0 / prm.q_period
-                                 ? Nk - prm.q_period
-                                 : q0 % prm.q_period + (Nk - prm.q_period);
+      // and the smallest last-visible key among the tile's rows (causal)
+      int last_col = Nk - 1, first_last = q0 + koff;
+      if constexpr (CAUSAL && SPLIT) {
+        // packed rows: position = row % q_period
+        const int P = prm.q_period;
+        last_col = min(Nk - 1, row % P + (Nk - P));
+        first_last = (min(q0 + kBM, N) - 1) / P != q0 / P ? Nk - P : q0 % P + (Nk - P);
+      } else if constexpr (CAUSAL) {
+        last_col = min(Nk - 1, row + koff);
+      }
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.0f;
       float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
@@ -911,7 +926,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           const float f = inv_l * v_mult;
           const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
           const bool store = row < N;
-          if (S > 1) {
+          if (SPLIT && S > 1) {
             // split-KV partial: O normalised over this split's keys, fp32,
             // and the split's LSE (a row without visible keys: 0, -inf)
             const size_t pr = ((size_t)w.split * prm.BH + bh) * N + (size_t)(store ? row : 0);
@@ -985,10 +1000,10 @@ struct AttnLaunch {
   cudaStream_t stream;
 };
 
-template <int ELEM, int D, bool CAUSAL>
+template <int ELEM, int D, bool CAUSAL, bool SPLIT>
 cudaError_t launch_attn(const AttnLaunch& L) {
   using C = AttnCfg<ELEM, D, CAUSAL>;
-  auto kern = attn_fwd_kernel<ELEM, D, CAUSAL>;
+  auto kern = attn_fwd_kernel<ELEM, D, CAUSAL, SPLIT>;
   static bool attr_done[64] = {};  // the attribute is per function and device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1006,7 +1021,7 @@ cudaError_t launch_attn(const AttnLaunch& L) {
   }
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 148;
   const long long groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  const long long units = (long long)L.BH * groups * (L.prm.splits > 1 ? L.prm.splits : 1);
+  const long long units = (long long)L.BH * groups * (SPLIT ? L.prm.splits : 1);
   (void)sms;
   if constexpr (C::REALLOC) {
     // the register split must fit what the kernel is launched with, or the

@@ -100,7 +100,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // MODE 0: per-block scale.  MODE 1: per-tensor amax into *amax_ws (atomic).
 // MODE 2: per-tensor encode with the amax in *amax_ws.
 // MODE 3: per-block amax stored to amax_ws[bh * nblk + blk] (no atomics).
-template <int D, int MODE>
+// ROPE: rotary embedding first (pairing `rope`, 1 or 2); separate instances
+// keep the plain path's code unchanged.
+template <int D, int MODE, bool ROPE>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
                                                          float* __restrict__ descale, int N, int nblk,
                                                          SignBits sg, int rot, float rinv,
@@ -156,12 +158,12 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
         v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
     }
-    if (rope) rope_row<D>(v, lane, rcos + (size_t)(r0 + r) * (D / 2), rsin + (size_t)(r0 + r) * (D / 2), rope);
+    if constexpr (ROPE) rope_row<D>(v, lane, rcos + (size_t)(r0 + r) * (D / 2), rsin + (size_t)(r0 + r) * (D / 2), rope);
     rotate_row<D>(v, lane, sg, rot != 0);
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
     if constexpr (MODE == 0) {
-      if (rot || rope) {
+      if (rot || ROPE) {
 #pragma unroll
         for (int e = 0; e < E; ++e) yrow[e] = v[e];
       }
@@ -231,14 +233,14 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
 
 // Dynamic shared memory of one block (128 rows x D fp32), set once per
 // device for each instance.
-template <int D, int MODE>
+template <int D, int MODE, bool ROPE>
 static cudaError_t prep_quant() {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(quant_e4m3_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(quant_e4m3_kernel<D, MODE, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(128u * D * sizeof(float)));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -246,14 +248,19 @@ static cudaError_t prep_quant() {
   return cudaSuccess;
 }
 
-template <int D, int MODE>
-static cudaError_t launch_mode(const QuantLaunch& L, float* ws) {
-  cudaError_t e = prep_quant<D, MODE>();
+template <int D, int MODE, bool ROPE>
+static cudaError_t launch_mode_r(const QuantLaunch& L, float* ws) {
+  cudaError_t e = prep_quant<D, MODE, ROPE>();
   if (e != cudaSuccess) return e;
   const dim3 grid(L.nblk, L.BH, 1);
-  quant_e4m3_kernel<D, MODE><<<grid, 256, 128u * D * sizeof(float), L.stream>>>(
+  quant_e4m3_kernel<D, MODE, ROPE><<<grid, 256, 128u * D * sizeof(float), L.stream>>>(
       L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv, L.rope_cos, L.rope_sin, L.rope, ws, L.err);
   return cudaGetLastError();
+}
+
+template <int D, int MODE>
+static cudaError_t launch_mode(const QuantLaunch& L, float* ws) {
+  return L.rope ? launch_mode_r<D, MODE, true>(L, ws) : launch_mode_r<D, MODE, false>(L, ws);
 }
 
 template <int D>
