@@ -126,9 +126,11 @@ fa_status dispatch(const fa::AttnLaunch& L, int64_t d, int causal) {
 
 // Split-KV plan: the query heads of a key/value group are packed into one
 // head of g * Nq rows (contiguous in [B, Hq, Nq, d]), and each row's key
-// tiles are cut into S runs of T tiles, S chosen (when 0 is asked) to give
-// about two units per SM.  Workspace: partial O [S][B*Hkv][g*Nq][d] fp32,
-// then partial LSE [S][B*Hkv][g*Nq] fp32 (256-byte aligned start).
+// tiles are cut into S runs of T tiles.  Chosen S (when 0 is asked): about
+// eight units per SM -- the runs are memory-bound with little fixed cost, and
+// several waves keep the last one from leaving most SMs idle -- but at least
+// 8 key tiles per run.  Workspace: partial O [S][B*Hkv][g*Nq][d] fp32, then
+// partial LSE [S][B*Hkv][g*Nq] fp32 (256-byte aligned start).
 struct SplitPlan {
   int64_t BHp, Np;
   int S, T;
@@ -143,7 +145,12 @@ fa_status splitkv_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N
   const int64_t rows_per_unit = d <= 128 ? 256 : 128;
   const int64_t base = p->BHp * ((p->Np + rows_per_unit - 1) / rows_per_unit);
   const int64_t nkv = (Nk + 127) / 128;
-  int64_t S = num_splits > 0 ? num_splits : (2 * (int64_t)sms + base - 1) / base;
+  int64_t S = num_splits;
+  if (S == 0) {
+    S = (8 * (int64_t)sms + base - 1) / base;
+    const int64_t most = (nkv + 7) / 8;  // at least 8 key tiles per run
+    if (S > most) S = most;
+  }
   if (S > nkv) S = nkv;
   if (S > 1024) S = 1024;
   if (S < 1) S = 1;

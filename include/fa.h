@@ -147,9 +147,10 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
  *   parallel, whose partial results (O normalised per run, fp32, and the
  *   run's LSE) go to `workspace` and are merged by LSE weights in a second
  *   kernel on the same stream.  The merge is exact in real arithmetic.
- *   num_splits   0: chosen for the current device (about two work units per
- *                SM); else the requested count, capped at the number of
- *                128-key tiles (runs are never empty).
+ *   num_splits   0: chosen for the current device (about eight work units
+ *                per SM, at least 8 key tiles of 128 per run); else the
+ *                requested count, capped at the number of 128-key tiles
+ *                (runs are never empty).
  *   workspace    DEVICE pointer, 256-byte aligned, owned by the caller, at
  *                least the size fa_splitkv_workspace_bytes reports for the
  *                same shape and num_splits on the same device (NULL allowed
