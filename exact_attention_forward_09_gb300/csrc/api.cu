@@ -352,7 +352,7 @@ fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_
   if (per_tensor != 0 && per_tensor != 1) return FA_ERR_INVALID_ARG;
   if (rope_layout != 0 && rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
-  if (rope_layout != 0 && (!rope_cos || !rope_sin || ((uintptr_t)rope_cos & 3u) || ((uintptr_t)rope_sin & 3u)))
+  if (rope_layout != 0 && (!rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin)))
     return FA_ERR_INVALID_ARG;
   if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x8) || ((uintptr_t)descale & 3u)) return FA_ERR_INVALID_ARG;

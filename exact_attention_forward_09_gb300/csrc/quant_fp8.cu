@@ -21,8 +21,9 @@
 // 1, 2, 4, ... in fp32, so every element sees the same sequence of fp32
 // additions as the plain in-place butterfly.  The rotated rows stay in shared
 // memory between the amax pass and the encode pass.  The 1/sqrt(d) factor is
-// folded into the stored descale, so the codes are RNE(y / s) with
-// s = amax(y) / 448 of the unnormalised rotated block y.
+// folded into the stored descale, so the codes are RNE(y * r) with
+// r = RN(1 / s), s = amax(y) / 448 of the unnormalised rotated block y (one
+// correctly rounded reciprocal per block instead of a division per element).
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -61,6 +62,24 @@ __device__ __forceinline__ void rotate_row(float (&v)[D / 32], int lane, const S
   }
 }
 
+// n consecutive floats (16-byte aligned when n >= 4, 8-byte when n == 2)
+template <int n>
+__device__ __forceinline__ void load_row_f32(float (&out)[n], const float* __restrict__ p) {
+  if constexpr (n % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < n; i += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(p + i);
+      out[i] = t.x; out[i + 1] = t.y; out[i + 2] = t.z; out[i + 3] = t.w;
+    }
+  } else if constexpr (n == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    out[0] = t.x; out[1] = t.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < n; ++i) out[i] = p[i];
+  }
+}
+
 // Rotary embedding of one row (lane holds channels lane*E .. lane*E+E-1);
 // c, s: this row's cos / sin tables (d/2 entries each).
 template <int D>
@@ -68,11 +87,13 @@ __device__ __forceinline__ void rope_row(float (&v)[D / 32], int lane, const flo
                                          const float* __restrict__ s, int mode) {
   constexpr int E = D / 32;
   if (mode == 1) {
-    // pairs (2i, 2i+1), both in this lane
+    // pairs (2i, 2i+1), both in this lane: angles lane*E/2 .. +E/2
+    float cv[E / 2], sv[E / 2];
+    load_row_f32<E / 2>(cv, c + lane * (E / 2));
+    load_row_f32<E / 2>(sv, s + lane * (E / 2));
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
-      const int i = (lane * E + e) >> 1;
-      const float cs = c[i], sn = s[i];
+      const float cs = cv[e / 2], sn = sv[e / 2];
       const float a = v[e], b = v[e + 1];
       v[e] = __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn));
       v[e + 1] = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
@@ -80,10 +101,12 @@ __device__ __forceinline__ void rope_row(float (&v)[D / 32], int lane, const flo
   } else if (mode == 2) {
     // pairs (i, i + D/2): lane L < 16 holds i = L*E + e, lane L + 16 its partner
     const bool first = lane < 16;
+    float cv[E], sv[E];
+    load_row_f32<E>(cv, c + (lane & 15) * E);
+    load_row_f32<E>(sv, s + (lane & 15) * E);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int i = (lane & 15) * E + e;
-      const float cs = c[i], sn = s[i];
+      const float cs = cv[e], sn = sv[e];
       const float o = __shfl_xor_sync(0xffffffffu, v[e], 16);
       const float a = first ? v[e] : o, b = first ? o : v[e];
       v[e] = first ? __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)) : __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
@@ -171,14 +194,15 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
       // per-tensor encode: scale known up front
       const float am = *amax_ws;
       const float s = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+      const float rs = __frcp_rn(s);
       uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
       if constexpr (E == 2) {
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fmul_rn(v[0], rs), __fmul_rn(v[1], rs));
       } else {
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
-          const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * q], s), __fdiv_rn(v[4 * q + 1], s));
-          const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * q + 2], s), __fdiv_rn(v[4 * q + 3], s));
+          const uint32_t lo = e4m3x2(__fmul_rn(v[4 * q], rs), __fmul_rn(v[4 * q + 1], rs));
+          const uint32_t hi = e4m3x2(__fmul_rn(v[4 * q + 2], rs), __fmul_rn(v[4 * q + 3], rs));
           reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
         }
       }
@@ -213,16 +237,17 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict
     return;
   } else {
     const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float rs = __frcp_rn(s);
     for (int r = warp; r < nrows; r += 8) {
       uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
       const float* y = ys + r * D + lane * E;
       if constexpr (E == 2) {
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s));
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fmul_rn(y[0], rs), __fmul_rn(y[1], rs));
       } else {
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
-          const uint32_t lo = e4m3x2(__fdiv_rn(y[4 * q], s), __fdiv_rn(y[4 * q + 1], s));
-          const uint32_t hi = e4m3x2(__fdiv_rn(y[4 * q + 2], s), __fdiv_rn(y[4 * q + 3], s));
+          const uint32_t lo = e4m3x2(__fmul_rn(y[4 * q], rs), __fmul_rn(y[4 * q + 1], rs));
+          const uint32_t hi = e4m3x2(__fmul_rn(y[4 * q + 2], rs), __fmul_rn(y[4 * q + 3], rs));
           reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
         }
       }

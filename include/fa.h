@@ -193,7 +193,9 @@ fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t
  *   workspace      per_tensor = 1: DEVICE pointer to one float of scratch
  *                  (overwritten; calls sharing it must not overlap on the GPU);
  *                  per_tensor = 0: ignored, may be NULL
- * Codes are round-to-nearest-even of (y / scale) in fp32, saturated at 448.
+ * Codes are round-to-nearest-even of y * RN(1 / scale) in fp32 (the scale's
+ * correctly rounded reciprocal, then one product per element), saturated at
+ * 448.
  */
 fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
                        int64_t B, int64_t H, int64_t N, int64_t d,
@@ -213,7 +215,7 @@ fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
  * Pair (a, b) of row n becomes (a*c - b*s, a*s + b*c) with c = rope_cos[n][i],
  * s = rope_sin[n][i], in fp32 with each product rounded before the sum; then
  * the optional rotation and the quantisation proceed as in fa_quant_fp8.
- *   rope_cos, rope_sin  [N, d/2] fp32 (device, read only, 4-byte aligned),
+ *   rope_cos, rope_sin  [N, d/2] fp32 (device, read only, 16-byte aligned),
  *                       shared by every (b, h): row n is position n of each
  *                       sequence (offset positions by offsetting the tables)
  *   rope_layout         FA_ROPE_INTERLEAVED or FA_ROPE_HALF

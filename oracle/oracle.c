@@ -40,7 +40,8 @@
  *                    the rotation is the fast Walsh-Hadamard butterfly with
  *                    strides 1, 2, 4, ... in fp32, the 1/sqrt(d) factor is
  *                    carried in the stored descale, codes are
- *                    round-to-nearest-even of (y / s) with saturation at 448.
+ *                    round-to-nearest-even of y * RN(1 / s) with saturation at
+ *                    448 (one rounded reciprocal per block, then products).
  *
  *                    With a rotary position embedding requested, each row is
  *                    first turned pairwise by the caller's angles (the pages
@@ -282,7 +283,8 @@ int oracle_quant_e4m3(const float* x, uint8_t* codes, float* descale,
             else for (int64_t i = 0; i < cnt; ++i) { float a = fabsf(yb[i]); if (a > amax) amax = a; }
             const float s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
             uint8_t* cb = codes + (bh * N + r0) * d;
-            for (int64_t i = 0; i < cnt; ++i) cb[i] = oracle_e4m3_encode(yb[i] / s);
+            const float rs = 1.0f / s;
+            for (int64_t i = 0; i < cnt; ++i) cb[i] = oracle_e4m3_encode(yb[i] * rs);
             descale[bh * nblk + blk] = s * rinv;
         }
     }

@@ -103,6 +103,8 @@ def test_host_argument_checks(fa_lib):
                                     None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p + 2, fa.FA_ROPE_INTERLEAVED, None, 0, None,
                                     None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p + 8, p, fa.FA_ROPE_HALF, None, 0, None,
+                                    None) == fa.FA_ERR_INVALID_ARG  # tables must be 16-byte aligned
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 100, p, p, fa.FA_ROPE_HALF, None, 0, None,
                                     None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_quant_fp8_rope(None, None, None, 0, 1, 1, 128, None, None, fa.FA_ROPE_HALF, None, 0, None,
