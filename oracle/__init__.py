@@ -15,6 +15,12 @@ Functions and the passages they follow:
   softmax reaches exactly this result: same article sec. 2.1 and
   "FlashAttention-3: async pipelines on Hopper", section "Online Softmax is
   still the core of exact merging".
+* :func:`attn_bwd` -- fp64 gradients dQ, dK, dV of sum(dO * O): the
+  derivative of the same definition, one query row at a time with its row of
+  probabilities materialised.  The pages name the backward pass among the
+  paths to test ("FlashAttention-3: async pipelines on Hopper", section
+  "correctness validation must cover asynchronous boundaries") but print no
+  formula.
 * :func:`online_attn_fwd` -- the tiled online-softmax recurrence itself
   (running max m, running sum l, accumulator o, initial m=-inf, l=0, o=0;
   wmrh.cn article sec. 2.1), with an optional lazy-rescale threshold.  Kept
@@ -59,6 +65,9 @@ def _lib():
         lib.oracle_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                         i32, f64, vp, i64, i32]
         lib.oracle_attn_fwd.restype = i32
+        lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                        i32, f64, i32]
+        lib.oracle_attn_bwd.restype = i32
         lib.oracle_quant_e4m3.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i32, vp, vp, i32]
         lib.oracle_quant_e4m3.restype = i32
         lib.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
@@ -127,6 +136,36 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, rows=Non
     if rc != 0:
         raise RuntimeError("oracle_attn_fwd failed")
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, causal: bool = False, scale: float | None = None,
+             nthreads: int | None = None):
+    """fp64 gradients of sum(dout * O) for O = attention(q, k, v).
+
+    Shapes and masking as :func:`attn_fwd`; dout has q's shape.  Returns
+    (dq [B, Hq, Nq, d], dk [B, Hkv, Nk, d], dv [B, Hkv, Nk, d]) in fp64;
+    dk and dv sum over the query heads of each key/value group.
+    """
+    q = _np(q, np.float64)
+    k = _np(k, np.float64)
+    v = _np(v, np.float64)
+    dout = _np(dout, np.float64)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    assert v.shape == k.shape and Bk == B and dk_ == d and Hq % Hkv == 0
+    assert dout.shape == q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(k.shape, dtype=np.float64)
+    nt = nthreads if nthreads is not None else max_threads()
+    rc = _lib().oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                                B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), int(nt))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd failed")
+    return dq, dk, dv
 
 
 def online_attn_fwd(q, k, v, causal: bool = False, scale: float | None = None,

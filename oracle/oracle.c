@@ -51,6 +51,24 @@
  *                    a' = a cos - b sin, b' = a sin + b cos), in fp32 with each
  *                    product rounded before the sum, like the kernel.
  *
+ *  oracle_attn_bwd   Gradients dQ, dK, dV of the loss sum(dO * O) for the
+ *                    same attention (the pages list the backward pass among
+ *                    the paths a test must cover and compare its speed with
+ *                    FA2 ["FlashAttention-3: async pipelines on Hopper",
+ *                    sections "correctness validation must cover asynchronous
+ *                    boundaries" and "how to read the paper's performance
+ *                    numbers"], but print no formula).  It is the derivative
+ *                    of the definition above, written out per query row with
+ *                    the row of probabilities materialised:
+ *                      P_ij  = exp(s_ij - m_i) / l_i       (visible j only)
+ *                      dP_ij = dO_i . v_j
+ *                      D_i   = sum_j P_ij dP_ij
+ *                      dS_ij = P_ij (dP_ij - D_i)
+ *                      dQ_i  = scale sum_j dS_ij k_j
+ *                      dK_j  = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i,
+ *                    the last two summed over every query head of the
+ *                    key/value head's group.
+ *
  *  oracle_e4m3_encode / oracle_e4m3_decode
  *                    The E4M3 format from its definition: 1 sign bit, 4
  *                    exponent bits (bias 7), 3 mantissa bits, subnormals at
@@ -146,6 +164,104 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v,
         }
         free(s);
         free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Backward pass.  q, dout, dq [B, Hq, Nq, d]; k, v, dk, dv [B, Hkv, Nk, d].
+ * Work is split over (b, key/value head), so each thread owns the dK and dV
+ * rows it accumulates into.  A query with no visible key gets dq = 0 and
+ * contributes nothing.  Returns 0, or -1 on bad arguments / allocation
+ * failure.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv,
+                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk,
+                    int64_t d, int causal, double scale, int nthreads)
+{
+    if (B < 0 || Hq < 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int64_t group = Hq / Hkv;
+    const int64_t total = B * Hkv;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = 1;
+
+#pragma omp parallel num_threads(nthreads)
+    {
+        const size_t nk1 = (size_t)(Nk > 0 ? Nk : 1);
+        double* p = (double*)malloc(sizeof(double) * nk1);
+        double* dp = (double*)malloc(sizeof(double) * nk1);
+        if (!p || !dp) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < total; ++t) {
+            if (!p || !dp) continue;
+            const int64_t b = t / Hkv, hk = t % Hkv;
+            const double* kb = k + (b * Hkv + hk) * Nk * d;
+            const double* vb = v + (b * Hkv + hk) * Nk * d;
+            double* dkb = dk + (b * Hkv + hk) * Nk * d;
+            double* dvb = dv + (b * Hkv + hk) * Nk * d;
+            for (int64_t e = 0; e < Nk * d; ++e) {
+                dkb[e] = 0.0;
+                dvb[e] = 0.0;
+            }
+            for (int64_t h = hk * group; h < (hk + 1) * group; ++h) {
+                for (int64_t i = 0; i < Nq; ++i) {
+                    const int64_t row = (b * Hq + h) * Nq + i;
+                    const double* qi = q + row * d;
+                    const double* doi = dout + row * d;
+                    double* dqi = dq + row * d;
+                    for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
+                    int64_t jend = Nk;
+                    if (causal) {
+                        int64_t lim = i + (Nk - Nq) + 1;
+                        if (lim < jend) jend = lim;
+                        if (jend < 0) jend = 0;
+                    }
+                    if (jend == 0) continue;
+                    /* probabilities of the row */
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < jend; ++j) {
+                        const double* kj = kb + j * d;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kj[c];
+                        p[j] = scale * dot;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (int64_t j = 0; j < jend; ++j) {
+                        p[j] = exp(p[j] - m);
+                        l += p[j];
+                    }
+                    for (int64_t j = 0; j < jend; ++j) p[j] /= l;
+                    /* dP = dO_i . v_j and D_i = sum_j P dP */
+                    double Di = 0.0;
+                    for (int64_t j = 0; j < jend; ++j) {
+                        const double* vj = vb + j * d;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += doi[c] * vj[c];
+                        dp[j] = dot;
+                        Di += p[j] * dot;
+                    }
+                    for (int64_t j = 0; j < jend; ++j) {
+                        const double ds = p[j] * (dp[j] - Di);
+                        const double* kj = kb + j * d;
+                        double* dkj = dkb + j * d;
+                        double* dvj = dvb + j * d;
+                        for (int64_t c = 0; c < d; ++c) {
+                            dqi[c] += scale * ds * kj[c];
+                            dkj[c] += scale * ds * qi[c];
+                            dvj[c] += p[j] * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
     }
     return bad ? -1 : 0;
 }

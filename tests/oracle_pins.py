@@ -20,6 +20,9 @@ Sources of truth used here:
     sec. 2.1: the tiled result is the same as the global one);
   * torch.float8_e4m3fn for the E4M3 codec, and 448 as its maximum (wmrh.cn
     article, sec. 3.3);
+  * for the backward pass: torch autograd through CPU float64 SDPA, central
+    finite differences of the pinned forward, and the sums fixed by the
+    softmax (rows of dS sum to zero, rows of P to one);
   * for the rotary embedding (which the pages only place before the
     quantisation pass): complex multiplication of each channel pair by
     e^{i theta} (numpy complex arithmetic), the permutation relating the two
@@ -180,6 +183,122 @@ def pin_row_subset(oracle):
         o, lse = oracle.attn_fwd(q, k, v, causal=causal, scale=0.25)
         os_, ls_ = oracle.attn_fwd(q, k, v, causal=causal, scale=0.25, rows=rows)
         assert np.array_equal(o[:, :, rows], os_) and np.array_equal(lse[:, :, rows], ls_)
+
+
+# --------------------------------------------------------------------------
+# backward pass
+# --------------------------------------------------------------------------
+
+def _torch_grads(q, k, v, do, causal, scale):
+    """dQ, dK, dV of sum(do * O) by torch autograd through CPU float64 SDPA
+    (bottom-right causal mask; K/V heads repeated for grouped queries, so
+    autograd sums the group's contributions)."""
+    qt, kt, vt = (torch.tensor(np.asarray(a, dtype=np.float64), requires_grad=True) for a in (q, k, v))
+    Hq, Hkv = qt.shape[1], kt.shape[1]
+    kr = kt.repeat_interleave(Hq // Hkv, dim=1) if Hq != Hkv else kt
+    vr = vt.repeat_interleave(Hq // Hkv, dim=1) if Hq != Hkv else vt
+    Nq, Nk = qt.shape[2], kt.shape[2]
+    mask = None
+    if causal:
+        mask = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kr, vr, attn_mask=mask, scale=scale)
+    o.backward(torch.tensor(np.asarray(do, dtype=np.float64)))
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def _bwd_inputs(shape_q, shape_k, seed):
+    q = gen.normal(shape_q, seed, 0).astype(np.float64)
+    k = gen.normal(shape_k, seed, 1).astype(np.float64)
+    v = gen.normal(shape_k, seed, 2).astype(np.float64)
+    do = gen.normal(shape_q, seed, 3).astype(np.float64)
+    return q, k, v, do
+
+
+def pin_bwd_autograd(oracle):
+    cases = [
+        # (B, Hq, Hkv, Nq, Nk, d, causal, scale)
+        (1, 2, 2, 64, 64, 16, False, 0.25),
+        (1, 2, 2, 64, 64, 16, True, 0.25),
+        (2, 4, 2, 37, 37, 8, True, 0.6),
+        (1, 3, 1, 20, 50, 8, True, 0.5),
+        (1, 2, 2, 50, 20, 8, False, -0.7),
+    ]
+    for t, (B, Hq, Hkv, Nq, Nk, d, causal, scale) in enumerate(cases):
+        q, k, v, do = _bwd_inputs((B, Hq, Nq, d), (B, Hkv, Nk, d), 30 + t)
+        got = oracle.attn_bwd(q, k, v, do, causal=causal, scale=scale)
+        ref = _torch_grads(q, k, v, do, causal, scale)
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert np.allclose(g, r, rtol=0, atol=1e-11), f"case {t}: {name} differs from torch autograd"
+
+
+def pin_bwd_finite_difference(oracle):
+    """Directional derivatives of L = sum(dO * O), with O from the (separately
+    pinned) forward oracle, by central differences."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 24, 8
+    q, k, v, do = _bwd_inputs((B, Hq, N, d), (B, Hkv, N, d), 40)
+    rng = np.random.Generator(np.random.PCG64(41))
+    for causal in (False, True):
+        grads = oracle.attn_bwd(q, k, v, do, causal=causal, scale=0.4)
+
+        def loss(qq, kk, vv):
+            o, _ = oracle.attn_fwd(qq, kk, vv, causal=causal, scale=0.4)
+            return float(np.sum(do * o))
+
+        h = 1e-5
+        for which in range(3):
+            x = [q, k, v]
+            u = rng.standard_normal(x[which].shape)
+            xp = list(x)
+            xm = list(x)
+            xp[which] = x[which] + h * u
+            xm[which] = x[which] - h * u
+            fd = (loss(*xp) - loss(*xm)) / (2 * h)
+            an = float(np.sum(grads[which] * u))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (causal, which, fd, an)
+
+
+def pin_bwd_invariants(oracle):
+    B, Hq, Hkv, N, d = 1, 4, 2, 40, 8
+    q, k, v, do = _bwd_inputs((B, Hq, N, d), (B, Hkv, N, d), 50)
+    g = Hq // Hkv
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=causal, scale=0.3)
+        # each row of dS sums to zero, so the key gradients sum to zero
+        assert np.allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+        # each row of P sums to one, so the value gradients sum to sum(dO)
+        want = do.reshape(B, Hkv, g, N, d).sum(axis=(2, 3))
+        assert np.allclose(dv.sum(axis=2), want, atol=1e-12)
+    # scale 0: uniform weights, no gradient into Q or K
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=False, scale=0.0)
+    assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
+    want = do.reshape(B, Hkv, g, N, d).sum(axis=(2, 3))[:, :, None, :] / N
+    assert np.allclose(dv, np.broadcast_to(want, dv.shape), atol=1e-13)
+    # causal, scale 0: row i spreads dO_i evenly over keys 0..i
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=True, scale=0.0)
+    w = do.reshape(B, Hkv, g, N, d).sum(axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    want = np.cumsum(w[:, :, ::-1], axis=2)[:, :, ::-1]
+    assert np.allclose(dv, want, atol=1e-13)
+    # a single key: P = 1, so dS = 0 and dV_0 = sum of dO
+    dq, dk, dv = oracle.attn_bwd(q, k[:, :, :1], v[:, :, :1], do, causal=False, scale=0.7)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    assert np.allclose(dv[:, :, 0], do.reshape(B, Hkv, g, N, d).sum(axis=(2, 3)), atol=1e-12)
+    # dO = 0: no gradient at all
+    z = oracle.attn_bwd(q, k, v, np.zeros_like(do), causal=True, scale=0.3)
+    assert all(np.abs(a).max() == 0.0 for a in z)
+
+
+def pin_bwd_empty_rows(oracle):
+    """Nq > Nk causal: the first Nq - Nk queries see no key; they get dQ = 0
+    and add nothing, and the rest behave as the square problem (their masks
+    are the same)."""
+    B, H, Nq, Nk, d = 1, 2, 30, 18, 8
+    q, k, v, do = _bwd_inputs((B, H, Nq, d), (B, H, Nk, d), 60)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=True, scale=0.5)
+    e = Nq - Nk
+    assert np.abs(dq[:, :, :e]).max() == 0.0
+    ref = _torch_grads(q[:, :, e:], k, v, do[:, :, e:], True, 0.5)
+    assert np.allclose(dq[:, :, e:], ref[0], atol=1e-11)
+    assert np.allclose(dk, ref[1], atol=1e-11) and np.allclose(dv, ref[2], atol=1e-11)
 
 
 # --------------------------------------------------------------------------
@@ -354,4 +473,5 @@ ALL_PINS = [
     pin_rotation_invariance, pin_online_recurrence, pin_row_subset,
     pin_e4m3_decode, pin_e4m3_encode, pin_fwht, pin_quantiser, pin_flop_convention,
     pin_rope_complex, pin_rope_layouts, pin_rope_relative_position, pin_rope_quantiser,
+    pin_bwd_autograd, pin_bwd_finite_difference, pin_bwd_invariants, pin_bwd_empty_rows,
 ]

@@ -33,6 +33,14 @@ MUTANTS = {
     "rope_pairing": ("const int64_t ib = (layout == 1) ? 2 * i + 1 : i + half;",
                      "const int64_t ib = (layout == 1) ? 2 * i + 1 : half - 1 - i;"),
     "rope_position": ("const int64_t n = r % N;", "const int64_t n = r / N;"),
+    "bwd_D_dropped": ("const double ds = p[j] * (dp[j] - Di);", "const double ds = p[j] * dp[j];"),
+    "bwd_dk_operand": ("dkj[c] += scale * ds * qi[c];", "dkj[c] += scale * ds * kj[c];"),
+    "bwd_dq_scale": ("dqi[c] += scale * ds * kj[c];", "dqi[c] += ds * kj[c];"),
+    "bwd_dv_operand": ("dvj[c] += p[j] * doi[c];", "dvj[c] += p[j] * qi[c];"),
+    "bwd_unnormalised": ("for (int64_t j = 0; j < jend; ++j) p[j] /= l;",
+                         "for (int64_t j = 0; j < jend; ++j) p[j] /= 1.0;"),
+    "bwd_dp_operand": ("for (int64_t c = 0; c < d; ++c) dot += doi[c] * vj[c];",
+                       "for (int64_t c = 0; c < d; ++c) dot += qi[c] * vj[c];"),
 }
 
 
