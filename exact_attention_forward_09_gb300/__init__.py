@@ -17,7 +17,7 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["fwd_splitkv", "splitkv_workspace_bytes", "fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
+__all__ = ["bwd", "bwd_workspace_bytes", "fwd_splitkv", "splitkv_workspace_bytes", "fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
            "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
            "FA_ROPE_INTERLEAVED", "FA_ROPE_HALF",
@@ -68,6 +68,11 @@ def _lib():
         lib.fa_quant_fp8_rope.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
         lib.fa_quant_fp8_per_tensor_noalloc.restype = i32
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32,
+                               vp, ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = i32
+        lib.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_bwd_workspace_bytes.restype = i32
         lib.fa_status_string.argtypes = [i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_check_device_error.argtypes = [vp]
@@ -162,6 +167,47 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool 
                                    wp, wb, _stream(q))
     _check(st, "fa_fwd_splitkv")
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, Hq: int, Nq: int, d: int) -> int:
+    """Bytes of device workspace ``fa_bwd`` needs for this shape."""
+    n = ctypes.c_size_t(0)
+    _check(_lib().fa_bwd_workspace_bytes(B, Hq, Nq, d, ctypes.byref(n)), "fa_bwd_workspace_bytes")
+    return int(n.value)
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, causal: bool = False, scale: float | None = None, dq: torch.Tensor | None = None,
+        dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Gradients of sum(dout * O) (``fa_bwd``): q, out, dout [B, Hq, Nq, d],
+    k/v [B, Hkv, Nk, d], lse [B, Hq, Nq] fp32 from the forward with the same
+    causal flag and scale.  Returns (dq, dk, dv)."""
+    _check_gqa(q, k, v, (torch.bfloat16, torch.float16))
+    for name, t in (("out", out), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() \
+                or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous tensor with q's shape, dtype and device")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if not isinstance(lse, torch.Tensor) or lse.shape != (B, Hq, Nq) or lse.dtype != torch.float32 \
+            or not lse.is_contiguous() or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dt = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    with torch.cuda.device(q.device):
+        need = bwd_workspace_bytes(B, Hq, Nq, d)
+        if workspace is None:
+            workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+        st = _lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), dt,
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(q))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def _check_gqa(q, k, v, allowed):

@@ -18,8 +18,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
 UNITS = ["api.cu", "attn_bf16.cu", "attn_fp16.cu", "attn_fp8.cu", "quant_fp8.cu", "quant_fp8_noalloc.cu",
-         "splitkv.cu", "attn_split_bf16.cu", "attn_split_fp16.cu"]
-HEADERS = ["ptx.cuh", "attn_fwd.cuh", "quant_fp8.h"]
+         "splitkv.cu", "attn_split_bf16.cu", "attn_split_fp16.cu", "attn_bwd.cu"]
+HEADERS = ["ptx.cuh", "attn_fwd.cuh", "quant_fp8.h", "attn_bwd.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -16,6 +16,7 @@
 #include "attn_fwd.cuh"
 #include "splitkv.h"
 #include "quant_fp8.h"
+#include "attn_bwd.h"
 
 namespace fa {
 template <int ELEM, int D, bool CAUSAL, bool SPLIT>
@@ -76,12 +77,13 @@ fa_status device_setup(int* dev_out, int** err_out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 3-D tiled map over a contiguous [BH, N, d] tensor: box = (128-byte row
-// chunk) x 128 rows x 1 head, 128-byte swizzle, out-of-range rows read as 0.
+// chunk) x box_rows rows x 1 head, 128-byte swizzle, out-of-range rows read
+// as 0.
 fa_status encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t BH,
-                     int64_t N, int64_t d) {
+                     int64_t N, int64_t d, uint32_t box_rows = 128) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)(d * elem_bytes), (cuuint64_t)(N * d * elem_bytes)};
-  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), 128u, 1u};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), box_rows, 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -406,6 +408,92 @@ fa_status fa_quant_fp8_rope(const float* x, void* x8, float* descale, int64_t B,
   if (rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
   return quant_impl(x, x8, descale, B, H, N, d, rope_cos, rope_sin, rope_layout, hadamard_signs, per_tensor,
                     workspace, stream);
+}
+
+fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 0 || Nq < 0 || d < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  const int64_t rows = B * Hq * Nq;
+  if (rows > (int64_t)1 << 40) return FA_ERR_UNSUPPORTED;
+  const int64_t acc = (rows * d * 4 + 255) / 256 * 256;   // fp32 dQ accumulator
+  const int64_t drow = (rows * 4 + 255) / 256 * 256;      // D_i = dO_i . O_i
+  *bytes = (size_t)(acc + drow);
+  return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                 int causal, float scale, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (d != 128) return FA_ERR_UNSUPPORTED;  // the backward kernel covers d = 128
+  if (B == 0 || Hq == 0) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0 || Nk == 0) return FA_ERR_INVALID_ARG;
+  const int64_t lim = 0x7fffffffLL - 256;
+  if (Nq > lim || Nk > lim || B * Hq > 0x7fffffffLL || B * Hkv * ((Nk + 127) / 128) > 0x7fffffffLL ||
+      B * Hq * Nq > ((int64_t)1 << 40))
+    return FA_ERR_UNSUPPORTED;
+  if (!k || !v || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st;
+  if (Nq == 0) {
+    // no query: dK = dV = 0
+    if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+    const long long bytes = (long long)(B * Hkv * Nk * d * 2);
+    if (fa::launch_zero_fill(dk, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_zero_fill(dv, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  if (!q || !o || !lse || !dout || !dq) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq))
+    return FA_ERR_INVALID_ARG;
+  size_t need = 0;
+  if ((st = fa_bwd_workspace_bytes(B, Hq, Nq, d, &need)) != FA_OK) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return FA_ERR_INVALID_ARG;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  const int64_t rows = B * Hq * Nq;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* drow = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  if (fa::launch_bwd_prep(o, dout, drow, dq_acc, (long long)rows, (int)d, f16, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+
+  fa::BwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((st = encode_map(&L.q, q, dt, 2, B * Hq, Nq, d, 64)) != FA_OK) return st;
+  if ((st = encode_map(&L.dout, dout, dt, 2, B * Hq, Nq, d, 64)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
+  L.prm.dq_acc = dq_acc;
+  L.prm.dk = dk;
+  L.prm.dv = dv;
+  L.prm.lse = lse;
+  L.prm.drow = drow;
+  L.prm.err = err;
+  L.prm.Nq = (int)Nq;
+  L.prm.Nk = (int)Nk;
+  L.prm.Hq = (int)Hq;
+  L.prm.Hkv = (int)Hkv;
+  L.prm.BHkv = (int)(B * Hkv);
+  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  L.prm.scale = scale;
+  L.stream = stream;
+  cudaError_t e;
+  if (f16) e = causal ? fa::launch_attn_bwd<1, 128, true>(L) : fa::launch_attn_bwd<1, 128, false>(L);
+  else e = causal ? fa::launch_attn_bwd<0, 128, true>(L) : fa::launch_attn_bwd<0, 128, false>(L);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::launch_bwd_dq_convert(dq_acc, dq, scale, (long long)(rows * d), f16, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 const char* fa_status_string(fa_status status) {

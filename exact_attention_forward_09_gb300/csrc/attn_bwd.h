@@ -1,0 +1,46 @@
+// attn_bwd.h -- launch interface of the attention backward kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct BwdParams {
+  float* dq_acc;       // [BHq, Nq, D] fp32, zeroed by the preprocessing kernel
+  void* dk;            // [BHkv, Nk, D] bf16 / f16
+  void* dv;            // [BHkv, Nk, D]
+  const float* lse;    // [BHq, Nq] natural-log row log-sum-exp of the forward
+  const float* drow;   // [BHq, Nq] D_i = dO_i . O_i
+  int* err;            // device error word
+  int Nq, Nk;          // query rows / keys per head
+  int Hq, Hkv;         // heads (Hq % Hkv == 0)
+  int BHkv;            // batch x key/value heads
+  float scale_log2;    // scale * log2(e)
+  float scale;         // dK = scale * dS^T Q
+};
+
+struct BwdLaunch {
+  CUtensorMap q, dout;  // [BHq, Nq, D], 64-row boxes
+  CUtensorMap k, v;     // [BHkv, Nk, D], 128-row boxes
+  BwdParams prm;
+  cudaStream_t stream;
+};
+
+// ELEM: 0 bf16, 1 f16 (the forward's element kinds)
+template <int ELEM, int D, bool CAUSAL>
+cudaError_t launch_attn_bwd(const BwdLaunch& L);
+
+// D_i = sum_c dO_ic O_ic for every row, and dq_acc := 0.
+cudaError_t launch_bwd_prep(const void* o, const void* dout, float* drow, float* dq_acc, long long rows, int d,
+                            bool f16, cudaStream_t stream);
+
+// dq = RN(scale * dq_acc) in the element type.
+cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, float scale, long long elems, bool f16,
+                                  cudaStream_t stream);
+
+// Zero `bytes` bytes (a multiple of 16, 16-byte aligned).
+cudaError_t launch_zero_fill(void* p, long long bytes, cudaStream_t stream);
+
+}  // namespace fa

@@ -174,6 +174,51 @@ fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t
                                      int num_splits, size_t* bytes);
 
 /*
+ * fa_bwd -- gradients of the loss sum(dout * O) for O = fa_fwd_gqa(q, k, v):
+ * dq, dk, dv (the pages list the backward pass dQ, dK, dV among the paths a
+ * test must cover and compare its speed with FA2: "FlashAttention-3: async
+ * pipelines on Hopper", sections "correctness validation must cover
+ * asynchronous boundaries" and "how to read the paper's performance
+ * numbers").  With P = softmax(scale q k^T) recomputed from the forward's
+ * LSE, dP = dout v^T, D_i = dout_i . o_i and dS = P * (dP - D):
+ *   dv = P^T dout,   dk = scale dS^T q,   dq = scale dS k,
+ * dk and dv summed over the query heads of each key/value group.
+ *   q, dout, o, dq  [B, Hq, Nq, d]   bf16 or fp16 (dtype), device
+ *   k, v, dk, dv    [B, Hkv, Nk, d]  same dtype, device
+ *   lse             [B, Hq, Nq] fp32, the natural-log LSE fa_fwd_gqa wrote
+ *                   for the same q, k, v, causal and scale (-inf: a row that
+ *                   sees no key; it gets dq = 0 and adds nothing)
+ *   causal          0 / 1, masks aligned at the bottom right as in fa_fwd_gqa
+ *   workspace       DEVICE pointer, 256-byte aligned, owned by the caller, at
+ *                   least fa_bwd_workspace_bytes(B, Hq, Nq, d) bytes (an fp32
+ *                   dQ accumulator and one float per query row); overwritten;
+ *                   calls sharing it must not overlap on the GPU
+ * q, k, v, o, lse, dout are read only; dq, dk, dv are fully overwritten.
+ * All pointers 16-byte aligned.  Asynchronous on `stream` (four kernels:
+ * D and accumulator clear, the fused gradient kernel, dQ conversion), no
+ * host synchronisation, no allocation.  dq is accumulated across key tiles
+ * with fp32 reduce-adds, so its rounding may differ between runs.
+ * Errors: FA_ERR_INVALID_ARG for bad pointers, alignment, sizes, dtype,
+ * causal flag, scale or workspace; FA_ERR_UNSUPPORTED for d other than 128
+ * (the backward kernel's head dimension) or a device other than sm_103;
+ * FA_ERR_CUDA for a launch failure; a pipeline timeout is reported by
+ * fa_check_device_error.  B*Hq = 0 is a no-op; Nq = 0 writes dk = dv = 0.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv,
+                 int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                 int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs:
+ * B*Hq*Nq*d*4 (fp32 dQ accumulator) + B*Hq*Nq*4 (row terms D), each rounded
+ * up to 256.  Writes *bytes.  FA_ERR_INVALID_ARG for negative sizes or a null
+ * `bytes`, FA_ERR_UNSUPPORTED for d not in {64, 128, 256}.
+ */
+fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, size_t* bytes);
+
+/*
  * fa_quant_fp8 -- quantise fp32 [B, H, N, d] to E4M3 with one scale per
  * 128-row block (per_tensor = 0) or one scale for the whole tensor
  * (per_tensor = 1, the baseline), optionally after the incoherent-processing

@@ -109,6 +109,32 @@ def test_host_argument_checks(fa_lib):
                                     None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_quant_fp8_rope(None, None, None, 0, 1, 1, 128, None, None, fa.FA_ROPE_HALF, None, 0, None,
                                     None) == fa.FA_OK
+    # backward: d = 128 only; workspace present, aligned and large enough; empty batch a no-op
+    ws = 1 << 24
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 64, 0, 0.1, 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 96, 0, 0.1, 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, None, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws + 16, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG  # 256-byte alignment
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws, 100,
+                         None) == fa.FA_ERR_INVALID_ARG  # too small
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 3, 2, 64, 64, 128, 0, 0.1, 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG  # Hq % Hkv
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 128, 2, 0.1, 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG  # causal flag
+    assert fa_lib.fa_bwd(p, p, p, p, p + 4, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG  # misaligned lse
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, float("nan"), 0, ws, 1 << 20,
+                         None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_bwd(None, None, None, None, None, None, None, None, None, 0, 2, 2, 64, 64, 128, 0, 0.1, 0,
+                         None, 0, None) == fa.FA_OK
+    assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_OK
+    assert nbytes.value == 2 * 4 * 100 * 128 * 4 + (2 * 4 * 100 * 4 + 255) // 256 * 256
+    assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 96, ctypes.byref(nbytes)) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_bwd_workspace_bytes(-1, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

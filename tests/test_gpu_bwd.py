@@ -1,0 +1,174 @@
+"""Attention backward (fa_bwd) against the fp64 oracle's gradients.
+
+The backward kernel gets the forward's O and LSE as inputs.  The parity
+tests give it the oracle's (O rounded to the element type like the forward's
+output, LSE in fp32), so that what is measured is the backward kernel's own
+error; ``test_bwd_end_to_end`` chains the GPU forward into it, as in
+training.  The oracle differentiates the definition directly from the same
+low-precision q, k, v, dO.  Errors are normalised by the reference: the
+largest error by the largest |reference| entry, the rms error by the
+reference's rms.  Bounds come from the element type's unit roundoff u (2^-8
+bf16, 2^-11 fp16): the outputs are rounded once (up to u/2 relative), P and
+dS are rounded to the element type before their products, and D = dO . O
+inherits O's rounding (a per-row error that grows as the softmax gets
+peakier); the bounds allow 2.5 u for the largest error and 1.25 u for the
+rms.  A CPU emulation of exactly these roundings gives up to 1.6 u and
+0.9 u over the scales tested here.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+UNIT = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_09_gb300 as fa
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+    return fa
+
+
+def _inputs(B, Hq, Hkv, Nq, Nk, d, seed, dtype):
+    q = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 0)).to(dtype)
+    k = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 1)).to(dtype)
+    v = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 2)).to(dtype)
+    do = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 3)).to(dtype)
+    return q, k, v, do
+
+
+def _gpu_grads(fa, q, k, v, do, causal, scale, forward="oracle"):
+    """GPU gradients; O and LSE from the oracle (rounded like the kernel's
+    outputs) or, with forward="gpu", from the GPU forward."""
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    if forward == "gpu":
+        o, lse = fa.fwd_gqa(qd, kd, vd, causal=causal, scale=scale)
+    else:
+        o64, l64 = oracle.attn_fwd(q, k, v, causal=causal, scale=scale)
+        o = torch.from_numpy(o64).to(q.dtype).cuda()
+        lse = torch.from_numpy(l64).to(torch.float32).cuda()
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    fa.check_device_error()
+    return dq, dk, dv
+
+
+def _check(got, ref, dtype, what):
+    u = UNIT[dtype]
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.float().cpu().numpy().astype(np.float64)
+        assert g.shape == r.shape, f"{what} {name}: shape"
+        assert np.isfinite(g).all(), f"{what} {name}: non-finite values"
+        if r.size == 0:
+            continue
+        e = g - r
+        rmax = np.abs(r).max()
+        rrms = math.sqrt((r ** 2).mean())
+        if rmax == 0.0:
+            # an exactly zero gradient (a single key: dS = 0) comes out as
+            # fp32 rounding residue of P (dP - D)
+            assert np.abs(g).max() <= 1e-5, f"{what} {name}: expected zeros, got {np.abs(g).max():.3e}"
+            continue
+        assert np.abs(e).max() <= 2.5 * u * rmax, f"{what} {name}: max error {np.abs(e).max() / rmax:.3e} of max|ref|"
+        assert math.sqrt((e ** 2).mean()) <= 1.25 * u * rrms, \
+            f"{what} {name}: rms error {math.sqrt((e ** 2).mean()) / rrms:.3e} of rms(ref)"
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk", [
+    (1, 2, 2, 128, 128),    # one key tile, two query tiles
+    (2, 2, 2, 200, 200),    # ragged tails of both
+    (1, 4, 2, 256, 384),    # grouped queries, Nq != Nk
+    (1, 2, 2, 100, 300),    # few queries, many keys
+    (1, 2, 2, 300, 100),    # causal: the first 200 rows see no key
+    (1, 3, 1, 64, 64),      # multi-query
+    (1, 1, 1, 1, 1),        # smallest
+    (1, 2, 1, 37, 1000),    # short queries against a long sequence
+])
+def test_bwd_parity(fa, dtype, causal, B, Hq, Hkv, Nq, Nk):
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = _inputs(B, Hq, Hkv, Nq, Nk, d, 900 + Nq + 7 * Nk + Hkv, dtype)
+    got = _gpu_grads(fa, q, k, v, do, causal, scale)
+    ref = oracle.attn_bwd(q, k, v, do, causal=causal, scale=scale)
+    _check(got, ref, dtype, f"B={B} Hq={Hq} Hkv={Hkv} Nq={Nq} Nk={Nk} causal={causal} {dtype}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2, 0.3])
+def test_bwd_scales(fa, scale):
+    d = 128
+    q, k, v, do = _inputs(1, 2, 2, 192, 192, d, 77, torch.bfloat16)
+    for causal in (False, True):
+        got = _gpu_grads(fa, q, k, v, do, causal, scale)
+        ref = oracle.attn_bwd(q, k, v, do, causal=causal, scale=scale)
+        _check(got, ref, torch.bfloat16, f"scale={scale} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_end_to_end(fa, dtype, causal):
+    """GPU forward -> GPU backward at the usual scale 1/sqrt(d)."""
+    d = 128
+    q, k, v, do = _inputs(2, 4, 2, 333, 333, d, 4242, dtype)
+    got = _gpu_grads(fa, q, k, v, do, causal, 1.0 / math.sqrt(d), forward="gpu")
+    ref = oracle.attn_bwd(q, k, v, do, causal=causal, scale=1.0 / math.sqrt(d))
+    _check(got, ref, dtype, f"end to end causal={causal} {dtype}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_mid_sampled_heads(fa, causal):
+    """The benchmark's backward workload (B=4, H=16, N=2048, d=128, bf16) in
+    one call; the oracle checks whole heads (every gradient entry of the
+    head), the first and the last."""
+    B, H, N, d = 4, 16, 2048, 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = _inputs(B, H, H, N, N, d, 1234, torch.bfloat16)
+    dq, dk, dv = _gpu_grads(fa, q, k, v, do, causal, scale, forward="gpu")
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attn_bwd(q[sl], k[sl], v[sl], do[sl], causal=causal, scale=scale)
+        _check((dq[sl], dk[sl], dv[sl]), ref, torch.bfloat16, f"mid head ({b},{h}) causal={causal}")
+
+
+def test_bwd_repeatable_dk_dv(fa):
+    """dK and dV are summed in a fixed order inside one CTA: bit-identical
+    over repeated calls (dQ is added across CTAs in any order)."""
+    q, k, v, do = _inputs(1, 4, 2, 320, 320, 128, 55, torch.bfloat16)
+    a = _gpu_grads(fa, q, k, v, do, True, 0.1)
+    b = _gpu_grads(fa, q, k, v, do, True, 0.1)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_bwd_no_query(fa):
+    k = torch.randn(1, 2, 130, 128, device="cuda").to(torch.bfloat16)
+    v = torch.randn_like(k)
+    q = torch.empty(1, 2, 0, 128, device="cuda", dtype=torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 0, device="cuda", dtype=torch.float32)
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    fa.bwd(q, k, v, o, lse, torch.empty_like(q), dk=dk, dv=dv)
+    fa.check_device_error()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+def test_bwd_rejects(fa):
+    q = torch.randn(1, 1, 64, 64, device="cuda").to(torch.bfloat16)
+    o, lse = fa.fwd(q, q, q)
+    with pytest.raises(fa.FaError) as ei:
+        fa.bwd(q, q, q, o, lse, q)
+    assert ei.value.status == fa.FA_ERR_UNSUPPORTED
+    q = torch.randn(1, 1, 64, 128, device="cuda").to(torch.bfloat16)
+    o, lse = fa.fwd(q, q, q)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as ei:
+        fa.bwd(q, q, q, o, lse, q, workspace=small)
+    assert ei.value.status == fa.FA_ERR_INVALID_ARG
