@@ -417,8 +417,8 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, s
   const int64_t rows = B * Hq * Nq;
   if (rows > (int64_t)1 << 40) return FA_ERR_UNSUPPORTED;
   const int64_t acc = (rows * d * 4 + 255) / 256 * 256;   // fp32 dQ accumulator
-  const int64_t drow = (rows * 4 + 255) / 256 * 256;      // D_i = dO_i . O_i
-  *bytes = (size_t)(acc + drow);
+  const int64_t recs = B * Hq * ((Nq + 63) / 64) * 512;   // per 64-row tile: 64 x (-LSE log2 e), 64 x (-D)
+  *bytes = (size_t)(acc + recs);
   return FA_OK;
 }
 
@@ -461,9 +461,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
   const int64_t rows = B * Hq * Nq;
   float* dq_acc = static_cast<float*>(workspace);
-  float* drow = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
+  float* vecs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
   const bool f16 = dtype == FA_DTYPE_FP16;
-  if (fa::launch_bwd_prep(o, dout, drow, dq_acc, (long long)rows, (int)d, f16, stream) != cudaSuccess)
+  if (fa::launch_bwd_prep(o, dout, lse, vecs, dq_acc, (long long)(B * Hq), (int)Nq, (int)d, f16, stream) !=
+      cudaSuccess)
     return FA_ERR_CUDA;
 
   fa::BwdLaunch L;
@@ -476,8 +477,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   L.prm.dq_acc = dq_acc;
   L.prm.dk = dk;
   L.prm.dv = dv;
-  L.prm.lse = lse;
-  L.prm.drow = drow;
+  L.prm.vecs = vecs;
   L.prm.err = err;
   L.prm.Nq = (int)Nq;
   L.prm.Nk = (int)Nk;

@@ -19,10 +19,13 @@
 // the 64-query tiles of every query head of the group.  Per query tile the
 // MMA warp computes S^T = K Q^T and dP^T = V dO^T into TMEM; the compute
 // warpgroup (one thread per key) turns a row of each into P and dS (bf16 /
-// f16) in shared memory; the MMA warp then accumulates dV += P^T dO and
-// dK += dS^T Q and computes dQ^T = K^T dS^T for the tile, which a second
-// warpgroup (one thread per head-dim column) moves through shared memory and
-// adds to an fp32 dQ accumulator in global memory with a bulk reduce-add.
+// f16), written back to TMEM (dS also to shared memory); the MMA warp then
+// accumulates dV += P^T dO and dK += dS^T Q with the left operand read from
+// TMEM, and computes dQ^T = K^T dS^T for the tile, which a second warpgroup
+// (one thread per head-dim column) adds to an fp32 dQ accumulator in global
+// memory with coalesced reduce-adds.  Shared-memory bandwidth is the scarce
+// resource of this kernel (the tensor core reads its shared-memory operands
+// through it), so nothing that can stay in TMEM or registers goes through it.
 // S^T / dP^T of tile t+1 are issued as soon as tile t's rows are read out,
 // so the tensor core runs them while the compute warpgroup works on tile t.
 // A preprocessing kernel forms D and clears the dQ accumulator; a last
@@ -51,15 +54,13 @@ struct BwdCfg {
   static constexpr int Q_PANEL = kBQ * 128;        // one panel of a Q or dO tile
   static constexpr int KV_BYTES = NCH * KV_PANEL;
   static constexpr int QT_BYTES = NCH * Q_PANEL;
-  static constexpr int NST = 3;                    // Q/dO stages
+  static constexpr int NST = 4;                    // Q/dO stages
   static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q, then dO
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int OFF_ST = OFF_V + KV_BYTES;
-  static constexpr int OFF_P = OFF_ST + NST * STAGE_BYTES;
-  static constexpr int OFF_DS = OFF_P + kBK * kBQ * 2;
-  static constexpr int OFF_DQ = OFF_DS + kBK * kBQ * 2;   // dQ tile staging, fp32 [kBQ][D]
-  static constexpr int OFF_VEC = OFF_DQ + kBQ * D * 4;    // per stage: log2-scaled LSE[kBQ], D[kBQ]
+  static constexpr int OFF_DS = OFF_ST + NST * STAGE_BYTES;
+  static constexpr int OFF_VEC = OFF_DS + kBK * kBQ * 2;  // per stage: -LSE log2(e) [kBQ], -D [kBQ]
   static constexpr int OFF_BAR = OFF_VEC + NST * 2 * kBQ * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemCap, "shared memory budget");
@@ -67,29 +68,35 @@ struct BwdCfg {
   static constexpr uint32_t COL_DK = D;
   static constexpr uint32_t COL_S = 2 * D;
   static constexpr uint32_t COL_DP = 2 * D + kBQ;
-  static constexpr uint32_t COL_DQ = 2 * D + 2 * kBQ;  // two buffers of kBQ columns
+  static constexpr uint32_t COL_DQ = 2 * D + 2 * kBQ;
+  static constexpr uint32_t COL_P = COL_DQ + kBQ;       // P, 16-bit pairs: kBQ / 2 columns
+  static constexpr uint32_t COL_DSM = COL_P + kBQ / 2;  // dS, likewise
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(COL_DQ + 2 * kBQ <= TMEM_COLS, "TMEM budget");
+  static_assert(COL_DSM + kBQ / 2 <= TMEM_COLS, "TMEM budget");
   static constexpr uint32_t FMT = (ELEM == 0) ? 1u : 0u;  // bf16 = 1, f16 = 0
   static constexpr uint32_t IDESC_S = instr_desc(FMT, FMT, 0, 0, kBK, kBQ);  // S^T, dP^T
   static constexpr uint32_t IDESC_KV = instr_desc(FMT, FMT, 0, 1, kBK, D);   // dV, dK
   static constexpr uint32_t IDESC_DQ = instr_desc(FMT, FMT, 1, 1, D, kBQ);   // dQ^T
-  static constexpr int DQ_WARP0 = 4;  // warps 0-3: compute (thread = key); 4-7: dQ (thread = column)
-  static constexpr int LOAD_WARP = 8;
-  static constexpr int MMA_WARP = 9;
-  static constexpr int THREADS = 320;
+  // warps 0-7: compute, two warpgroups (thread = key) that split each
+  // step's kBQ query columns in halves; 8-11: dQ (thread = head-dim column)
+  static constexpr int COMPUTE_WARPS = 8;
+  static constexpr int HALF_Q = kBQ / 2;  // query columns per compute warpgroup
+  static constexpr int DQ_WARP0 = 8;
+  static constexpr int LOAD_WARP = 12;
+  static constexpr int MMA_WARP = 13;
+  static constexpr int THREADS = 448;
 };
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t st_full[3];
-  uint64_t st_empty[3];
+  uint64_t st_full[4];
+  uint64_t st_empty[4];
   uint64_t s_full;
   uint64_t s_free;
   uint64_t p_full;
   uint64_t p_free;
-  uint64_t dq_full[2];
-  uint64_t dq_free[2];
+  uint64_t dq_full;
+  uint64_t dq_free;
   uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -110,7 +117,7 @@ __device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity) {
 }
 
 template <int ELEM, int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const BwdParams prm) {
@@ -157,17 +164,15 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bars->st_full[s], 32);
+      mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->st_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 128);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->s_free, 32 * C::COMPUTE_WARPS);
+    mbar_init(&bars->p_full, 32 * C::COMPUTE_WARPS);
     mbar_init(&bars->p_free, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->dq_full[b], 1);
-      mbar_init(&bars->dq_free[b], 128);
-    }
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -184,62 +189,42 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ load --
-    // Lane 0 issues the TMA copies; all lanes stage the per-row LSE (scaled
-    // to log2 units) and D of each query tile, and all arrive on the stage.
-    if (T > 0) {
-      bool ok = true;
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_do);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
-        for (int ch = 0; ch < C::NCH; ++ch) {
-          tma_load_3d(smem + C::OFF_K + ch * C::KV_PANEL, &tm_k, &bars->kv_full, ch * 64, k0, bkv);
-          tma_load_3d(smem + C::OFF_V + ch * C::KV_PANEL, &tm_v, &bars->kv_full, ch * 64, k0, bkv);
-        }
+    // Lane 0 issues every copy: K and V once, then per step the Q and dO
+    // tiles and the tile's 64 log2-scaled LSE values and 64 D values (one
+    // contiguous 512-byte record prepared by the preprocessing kernel), all
+    // counted on the stage's barrier.
+    if (T > 0 && lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
+      for (int ch = 0; ch < C::NCH; ++ch) {
+        tma_load_3d(smem + C::OFF_K + ch * C::KV_PANEL, &tm_k, &bars->kv_full, ch * 64, k0, bkv);
+        tma_load_3d(smem + C::OFF_V + ch * C::KV_PANEL, &tm_v, &bars->kv_full, ch * 64, k0, bkv);
       }
       int t = 0;
       for (; t < T; ++t) {
         const int s = t % C::NST;
-        if (t >= C::NST) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bars->st_empty[s], (uint32_t)(((t / C::NST) - 1) & 1), abort_flag, prm.err));
-          if (!ok) break;
-        }
+        if (t >= C::NST &&
+            !mbar_wait(&bars->st_empty[s], (uint32_t)(((t / C::NST) - 1) & 1), abort_flag, prm.err))
+          break;
         int bhq, q0;
         step_of(t, bhq, q0);
-        float* l2s = vec + s * 2 * kBQ;
-        float* drs = l2s + kBQ;
-        for (int e = lane; e < kBQ; e += 32) {
-          const int i = q0 + e;
-          float l2 = INFINITY, dr = 0.0f;  // rows past Nq: P = 0
-          if (i < Nq) {
-            const float l = prm.lse[(size_t)bhq * Nq + i];
-            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;  // a row with no key: P = 0
-            dr = prm.drow[(size_t)bhq * Nq + i];
-          }
-          l2s[e] = l2;
-          drs[e] = dr;
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QT_BYTES + 2 * kBQ * 4);
+        uint8_t* st = smem + C::OFF_ST + s * C::STAGE_BYTES;
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          tma_load_3d(st + ch * C::Q_PANEL, &tm_q, &bars->st_full[s], ch * 64, q0, bhq);
+          tma_load_3d(st + C::QT_BYTES + ch * C::Q_PANEL, &tm_do, &bars->st_full[s], ch * 64, q0, bhq);
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QT_BYTES);
-          uint8_t* st = smem + C::OFF_ST + s * C::STAGE_BYTES;
-          for (int ch = 0; ch < C::NCH; ++ch) {
-            tma_load_3d(st + ch * C::Q_PANEL, &tm_q, &bars->st_full[s], ch * 64, q0, bhq);
-            tma_load_3d(st + C::QT_BYTES + ch * C::Q_PANEL, &tm_do, &bars->st_full[s], ch * 64, q0, bhq);
-          }
-        } else {
-          mbar_arrive(&bars->st_full[s]);
-        }
+        bulk_load(vec + s * 2 * kBQ, prm.vecs + ((size_t)bhq * nqt + q0 / kBQ) * (2 * kBQ), 2 * kBQ * 4,
+                  &bars->st_full[s]);
       }
       // never leave with copies in flight: the K/V tile and each stage's last fill
-      if (lane == 0) {
-        settle(&bars->kv_full, 0);
-        for (int i = 0; i < C::NST && i < t; ++i) {
-          const int tl = t - 1 - i;
-          settle(&bars->st_full[tl % C::NST], (uint32_t)((tl / C::NST) & 1));
-        }
+      settle(&bars->kv_full, 0);
+      for (int i = 0; i < C::NST && i < t; ++i) {
+        const int tl = t - 1 - i;
+        settle(&bars->st_full[tl % C::NST], (uint32_t)((tl / C::NST) & 1));
       }
     }
     __syncwarp();
@@ -257,8 +242,6 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t k_kdesc = smem_desc(k_s, 16, 1024, 2);
       const uint64_t v_kdesc = smem_desc(v_s, 16, 1024, 2);
       const uint64_t st_kdesc = smem_desc(st_s, 16, 1024, 2);
-      const uint64_t p_kdesc = smem_desc(smem_u32(smem + C::OFF_P), 16, 1024, 2);
-      const uint64_t ds_kdesc = smem_desc(smem_u32(smem + C::OFF_DS), 16, 1024, 2);
       // MN-major views: the next 64 columns of the MN dimension one panel on
       const uint64_t st_mdesc = smem_desc(st_s, C::Q_PANEL, 1024, 2);   // Q, dO as [K = query][N = d]
       const uint64_t k_mdesc = smem_desc(k_s, C::KV_PANEL, 1024, 2);    // K as [K = key][M = d]
@@ -277,28 +260,27 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss_elect<0>(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
         }
       };
-      // dV += P^T dO  and  dK += dS^T Q  over the kBQ queries of stage s
+      // dV += P^T dO  and  dK += dS^T Q  over the kBQ queries of stage s,
+      // P^T and dS^T read from TMEM (16 queries = 8 columns per step)
       auto issue_kv = [&](int s, bool acc) {
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks) {
-          const uint64_t a = p_kdesc + (uint64_t)((ks * 32) >> 4);
           const uint64_t b = st_mdesc + (uint64_t)((s * C::STAGE_BYTES + C::QT_BYTES + ks * 2048) >> 4);
-          mma_ss_elect<0>(tmem + C::COL_DV, a, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
+          mma_ts_elect<0>(tmem + C::COL_DV, tmem + C::COL_P + ks * 8, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks) {
-          const uint64_t a = ds_kdesc + (uint64_t)((ks * 32) >> 4);
           const uint64_t b = st_mdesc + (uint64_t)((s * C::STAGE_BYTES + ks * 2048) >> 4);
-          mma_ss_elect<0>(tmem + C::COL_DK, a, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
+          mma_ts_elect<0>(tmem + C::COL_DK, tmem + C::COL_DSM + ks * 8, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
         }
       };
-      // dQ^T (d x queries) = K^T dS^T over the kBK keys, into buffer bq
-      auto issue_dq = [&](int bq) {
+      // dQ^T (d x queries) = K^T dS^T over the kBK keys
+      auto issue_dq = [&]() {
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks) {
           const uint64_t a = k_mdesc + (uint64_t)((ks * 2048) >> 4);
           const uint64_t b = ds_mdesc + (uint64_t)((ks * 2048) >> 4);
-          mma_ss_elect<0>(tmem + C::COL_DQ + bq * kBQ, a, b, C::IDESC_DQ, ks > 0 ? 1u : 0u);
+          mma_ss_elect<0>(tmem + C::COL_DQ, a, b, C::IDESC_DQ, ks > 0 ? 1u : 0u);
         }
       };
 
@@ -327,14 +309,13 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         issue_kv(s, t > 0);
         mma_commit_elect(&bars->st_empty[s]);  // last reads of this stage's Q and dO
-        const int bq = t & 1;
-        if (t >= 2) {
-          ok = warp_wait(&bars->dq_free[bq], (uint32_t)(((t >> 1) - 1) & 1));
+        if (t >= 1) {
+          ok = warp_wait(&bars->dq_free, (uint32_t)((t - 1) & 1));
           if (!ok) break;
           tc_fence_after();
         }
-        issue_dq(bq);
-        mma_commit_elect(&bars->dq_full[bq]);
+        issue_dq();
+        mma_commit_elect(&bars->dq_full);
         mma_commit_elect(&bars->p_free);  // last reads of P and dS
       }
       if (ok) mma_commit_elect(&bars->acc_full);
@@ -343,12 +324,16 @@ __global__ void __launch_bounds__(320, 1)
       settle(&bars->drain, 0);
     }
     __syncwarp();
-  } else if (warp < C::DQ_WARP0) {
+  } else if (warp < C::COMPUTE_WARPS) {
     // --------------------------------------------------------- compute --
-    const int r = threadIdx.x;                       // key within the tile = TMEM lane
-    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    // Warpgroup g handles query columns [g * HALF_Q, (g + 1) * HALF_Q) of
+    // each step; thread r of a warpgroup owns key r (TMEM lane r).
+    const int cg = warp / 4;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     const int key = k0 + r;
-    const float sl2 = prm.scale_log2;
+    const int cb = cg * C::HALF_Q;
+    const float2 sl2 = make_float2(prm.scale_log2, prm.scale_log2);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::NST;
@@ -359,48 +344,52 @@ __global__ void __launch_bounds__(320, 1)
                                                  prm.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sa[32], sb[32], pa[32], pb[32];
-      tmem_ld32(tmem + lane_addr + C::COL_S, sa);
-      tmem_ld32(tmem + lane_addr + C::COL_S + 32, sb);
-      tmem_ld32(tmem + lane_addr + C::COL_DP, pa);
-      tmem_ld32(tmem + lane_addr + C::COL_DP + 32, pb);
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lane_addr + C::COL_S + cb, sr);
+      tmem_ld32(tmem + lane_addr + C::COL_DP + cb, dr);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->s_free);
 
-      const float* l2s = vec + s * 2 * kBQ;
-      const float* drs = l2s + kBQ;
+      // the step's -LSE * log2(e) and -D values, this warpgroup's columns
+      const float* nl2 = vec + s * 2 * kBQ + cb;
+      const float* nd = vec + s * 2 * kBQ + kBQ + cb;
       // causal: columns c < lim are keys past the query's last visible key
       int lim = 0;
       bool need_mask = false;
       if constexpr (CAUSAL) {
-        lim = key - koff - q0;
-        need_mask = (k0 + kBK - 1 - koff - q0) > 0;  // same for the whole CTA step
+        lim = key - koff - q0 - cb;
+        need_mask = (k0 + kBK - 1 - koff - q0 - cb) > 0;  // same for the whole warpgroup
       }
-      uint32_t pp[32], dd[32];
-      auto half = [&](const uint32_t(&sr)[32], const uint32_t(&dr)[32], int cb) {
+      uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(l2s + cb + i);
-          const float4 d4 = *reinterpret_cast<const float4*>(drs + cb + i);
-          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float p = ex2(fmaf(__uint_as_float(sr[i + u]), sl2, -la[u]));
-            if (CAUSAL && need_mask) p = (cb + i + u < lim) ? 0.0f : p;
-            pv[u] = p;
-            dv[u] = p * (__uint_as_float(dr[i + u]) - da[u]);
-          }
-          pp[(cb + i) / 2] = pack2<ELEM>(pv[0], pv[1]);
-          pp[(cb + i) / 2 + 1] = pack2<ELEM>(pv[2], pv[3]);
-          dd[(cb + i) / 2] = pack2<ELEM>(dv[0], dv[1]);
-          dd[(cb + i) / 2 + 1] = pack2<ELEM>(dv[2], dv[3]);
+      for (int i = 0; i < 32; i += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);
+        const float4 d4 = *reinterpret_cast<const float4*>(nd + i);
+        // P = 2^(s * scale * log2 e - LSE * log2 e), in pairs
+        const float2 x01 = fma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2,
+                                make_float2(l4.x, l4.y));
+        const float2 x23 = fma2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2,
+                                make_float2(l4.z, l4.w));
+        float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+        if (CAUSAL && need_mask) {
+          p0 = (i < lim) ? 0.0f : p0;
+          p1 = (i + 1 < lim) ? 0.0f : p1;
+          p2 = (i + 2 < lim) ? 0.0f : p2;
+          p3 = (i + 3 < lim) ? 0.0f : p3;
         }
-      };
-      half(sa, pa, 0);
-      half(sb, pb, 32);
+        // dS = P (dP - D)
+        const float2 g01 = add2(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
+                                make_float2(d4.x, d4.y));
+        const float2 g23 = add2(make_float2(__uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3])),
+                                make_float2(d4.z, d4.w));
+        const float2 s01 = mul2(make_float2(p0, p1), g01);
+        const float2 s23 = mul2(make_float2(p2, p3), g23);
+        pp[i / 2] = pack2<ELEM>(p0, p1);
+        pp[i / 2 + 1] = pack2<ELEM>(p2, p3);
+        dd[i / 2] = pack2<ELEM>(s01.x, s01.y);
+        dd[i / 2 + 1] = pack2<ELEM>(s23.x, s23.y);
+      }
 
       // P and dS of the previous step have been consumed
       if (t > 0) {
@@ -408,16 +397,20 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      // row r of P and dS, 128-byte swizzle: 16-byte chunk c at c ^ (r % 8)
-      uint8_t* prow = smem + C::OFF_P + r * 128;
+      // P and dS into TMEM (left operands of dV and dK; 16-bit pairs) ...
+      tmem_st16(tmem + lane_addr + C::COL_P + cb / 2, pp);
+      tmem_st16(tmem + lane_addr + C::COL_DSM + cb / 2, dd);
+      // ... and dS into row r of shared memory (right operand of dQ^T),
+      // 128-byte swizzle: 16-byte chunk c at c ^ (r % 8)
       uint8_t* drow = smem + C::OFF_DS + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const int pc = (ch ^ (r & 7)) * 16;
-        *reinterpret_cast<uint4*>(prow + pc) = make_uint4(pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2], pp[4 * ch + 3]);
+      for (int ch = 0; ch < 4; ++ch) {
+        const int pc = ((ch + 4 * cg) ^ (r & 7)) * 16;
         *reinterpret_cast<uint4*>(drow + pc) = make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
       }
       fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
     // epilogue: dV and scale * dK rows of this tile's keys
@@ -426,9 +419,10 @@ __global__ void __launch_bounds__(320, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
+      // warpgroup 0 stores dV, warpgroup 1 scale * dK
       const bool store = key < Nk;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = cg;
         const uint32_t col = which ? C::COL_DK : C::COL_DV;
         const float mult = which ? prm.scale : 1.0f;
         uint8_t* dst = reinterpret_cast<uint8_t*>(which ? prm.dk : prm.dv) + ((size_t)bkv * Nk + key) * D * 2;
@@ -459,44 +453,30 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp < C::LOAD_WARP) {
     // ------------------------------------------------------------- dQ --
-    // Thread c holds column c of the dQ^T tile (TMEM lane c); it writes the
-    // tile row-major into shared memory, then one thread adds the tile's
-    // valid rows to the fp32 accumulator with a bulk reduce-add.
+    // Thread c holds column c of the dQ^T tile (TMEM lane c) and adds it to
+    // the fp32 accumulator: per query row, a warp adds 32 consecutive floats.
     const int c = threadIdx.x - 32 * C::DQ_WARP0;
     const uint32_t lane_addr = (uint32_t)((warp - C::DQ_WARP0) * 32) << 16;
-    float* stg = reinterpret_cast<float*>(smem + C::OFF_DQ);
     for (int t = 0; t < T; ++t) {
-      const int bq = t & 1;
       int bhq, q0;
       step_of(t, bhq, q0);
-      const bool w_ok =
-          __all_sync(0xffffffffu, mbar_wait(&bars->dq_full[bq], (uint32_t)((t >> 1) & 1), abort_flag, prm.err));
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err))) break;
+      tc_fence_after();
       uint32_t a[32], b[32];
-      if (w_ok) {
-        tc_fence_after();
-        tmem_ld32(tmem + lane_addr + C::COL_DQ + bq * kBQ, a);
-        tmem_ld32(tmem + lane_addr + C::COL_DQ + bq * kBQ + 32, b);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->dq_free[bq]);
-      }
-      // the staging tile is free once the previous reduce has read it
-      if (c == 0 && t > 0) bulk_wait_read_all();
-      if (!bar_and(1, 128, w_ok)) break;
+      tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
+      tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0) * D + c;
+      const int rows = Nq - q0 < kBQ ? Nq - q0 : kBQ;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        stg[q * D + c] = __uint_as_float(a[q]);
-        stg[(q + 32) * D + c] = __uint_as_float(b[q]);
-      }
-      fence_proxy_async_smem();
-      bar_sync_n(1, 128);
-      if (c == 0) {
-        const int rows = Nq - q0 < kBQ ? Nq - q0 : kBQ;
-        bulk_reduce_add_f32(prm.dq_acc + ((size_t)bhq * Nq + q0) * D, stg, (uint32_t)(rows * D * 4));
-        bulk_commit_group();
-      }
+      for (int q = 0; q < 32; ++q)
+        if (q < rows) red_add_f32(dst + (size_t)q * D, __uint_as_float(a[q]));
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        if (q + 32 < rows) red_add_f32(dst + (size_t)(q + 32) * D, __uint_as_float(b[q]));
     }
-    if (c == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -509,13 +489,27 @@ __global__ void __launch_bounds__(320, 1)
 
 // ------------------------------------------------------- small kernels --
 
+// One warp per query row, padded to whole 64-row tiles: the row's record
+// entries (-LSE * log2 e, -D) and a cleared dq_acc row.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ o, const void* __restrict__ dout,
-                                                       float* __restrict__ drow, float* __restrict__ dq_acc,
-                                                       long long rows) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+                                                       const float* __restrict__ lse, float* __restrict__ vecs,
+                                                       float* __restrict__ dq_acc, long long prow_total, int nq,
+                                                       int nqt) {
+  const long long prow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+  if (prow >= prow_total) return;
+  const long long bhq = prow / ((long long)nqt * kBQ);
+  const int qp = (int)(prow % ((long long)nqt * kBQ));  // row within the head, padded
+  float* rec = vecs + (bhq * nqt + qp / kBQ) * (2 * kBQ) + (qp % kBQ);
+  if (qp >= nq) {
+    if (lane == 0) {
+      rec[0] = -INFINITY;
+      rec[kBQ] = 0.0f;
+    }
+    return;
+  }
+  const long long row = bhq * nq + qp;
   constexpr int EPL = D / 32;  // elements per lane
   const uint16_t* op = reinterpret_cast<const uint16_t*>(o) + row * D + lane * EPL;
   const uint16_t* dp = reinterpret_cast<const uint16_t*>(dout) + row * D + lane * EPL;
@@ -545,13 +539,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ 
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) drow[row] = acc;
-  float4* z = reinterpret_cast<float4*>(dq_acc + row * D + lane * EPL);
-#pragma unroll
-  for (int i = 0; i < (EPL + 3) / 4; ++i) {
-    if (EPL >= 4) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (lane == 0) {
+    const float l = lse[row];
+    rec[0] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // a row with no key: P = 0
+    rec[kBQ] = -acc;
   }
-  if constexpr (EPL == 2) *reinterpret_cast<float2*>(dq_acc + row * D + lane * 2) = make_float2(0.0f, 0.0f);
+  float* z = dq_acc + row * D + lane * EPL;
+  if constexpr (EPL == 2) {
+    *reinterpret_cast<float2*>(z) = make_float2(0.0f, 0.0f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL / 4; ++i) reinterpret_cast<float4*>(z)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
 }
 
 template <bool F16>
@@ -618,18 +617,20 @@ template cudaError_t launch_attn_bwd<0, 128, true>(const BwdLaunch&);
 template cudaError_t launch_attn_bwd<1, 128, false>(const BwdLaunch&);
 template cudaError_t launch_attn_bwd<1, 128, true>(const BwdLaunch&);
 
-cudaError_t launch_bwd_prep(const void* o, const void* dout, float* drow, float* dq_acc, long long rows, int d,
-                            bool f16, cudaStream_t stream) {
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* vecs, float* dq_acc,
+                            long long bhq, int nq, int d, bool f16, cudaStream_t stream) {
+  const int nqt = (nq + kBQ - 1) / kBQ;
+  const long long prows = bhq * nqt * kBQ;
+  const unsigned blocks = (unsigned)((prows + 7) / 8);
   if (d == 64) {
-    if (f16) bwd_prep_kernel<64, true><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
-    else bwd_prep_kernel<64, false><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
+    if (f16) bwd_prep_kernel<64, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
+    else bwd_prep_kernel<64, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
   } else if (d == 128) {
-    if (f16) bwd_prep_kernel<128, true><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
-    else bwd_prep_kernel<128, false><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
+    if (f16) bwd_prep_kernel<128, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
+    else bwd_prep_kernel<128, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
   } else if (d == 256) {
-    if (f16) bwd_prep_kernel<256, true><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
-    else bwd_prep_kernel<256, false><<<blocks, 256, 0, stream>>>(o, dout, drow, dq_acc, rows);
+    if (f16) bwd_prep_kernel<256, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
+    else bwd_prep_kernel<256, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
   } else {
     return cudaErrorInvalidValue;
   }

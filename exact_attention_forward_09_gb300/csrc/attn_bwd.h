@@ -11,8 +11,9 @@ struct BwdParams {
   float* dq_acc;       // [BHq, Nq, D] fp32, zeroed by the preprocessing kernel
   void* dk;            // [BHkv, Nk, D] bf16 / f16
   void* dv;            // [BHkv, Nk, D]
-  const float* lse;    // [BHq, Nq] natural-log row log-sum-exp of the forward
-  const float* drow;   // [BHq, Nq] D_i = dO_i . O_i
+  // [BHq, ceil(Nq / 64), 2, 64]: per 64-row query tile, -LSE_i * log2(e)
+  // (-inf for a row with no key or past Nq) then -D_i (0 past Nq)
+  const float* vecs;
   int* err;            // device error word
   int Nq, Nk;          // query rows / keys per head
   int Hq, Hkv;         // heads (Hq % Hkv == 0)
@@ -32,9 +33,10 @@ struct BwdLaunch {
 template <int ELEM, int D, bool CAUSAL>
 cudaError_t launch_attn_bwd(const BwdLaunch& L);
 
-// D_i = sum_c dO_ic O_ic for every row, and dq_acc := 0.
-cudaError_t launch_bwd_prep(const void* o, const void* dout, float* drow, float* dq_acc, long long rows, int d,
-                            bool f16, cudaStream_t stream);
+// Per-tile records of -LSE_i * log2(e) and -D_i (D_i = dO_i . O_i) for every
+// query row, padded to whole 64-row tiles, and dq_acc := 0.
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* vecs, float* dq_acc,
+                            long long bhq, int nq, int d, bool f16, cudaStream_t stream);
 
 // dq = RN(scale * dq_acc) in the element type.
 cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, float scale, long long elems, bool f16,

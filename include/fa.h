@@ -191,7 +191,7 @@ fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t
  *   causal          0 / 1, masks aligned at the bottom right as in fa_fwd_gqa
  *   workspace       DEVICE pointer, 256-byte aligned, owned by the caller, at
  *                   least fa_bwd_workspace_bytes(B, Hq, Nq, d) bytes (an fp32
- *                   dQ accumulator and one float per query row); overwritten;
+ *                   dQ accumulator and two floats per query row); overwritten;
  *                   calls sharing it must not overlap on the GPU
  * q, k, v, o, lse, dout are read only; dq, dk, dv are fully overwritten.
  * All pointers 16-byte aligned.  Asynchronous on `stream` (four kernels:
@@ -212,8 +212,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs:
- * B*Hq*Nq*d*4 (fp32 dQ accumulator) + B*Hq*Nq*4 (row terms D), each rounded
- * up to 256.  Writes *bytes.  FA_ERR_INVALID_ARG for negative sizes or a null
+ * B*Hq*Nq*d*4 (fp32 dQ accumulator, rounded up to 256) + B*Hq*ceil(Nq/64)*512
+ * (per 64-row query tile, the rows' log-sum-exp and D terms).  Writes *bytes.  FA_ERR_INVALID_ARG for negative sizes or a null
  * `bytes`, FA_ERR_UNSUPPORTED for d not in {64, 128, 256}.
  */
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, size_t* bytes);

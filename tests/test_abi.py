@@ -132,7 +132,7 @@ def test_host_argument_checks(fa_lib):
     assert fa_lib.fa_bwd(None, None, None, None, None, None, None, None, None, 0, 2, 2, 64, 64, 128, 0, 0.1, 0,
                          None, 0, None) == fa.FA_OK
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_OK
-    assert nbytes.value == 2 * 4 * 100 * 128 * 4 + (2 * 4 * 100 * 4 + 255) // 256 * 256
+    assert nbytes.value == 2 * 4 * 100 * 128 * 4 + 2 * 4 * 2 * 512
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 96, ctypes.byref(nbytes)) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_bwd_workspace_bytes(-1, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_ERR_INVALID_ARG
 
