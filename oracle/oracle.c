@@ -201,7 +201,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
             if (!p || !dp) continue;
             const int64_t b = t / Hkv, hk = t % Hkv;
             const double* kb = k + (b * Hkv + hk) * Nk * d;
-            const double* vb = v + (b * Hkv + hk) * Nk * d;
+            const double* vbase = v + (b * Hkv + hk) * Nk * d;
             double* dkb = dk + (b * Hkv + hk) * Nk * d;
             double* dvb = dv + (b * Hkv + hk) * Nk * d;
             for (int64_t e = 0; e < Nk * d; ++e) {
@@ -217,8 +217,8 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                     for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
                     int64_t jend = Nk;
                     if (causal) {
-                        int64_t lim = i + (Nk - Nq) + 1;
-                        if (lim < jend) jend = lim;
+                        const int64_t visible = i + (Nk - Nq) + 1;
+                        if (visible < jend) jend = visible;
                         if (jend < 0) jend = 0;
                     }
                     if (jend == 0) continue;
@@ -226,9 +226,9 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                     double m = -INFINITY;
                     for (int64_t j = 0; j < jend; ++j) {
                         const double* kj = kb + j * d;
-                        double dot = 0.0;
-                        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kj[c];
-                        p[j] = scale * dot;
+                        double qk = 0.0;
+                        for (int64_t c = 0; c < d; ++c) qk += qi[c] * kj[c];
+                        p[j] = scale * qk;
                         if (p[j] > m) m = p[j];
                     }
                     double l = 0.0;
@@ -240,7 +240,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                     /* dP = dO_i . v_j and D_i = sum_j P dP */
                     double Di = 0.0;
                     for (int64_t j = 0; j < jend; ++j) {
-                        const double* vj = vb + j * d;
+                        const double* vj = vbase + j * d;
                         double dot = 0.0;
                         for (int64_t c = 0; c < d; ++c) dot += doi[c] * vj[c];
                         dp[j] = dot;

@@ -39,6 +39,8 @@ MUTANTS = {
     "bwd_dv_operand": ("dvj[c] += p[j] * doi[c];", "dvj[c] += p[j] * qi[c];"),
     "bwd_unnormalised": ("for (int64_t j = 0; j < jend; ++j) p[j] /= l;",
                          "for (int64_t j = 0; j < jend; ++j) p[j] /= 1.0;"),
+    "bwd_causal_diagonal_excluded": ("const int64_t visible = i + (Nk - Nq) + 1;",
+                                     "const int64_t visible = i + (Nk - Nq);"),
     "bwd_dp_operand": ("for (int64_t c = 0; c < d; ++c) dot += doi[c] * vj[c];",
                        "for (int64_t c = 0; c < d; ++c) dot += qi[c] * vj[c];"),
 }
