@@ -337,18 +337,22 @@ def run_extra(args, device):
     # backward (dQ, dK, dV) from the forward's O and LSE; FLOPs counted as
     # 2.5x the forward's (five matrix products against two)
     bwd = {}
-    for name, (B, H, N, causal) in (("mid", (4, 16, 2048, False)), ("mid_causal", (4, 16, 2048, True)),
-                                    ("N8192", (2, 16, 8192, False)), ("N8192_causal", (2, 16, 8192, True))):
-        q, k, v, do = (torch.randn((B, H, N, 128), device=device, generator=g).to(torch.bfloat16) for _ in range(4))
+    for name, (B, H, N, d, causal) in (("mid", (4, 16, 2048, 128, False)), ("mid_causal", (4, 16, 2048, 128, True)),
+                                       ("N8192", (2, 16, 8192, 128, False)),
+                                       ("N8192_causal", (2, 16, 8192, 128, True)),
+                                       ("N2048_d64", (4, 32, 2048, 64, False)),
+                                       ("N8192_d64", (2, 32, 8192, 64, False))):
+        q, k, v, do = (torch.randn((B, H, N, d), device=device, generator=g).to(torch.bfloat16) for _ in range(4))
         o, lse = fa.fwd(q, k, v, causal=causal)
-        ws = torch.empty((fa.bwd_workspace_bytes(B, H, N, 128),), dtype=torch.uint8, device=device)
+        ws = torch.empty((fa.bwd_workspace_bytes(B, H, N, d),), dtype=torch.uint8, device=device)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         fn = lambda: fa.bwd(q, k, v, o, lse, do, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
         fn()
         ms = _time_launches(fn, 5, device, flush)
-        tf = 2.5 * gen.flops(B, H, N, 128, causal) / (ms * 1e-3) / 1e12
+        tf = 2.5 * gen.flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
         bwd[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
-    bwd["workload"] = "bf16 d=128 H=16; mid: B=4 N=2048, N8192: B=2; dq, dk, dv from dO ~ N(0,1)"
+    bwd["workload"] = ("bf16, 16K tokens per point; d=128: H=16, d=64: H=32; mid: B=4 N=2048, N8192: B=2; "
+                       "dq, dk, dv from dO ~ N(0,1); one call per timed step after an L2 flush")
     out["backward"] = bwd
     return out
 

@@ -417,7 +417,8 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, s
   const int64_t rows = B * Hq * Nq;
   if (rows > (int64_t)1 << 40) return FA_ERR_UNSUPPORTED;
   const int64_t acc = (rows * d * 4 + 255) / 256 * 256;   // fp32 dQ accumulator
-  const int64_t recs = B * Hq * ((Nq + 63) / 64) * 512;   // per 64-row tile: 64 x (-LSE log2 e), 64 x (-D)
+  // per 64-row record: 64 x (-LSE log2 e), 64 x (-D), whole kernel steps per head
+  const int64_t recs = B * Hq * (int64_t)fa::bwd_records_per_head(Nq, d == 64 ? 64 : 128) * 512;
   *bytes = (size_t)(acc + recs);
   return FA_OK;
 }
@@ -430,7 +431,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  if (d != 128) return FA_ERR_UNSUPPORTED;  // the backward kernel covers d = 128
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // the backward kernel covers d = 64 and 128
   if (B == 0 || Hq == 0) return FA_OK;
   if (Hkv == 0 || Hq % Hkv != 0 || Nk == 0) return FA_ERR_INVALID_ARG;
   const int64_t lim = 0x7fffffffLL - 256;
@@ -463,21 +464,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   float* dq_acc = static_cast<float*>(workspace);
   float* vecs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
   const bool f16 = dtype == FA_DTYPE_FP16;
-  if (fa::launch_bwd_prep(o, dout, lse, vecs, dq_acc, (long long)(B * Hq), (int)Nq, (int)d, f16, stream) !=
-      cudaSuccess)
+  const long long nrec = fa::bwd_records_per_head(Nq, (int)d);
+  if (fa::launch_bwd_prep(o, dout, lse, vecs, dq_acc, (long long)(B * Hq), (int)Nq, (int)nrec, (int)d, f16,
+                          stream) != cudaSuccess)
     return FA_ERR_CUDA;
 
   fa::BwdLaunch L;
   std::memset(&L, 0, sizeof(L));
   const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if ((st = encode_map(&L.q, q, dt, 2, B * Hq, Nq, d, 64)) != FA_OK) return st;
-  if ((st = encode_map(&L.dout, dout, dt, 2, B * Hq, Nq, d, 64)) != FA_OK) return st;
+  const uint32_t step_rows = (uint32_t)fa::bwd_step_rows((int)d);
+  if ((st = encode_map(&L.q, q, dt, 2, B * Hq, Nq, d, step_rows)) != FA_OK) return st;
+  if ((st = encode_map(&L.dout, dout, dt, 2, B * Hq, Nq, d, step_rows)) != FA_OK) return st;
   if ((st = encode_map(&L.k, k, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   if ((st = encode_map(&L.v, v, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.dq_acc = dq_acc;
   L.prm.dk = dk;
   L.prm.dv = dv;
   L.prm.vecs = vecs;
+  L.prm.nrec = (int)nrec;
   L.prm.err = err;
   L.prm.Nq = (int)Nq;
   L.prm.Nk = (int)Nk;
@@ -488,8 +492,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   L.prm.scale = scale;
   L.stream = stream;
   cudaError_t e;
-  if (f16) e = causal ? fa::launch_attn_bwd<1, 128, true>(L) : fa::launch_attn_bwd<1, 128, false>(L);
-  else e = causal ? fa::launch_attn_bwd<0, 128, true>(L) : fa::launch_attn_bwd<0, 128, false>(L);
+  if (d == 64) {
+    if (f16) e = causal ? fa::launch_attn_bwd<1, 64, true>(L) : fa::launch_attn_bwd<1, 64, false>(L);
+    else e = causal ? fa::launch_attn_bwd<0, 64, true>(L) : fa::launch_attn_bwd<0, 64, false>(L);
+  } else {
+    if (f16) e = causal ? fa::launch_attn_bwd<1, 128, true>(L) : fa::launch_attn_bwd<1, 128, false>(L);
+    else e = causal ? fa::launch_attn_bwd<0, 128, true>(L) : fa::launch_attn_bwd<0, 128, false>(L);
+  }
   if (e != cudaSuccess) return FA_ERR_CUDA;
   if (fa::launch_bwd_dq_convert(dq_acc, dq, scale, (long long)(rows * d), f16, stream) != cudaSuccess)
     return FA_ERR_CUDA;

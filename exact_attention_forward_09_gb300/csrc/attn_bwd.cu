@@ -43,44 +43,56 @@ namespace fa {
 namespace {
 
 constexpr int kBK = 128;  // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
-constexpr int kBQ = 64;   // queries per step
+constexpr int kRec = 64;  // query rows per LSE / D record
 constexpr int kSmemCap = 232448;
 
+// d = 128: 64-query steps; dK + dV take 256 TMEM columns, so dQ is formed
+// transposed (dQ^T = K^T dS^T, M = d) and dS also goes to TMEM for dK.
+// d = 64: 128-query steps (S^T, dP^T with N = 128); dQ = dS K has M = 128
+// queries, so it comes out row-major per thread; dK reads dS from shared
+// memory (no TMEM left for it).
 template <int ELEM, int D>
 struct BwdCfg {
-  static_assert(D == 128, "the backward kernel covers head dimension 128");
+  static_assert(D == 64 || D == 128, "the backward kernel covers head dimensions 64 and 128");
+  static constexpr int BQ = (D == 64) ? 128 : 64;  // queries per step
   static constexpr int NCH = D / 64;               // 128-byte column panels per row
-  static constexpr int KV_PANEL = kBK * 128;       // one panel of a K or V tile
-  static constexpr int Q_PANEL = kBQ * 128;        // one panel of a Q or dO tile
+  static constexpr int KV_PANEL = kBK * 128;       // one panel of a K or V tile (= one dS panel)
+  static constexpr int Q_PANEL = BQ * 128;         // one panel of a Q or dO tile
   static constexpr int KV_BYTES = NCH * KV_PANEL;
   static constexpr int QT_BYTES = NCH * Q_PANEL;
   static constexpr int NST = 4;                    // Q/dO stages
   static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q, then dO
+  static constexpr int REC = BQ / kRec;            // LSE / D records per step
+  static constexpr int VEC_FLOATS = REC * 2 * kRec;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int OFF_ST = OFF_V + KV_BYTES;
-  static constexpr int OFF_DS = OFF_ST + NST * STAGE_BYTES;
-  static constexpr int OFF_VEC = OFF_DS + kBK * kBQ * 2;  // per stage: -LSE log2(e) [kBQ], -D [kBQ]
-  static constexpr int OFF_BAR = OFF_VEC + NST * 2 * kBQ * 4;
+  static constexpr int OFF_DS = OFF_ST + NST * STAGE_BYTES;   // dS [key][query], BQ / 64 panels
+  static constexpr int OFF_VEC = OFF_DS + kBK * BQ * 2;       // per stage: REC x (-LSE log2 e [64], -D [64])
+  static constexpr int OFF_BAR = OFF_VEC + NST * VEC_FLOATS * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemCap, "shared memory budget");
+  static constexpr bool DS_TMEM = (D == 128);      // dS in TMEM as dK's left operand
   static constexpr uint32_t COL_DV = 0;
   static constexpr uint32_t COL_DK = D;
   static constexpr uint32_t COL_S = 2 * D;
-  static constexpr uint32_t COL_DP = 2 * D + kBQ;
-  static constexpr uint32_t COL_DQ = 2 * D + 2 * kBQ;
-  static constexpr uint32_t COL_P = COL_DQ + kBQ;       // P, 16-bit pairs: kBQ / 2 columns
-  static constexpr uint32_t COL_DSM = COL_P + kBQ / 2;  // dS, likewise
+  static constexpr uint32_t COL_DP = 2 * D + BQ;
+  static constexpr uint32_t COL_DQ = 2 * D + 2 * BQ;    // dQ^T (d = 128) or dQ (d = 64): 64 columns
+  static constexpr uint32_t COL_P = COL_DQ + 64;        // P, 16-bit pairs: BQ / 2 columns
+  static constexpr uint32_t COL_DSM = COL_P + BQ / 2;   // dS likewise (d = 128 only)
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(COL_DSM + kBQ / 2 <= TMEM_COLS, "TMEM budget");
+  static_assert((DS_TMEM ? COL_DSM + BQ / 2 : COL_DSM) <= TMEM_COLS, "TMEM budget");
   static constexpr uint32_t FMT = (ELEM == 0) ? 1u : 0u;  // bf16 = 1, f16 = 0
-  static constexpr uint32_t IDESC_S = instr_desc(FMT, FMT, 0, 0, kBK, kBQ);  // S^T, dP^T
-  static constexpr uint32_t IDESC_KV = instr_desc(FMT, FMT, 0, 1, kBK, D);   // dV, dK
-  static constexpr uint32_t IDESC_DQ = instr_desc(FMT, FMT, 1, 1, D, kBQ);   // dQ^T
+  static constexpr uint32_t IDESC_S = instr_desc(FMT, FMT, 0, 0, kBK, BQ);  // S^T, dP^T
+  static constexpr uint32_t IDESC_KV = instr_desc(FMT, FMT, 0, 1, kBK, D);  // dV, dK
+  // dQ^T (M = d = 128, N = 64 queries) or dQ (M = 128 queries, N = d = 64)
+  static constexpr uint32_t IDESC_DQ = instr_desc(FMT, FMT, 1, 1, 128, 64);
   // warps 0-7: compute, two warpgroups (thread = key) that split each
-  // step's kBQ query columns in halves; 8-11: dQ (thread = head-dim column)
+  // step's BQ query columns in halves; 8-11: dQ (thread = head-dim column
+  // for d = 128, query row for d = 64)
   static constexpr int COMPUTE_WARPS = 8;
-  static constexpr int HALF_Q = kBQ / 2;  // query columns per compute warpgroup
+  static constexpr int HALF_Q = BQ / 2;   // query columns per compute warpgroup
+  static constexpr int NSUB = HALF_Q / 32;  // 32-column pieces per warpgroup and step
   static constexpr int DQ_WARP0 = 8;
   static constexpr int LOAD_WARP = 12;
   static constexpr int MMA_WARP = 13;
@@ -133,7 +145,8 @@ __global__ void __launch_bounds__(448, 1)
   const int Nq = prm.Nq;
   const int Nk = prm.Nk;
   const int nkt = (Nk + kBK - 1) / kBK;
-  const int nqt = (Nq + kBQ - 1) / kBQ;
+  const int nqt = (Nq + C::BQ - 1) / C::BQ;
+  const int nrec = prm.nrec;  // LSE / D records per query head
   const int grp = prm.Hq / prm.Hkv;
   const int koff = Nk - Nq;  // causal: key j visible to query i iff j <= i + koff
 
@@ -152,13 +165,13 @@ __global__ void __launch_bounds__(448, 1)
   int qt0 = 0;  // first query tile that sees a key of this tile
   if constexpr (CAUSAL) {
     const int first = k0 - koff;
-    qt0 = first > 0 ? first / kBQ : 0;
+    qt0 = first > 0 ? first / C::BQ : 0;
   }
   const int per_head = nqt > qt0 ? nqt - qt0 : 0;
   const int T = grp * per_head;  // steps of this CTA
   auto step_of = [&](int t, int& bhq, int& q0) {
     bhq = bq_head0 + t / per_head;
-    q0 = (qt0 + t % per_head) * kBQ;
+    q0 = (qt0 + t % per_head) * C::BQ;
   };
 
   if (threadIdx.x == 0) {
@@ -211,14 +224,14 @@ __global__ void __launch_bounds__(448, 1)
           break;
         int bhq, q0;
         step_of(t, bhq, q0);
-        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QT_BYTES + 2 * kBQ * 4);
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QT_BYTES + C::VEC_FLOATS * 4);
         uint8_t* st = smem + C::OFF_ST + s * C::STAGE_BYTES;
         for (int ch = 0; ch < C::NCH; ++ch) {
           tma_load_3d(st + ch * C::Q_PANEL, &tm_q, &bars->st_full[s], ch * 64, q0, bhq);
           tma_load_3d(st + C::QT_BYTES + ch * C::Q_PANEL, &tm_do, &bars->st_full[s], ch * 64, q0, bhq);
         }
-        bulk_load(vec + s * 2 * kBQ, prm.vecs + ((size_t)bhq * nqt + q0 / kBQ) * (2 * kBQ), 2 * kBQ * 4,
-                  &bars->st_full[s]);
+        bulk_load(vec + s * C::VEC_FLOATS, prm.vecs + ((size_t)bhq * nrec + q0 / kRec) * (2 * kRec),
+                  C::VEC_FLOATS * 4, &bars->st_full[s]);
       }
       // never leave with copies in flight: the K/V tile and each stage's last fill
       settle(&bars->kv_full, 0);
@@ -244,9 +257,10 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t st_kdesc = smem_desc(st_s, 16, 1024, 2);
       // MN-major views: the next 64 columns of the MN dimension one panel on
       const uint64_t st_mdesc = smem_desc(st_s, C::Q_PANEL, 1024, 2);   // Q, dO as [K = query][N = d]
-      const uint64_t k_mdesc = smem_desc(k_s, C::KV_PANEL, 1024, 2);    // K as [K = key][M = d]
-      const uint64_t ds_mdesc = smem_desc(smem_u32(smem + C::OFF_DS), C::KV_PANEL, 1024, 2);  // dS [K = key][N = query]
+      const uint64_t k_mdesc = smem_desc(k_s, C::KV_PANEL, 1024, 2);    // K as [K = key][MN = d]
+      const uint64_t ds_mdesc = smem_desc(smem_u32(smem + C::OFF_DS), C::KV_PANEL, 1024, 2);  // dS [K = key][MN = query]
 
+      const uint64_t ds_kdesc = smem_desc(smem_u32(smem + C::OFF_DS), 16, 1024, 2);  // dS [M = key][K = query]
       // S^T = K Q^T (is_dp: dP^T = V dO^T) from stage s; K = d in steps of 16
       auto issue_st = [&](int s, bool is_dp) {
         const uint64_t a0 = is_dp ? v_kdesc : k_kdesc;
@@ -260,27 +274,35 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss_elect<0>(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
         }
       };
-      // dV += P^T dO  and  dK += dS^T Q  over the kBQ queries of stage s,
-      // P^T and dS^T read from TMEM (16 queries = 8 columns per step)
+      // dV += P^T dO  and  dK += dS^T Q  over the BQ queries of stage s;
+      // P^T from TMEM (16 queries = 8 columns per step), dS^T from TMEM
+      // (d = 128) or from shared memory (d = 64)
       auto issue_kv = [&](int s, bool acc) {
 #pragma unroll
-        for (int ks = 0; ks < kBQ / 16; ++ks) {
+        for (int ks = 0; ks < C::BQ / 16; ++ks) {
           const uint64_t b = st_mdesc + (uint64_t)((s * C::STAGE_BYTES + C::QT_BYTES + ks * 2048) >> 4);
           mma_ts_elect<0>(tmem + C::COL_DV, tmem + C::COL_P + ks * 8, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int ks = 0; ks < kBQ / 16; ++ks) {
+        for (int ks = 0; ks < C::BQ / 16; ++ks) {
           const uint64_t b = st_mdesc + (uint64_t)((s * C::STAGE_BYTES + ks * 2048) >> 4);
-          mma_ts_elect<0>(tmem + C::COL_DK, tmem + C::COL_DSM + ks * 8, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
+          if constexpr (C::DS_TMEM) {
+            mma_ts_elect<0>(tmem + C::COL_DK, tmem + C::COL_DSM + ks * 8, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
+          } else {
+            const uint64_t a = ds_kdesc + (uint64_t)(((ks / 4) * C::KV_PANEL + (ks % 4) * 32) >> 4);
+            mma_ss_elect<0>(tmem + C::COL_DK, a, b, C::IDESC_KV, (acc || ks > 0) ? 1u : 0u);
+          }
         }
       };
-      // dQ^T (d x queries) = K^T dS^T over the kBK keys
+      // d = 128: dQ^T (d x queries) = K^T dS^T; d = 64: dQ (queries x d) =
+      // dS K; both over the kBK keys, operands MN-major in shared memory
       auto issue_dq = [&]() {
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks) {
-          const uint64_t a = k_mdesc + (uint64_t)((ks * 2048) >> 4);
-          const uint64_t b = ds_mdesc + (uint64_t)((ks * 2048) >> 4);
-          mma_ss_elect<0>(tmem + C::COL_DQ, a, b, C::IDESC_DQ, ks > 0 ? 1u : 0u);
+          const uint64_t kk = k_mdesc + (uint64_t)((ks * 2048) >> 4);
+          const uint64_t dd = ds_mdesc + (uint64_t)((ks * 2048) >> 4);
+          if constexpr (D == 128) mma_ss_elect<0>(tmem + C::COL_DQ, kk, dd, C::IDESC_DQ, ks > 0 ? 1u : 0u);
+          else mma_ss_elect<0>(tmem + C::COL_DQ, dd, kk, C::IDESC_DQ, ks > 0 ? 1u : 0u);
         }
       };
 
@@ -327,7 +349,8 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp < C::COMPUTE_WARPS) {
     // --------------------------------------------------------- compute --
     // Warpgroup g handles query columns [g * HALF_Q, (g + 1) * HALF_Q) of
-    // each step; thread r of a warpgroup owns key r (TMEM lane r).
+    // each step, in pieces of 32; thread r of a warpgroup owns key r (TMEM
+    // lane r).
     const int cg = warp / 4;
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
@@ -344,51 +367,59 @@ __global__ void __launch_bounds__(448, 1)
                                                  prm.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_addr + C::COL_S + cb, sr);
-      tmem_ld32(tmem + lane_addr + C::COL_DP + cb, dr);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->s_free);
-
-      // the step's -LSE * log2(e) and -D values, this warpgroup's columns
-      const float* nl2 = vec + s * 2 * kBQ + cb;
-      const float* nd = vec + s * 2 * kBQ + kBQ + cb;
-      // causal: columns c < lim are keys past the query's last visible key
+      // causal: columns c < lim (relative to cb) are keys past the query's
+      // last visible key
       int lim = 0;
       bool need_mask = false;
       if constexpr (CAUSAL) {
         lim = key - koff - q0 - cb;
         need_mask = (k0 + kBK - 1 - koff - q0 - cb) > 0;  // same for the whole warpgroup
       }
-      uint32_t pp[16], dd[16];
+      uint32_t pp[16 * C::NSUB], dd[16 * C::NSUB];
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);
-        const float4 d4 = *reinterpret_cast<const float4*>(nd + i);
-        // P = 2^(s * scale * log2 e - LSE * log2 e), in pairs
-        const float2 x01 = fma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2,
-                                make_float2(l4.x, l4.y));
-        const float2 x23 = fma2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2,
-                                make_float2(l4.z, l4.w));
-        float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
-        if (CAUSAL && need_mask) {
-          p0 = (i < lim) ? 0.0f : p0;
-          p1 = (i + 1 < lim) ? 0.0f : p1;
-          p2 = (i + 2 < lim) ? 0.0f : p2;
-          p3 = (i + 3 < lim) ? 0.0f : p3;
+      for (int sub = 0; sub < C::NSUB; ++sub) {
+        const int c0 = cb + 32 * sub;  // first query column of this piece
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_addr + C::COL_S + c0, sr);
+        tmem_ld32(tmem + lane_addr + C::COL_DP + c0, dr);
+        tmem_wait_ld();
+        if (sub == C::NSUB - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);  // this step's rows are read out
         }
-        // dS = P (dP - D)
-        const float2 g01 = add2(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
-                                make_float2(d4.x, d4.y));
-        const float2 g23 = add2(make_float2(__uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3])),
-                                make_float2(d4.z, d4.w));
-        const float2 s01 = mul2(make_float2(p0, p1), g01);
-        const float2 s23 = mul2(make_float2(p2, p3), g23);
-        pp[i / 2] = pack2<ELEM>(p0, p1);
-        pp[i / 2 + 1] = pack2<ELEM>(p2, p3);
-        dd[i / 2] = pack2<ELEM>(s01.x, s01.y);
-        dd[i / 2 + 1] = pack2<ELEM>(s23.x, s23.y);
+        // the piece's -LSE * log2(e) and -D values (record c0 / 64)
+        const float* nl2 = vec + s * C::VEC_FLOATS + (c0 / kRec) * (2 * kRec) + (c0 % kRec);
+        const float* nd = nl2 + kRec;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);
+          const float4 d4 = *reinterpret_cast<const float4*>(nd + i);
+          // P = 2^(s * scale * log2 e - LSE * log2 e), in pairs
+          const float2 x01 = fma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2,
+                                  make_float2(l4.x, l4.y));
+          const float2 x23 = fma2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2,
+                                  make_float2(l4.z, l4.w));
+          float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+          if (CAUSAL && need_mask) {
+            const int c = 32 * sub + i;
+            p0 = (c < lim) ? 0.0f : p0;
+            p1 = (c + 1 < lim) ? 0.0f : p1;
+            p2 = (c + 2 < lim) ? 0.0f : p2;
+            p3 = (c + 3 < lim) ? 0.0f : p3;
+          }
+          // dS = P (dP - D)
+          const float2 g01 = add2(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
+                                  make_float2(d4.x, d4.y));
+          const float2 g23 = add2(make_float2(__uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3])),
+                                  make_float2(d4.z, d4.w));
+          const float2 s01 = mul2(make_float2(p0, p1), g01);
+          const float2 s23 = mul2(make_float2(p2, p3), g23);
+          const int w = 16 * sub + i / 2;
+          pp[w] = pack2<ELEM>(p0, p1);
+          pp[w + 1] = pack2<ELEM>(p2, p3);
+          dd[w] = pack2<ELEM>(s01.x, s01.y);
+          dd[w + 1] = pack2<ELEM>(s23.x, s23.y);
+        }
       }
 
       // P and dS of the previous step have been consumed
@@ -397,16 +428,21 @@ __global__ void __launch_bounds__(448, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      // P and dS into TMEM (left operands of dV and dK; 16-bit pairs) ...
-      tmem_st16(tmem + lane_addr + C::COL_P + cb / 2, pp);
-      tmem_st16(tmem + lane_addr + C::COL_DSM + cb / 2, dd);
-      // ... and dS into row r of shared memory (right operand of dQ^T),
-      // 128-byte swizzle: 16-byte chunk c at c ^ (r % 8)
-      uint8_t* drow = smem + C::OFF_DS + r * 128;
+      // P (and for d = 128 dS) into TMEM, 16-bit pairs: left operands of dV (and dK) ...
+      if constexpr (C::NSUB == 1) {
+        tmem_st16(tmem + lane_addr + C::COL_P + cb / 2, pp);
+        if constexpr (C::DS_TMEM) tmem_st16(tmem + lane_addr + C::COL_DSM + cb / 2, dd);
+      } else {
+        tmem_st32(tmem + lane_addr + C::COL_P + cb / 2, pp);
+      }
+      // ... and dS into row r of shared memory ([key][query], 64-query
+      // panels, 128-byte swizzle: 16-byte chunk c of a row at c ^ (r % 8))
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int pc = ((ch + 4 * cg) ^ (r & 7)) * 16;
-        *reinterpret_cast<uint4*>(drow + pc) = make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
+      for (int ch = 0; ch < C::HALF_Q / 8; ++ch) {
+        const int c8 = cb / 8 + ch;  // 8-query chunk index within the step
+        uint8_t* row = smem + C::OFF_DS + (c8 / 8) * C::KV_PANEL + r * 128;
+        *reinterpret_cast<uint4*>(row + (((c8 % 8) ^ (r & 7)) * 16)) =
+            make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
       }
       fence_proxy_async_smem();
       tmem_wait_st();
@@ -453,8 +489,10 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp < C::LOAD_WARP) {
     // ------------------------------------------------------------- dQ --
-    // Thread c holds column c of the dQ^T tile (TMEM lane c) and adds it to
-    // the fp32 accumulator: per query row, a warp adds 32 consecutive floats.
+    // d = 128: thread c holds column c of the dQ^T tile (TMEM lane c) and
+    // adds it to the fp32 accumulator: per query row, a warp adds 32
+    // consecutive floats.  d = 64: thread r holds query row r of the dQ
+    // tile and adds its 64 floats four at a time.
     const int c = threadIdx.x - 32 * C::DQ_WARP0;
     const uint32_t lane_addr = (uint32_t)((warp - C::DQ_WARP0) * 32) << 16;
     for (int t = 0; t < T; ++t) {
@@ -468,14 +506,28 @@ __global__ void __launch_bounds__(448, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
-      float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0) * D + c;
-      const int rows = Nq - q0 < kBQ ? Nq - q0 : kBQ;
+      const int rows = Nq - q0 < C::BQ ? Nq - q0 : C::BQ;
+      if constexpr (D == 128) {
+        float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0) * D + c;
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        if (q < rows) red_add_f32(dst + (size_t)q * D, __uint_as_float(a[q]));
+        for (int q = 0; q < 32; ++q)
+          if (q < rows) red_add_f32(dst + (size_t)q * D, __uint_as_float(a[q]));
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        if (q + 32 < rows) red_add_f32(dst + (size_t)(q + 32) * D, __uint_as_float(b[q]));
+        for (int q = 0; q < 32; ++q)
+          if (q + 32 < rows) red_add_f32(dst + (size_t)(q + 32) * D, __uint_as_float(b[q]));
+      } else {
+        if (c < rows) {
+          float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0 + c) * D;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4_f32(dst + i, __uint_as_float(a[i]), __uint_as_float(a[i + 1]), __uint_as_float(a[i + 2]),
+                           __uint_as_float(a[i + 3]));
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4_f32(dst + 32 + i, __uint_as_float(b[i]), __uint_as_float(b[i + 1]), __uint_as_float(b[i + 2]),
+                           __uint_as_float(b[i + 3]));
+        }
+      }
     }
   }
 
@@ -489,23 +541,23 @@ __global__ void __launch_bounds__(448, 1)
 
 // ------------------------------------------------------- small kernels --
 
-// One warp per query row, padded to whole 64-row tiles: the row's record
-// entries (-LSE * log2 e, -D) and a cleared dq_acc row.
+// One warp per query row, padded to nrec 64-row records per head: the row's
+// record entries (-LSE * log2 e, -D) and a cleared dq_acc row.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ o, const void* __restrict__ dout,
                                                        const float* __restrict__ lse, float* __restrict__ vecs,
                                                        float* __restrict__ dq_acc, long long prow_total, int nq,
-                                                       int nqt) {
+                                                       int nrec) {
   const long long prow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (prow >= prow_total) return;
-  const long long bhq = prow / ((long long)nqt * kBQ);
-  const int qp = (int)(prow % ((long long)nqt * kBQ));  // row within the head, padded
-  float* rec = vecs + (bhq * nqt + qp / kBQ) * (2 * kBQ) + (qp % kBQ);
+  const long long bhq = prow / ((long long)nrec * kRec);
+  const int qp = (int)(prow % ((long long)nrec * kRec));  // row within the head, padded
+  float* rec = vecs + (bhq * nrec + qp / kRec) * (2 * kRec) + (qp % kRec);
   if (qp >= nq) {
     if (lane == 0) {
       rec[0] = -INFINITY;
-      rec[kBQ] = 0.0f;
+      rec[kRec] = 0.0f;
     }
     return;
   }
@@ -542,7 +594,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ 
   if (lane == 0) {
     const float l = lse[row];
     rec[0] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // a row with no key: P = 0
-    rec[kBQ] = -acc;
+    rec[kRec] = -acc;
   }
   float* z = dq_acc + row * D + lane * EPL;
   if constexpr (EPL == 2) {
@@ -616,21 +668,29 @@ template cudaError_t launch_attn_bwd<0, 128, false>(const BwdLaunch&);
 template cudaError_t launch_attn_bwd<0, 128, true>(const BwdLaunch&);
 template cudaError_t launch_attn_bwd<1, 128, false>(const BwdLaunch&);
 template cudaError_t launch_attn_bwd<1, 128, true>(const BwdLaunch&);
+template cudaError_t launch_attn_bwd<0, 64, false>(const BwdLaunch&);
+template cudaError_t launch_attn_bwd<0, 64, true>(const BwdLaunch&);
+template cudaError_t launch_attn_bwd<1, 64, false>(const BwdLaunch&);
+template cudaError_t launch_attn_bwd<1, 64, true>(const BwdLaunch&);
+
+// Query rows per step of the kernel for head dimension d (the Q / dO TMA
+// box height) and the 64-row LSE / D records it needs per query head.
+int bwd_step_rows(int d) { return d == 64 ? BwdCfg<0, 64>::BQ : BwdCfg<0, 128>::BQ; }
+long long bwd_records_per_head(long long nq, int d) {
+  const long long bq = bwd_step_rows(d);
+  return (nq + bq - 1) / bq * (bq / kRec);
+}
 
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* vecs, float* dq_acc,
-                            long long bhq, int nq, int d, bool f16, cudaStream_t stream) {
-  const int nqt = (nq + kBQ - 1) / kBQ;
-  const long long prows = bhq * nqt * kBQ;
+                            long long bhq, int nq, int nrec, int d, bool f16, cudaStream_t stream) {
+  const long long prows = bhq * nrec * kRec;
   const unsigned blocks = (unsigned)((prows + 7) / 8);
   if (d == 64) {
-    if (f16) bwd_prep_kernel<64, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
-    else bwd_prep_kernel<64, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
+    if (f16) bwd_prep_kernel<64, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nrec);
+    else bwd_prep_kernel<64, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nrec);
   } else if (d == 128) {
-    if (f16) bwd_prep_kernel<128, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
-    else bwd_prep_kernel<128, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
-  } else if (d == 256) {
-    if (f16) bwd_prep_kernel<256, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
-    else bwd_prep_kernel<256, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nqt);
+    if (f16) bwd_prep_kernel<128, true><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nrec);
+    else bwd_prep_kernel<128, false><<<blocks, 256, 0, stream>>>(o, dout, lse, vecs, dq_acc, prows, nq, nrec);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -11,9 +11,10 @@ struct BwdParams {
   float* dq_acc;       // [BHq, Nq, D] fp32, zeroed by the preprocessing kernel
   void* dk;            // [BHkv, Nk, D] bf16 / f16
   void* dv;            // [BHkv, Nk, D]
-  // [BHq, ceil(Nq / 64), 2, 64]: per 64-row query tile, -LSE_i * log2(e)
-  // (-inf for a row with no key or past Nq) then -D_i (0 past Nq)
+  // [BHq, nrec, 2, 64]: per 64-row record, -LSE_i * log2(e) (-inf for a
+  // row with no key or past Nq) then -D_i (0 past Nq)
   const float* vecs;
+  int nrec;            // records per query head (whole kernel steps)
   int* err;            // device error word
   int Nq, Nk;          // query rows / keys per head
   int Hq, Hkv;         // heads (Hq % Hkv == 0)
@@ -33,10 +34,15 @@ struct BwdLaunch {
 template <int ELEM, int D, bool CAUSAL>
 cudaError_t launch_attn_bwd(const BwdLaunch& L);
 
-// Per-tile records of -LSE_i * log2(e) and -D_i (D_i = dO_i . O_i) for every
-// query row, padded to whole 64-row tiles, and dq_acc := 0.
+// Records of -LSE_i * log2(e) and -D_i (D_i = dO_i . O_i) for every query
+// row, padded to nrec 64-row records per head, and dq_acc := 0.
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* vecs, float* dq_acc,
-                            long long bhq, int nq, int d, bool f16, cudaStream_t stream);
+                            long long bhq, int nq, int nrec, int d, bool f16, cudaStream_t stream);
+
+// Query rows per kernel step for head dimension d, and the records per
+// query head the kernel reads (whole steps).
+int bwd_step_rows(int d);
+long long bwd_records_per_head(long long nq, int d);
 
 // dq = RN(scale * dq_acc) in the element type.
 cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, float scale, long long elems, bool f16,

@@ -199,8 +199,8 @@ fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t
  * host synchronisation, no allocation.  dq is accumulated across key tiles
  * with fp32 reduce-adds, so its rounding may differ between runs.
  * Errors: FA_ERR_INVALID_ARG for bad pointers, alignment, sizes, dtype,
- * causal flag, scale or workspace; FA_ERR_UNSUPPORTED for d other than 128
- * (the backward kernel's head dimension) or a device other than sm_103;
+ * causal flag, scale or workspace; FA_ERR_UNSUPPORTED for d = 256 (the
+ * backward kernel covers d = 64 and 128) or a device other than sm_103;
  * FA_ERR_CUDA for a launch failure; a pipeline timeout is reported by
  * fa_check_device_error.  B*Hq = 0 is a no-op; Nq = 0 writes dk = dv = 0.
  */
@@ -212,8 +212,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs:
- * B*Hq*Nq*d*4 (fp32 dQ accumulator, rounded up to 256) + B*Hq*ceil(Nq/64)*512
- * (per 64-row query tile, the rows' log-sum-exp and D terms).  Writes *bytes.  FA_ERR_INVALID_ARG for negative sizes or a null
+ * B*Hq*Nq*d*4 (fp32 dQ accumulator, rounded up to 256) + B*Hq*R*512 with R
+ * the 64-row records per head: ceil(Nq/64) for d = 128, 2*ceil(Nq/128) for
+ * d = 64 (the kernel's step is 128 query rows there); each record holds
+ * its rows' log-sum-exp and D terms.  Writes *bytes.  FA_ERR_INVALID_ARG for negative sizes or a null
  * `bytes`, FA_ERR_UNSUPPORTED for d not in {64, 128, 256}.
  */
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, size_t* bytes);

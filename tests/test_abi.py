@@ -109,9 +109,9 @@ def test_host_argument_checks(fa_lib):
                                     None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_quant_fp8_rope(None, None, None, 0, 1, 1, 128, None, None, fa.FA_ROPE_HALF, None, 0, None,
                                     None) == fa.FA_OK
-    # backward: d = 128 only; workspace present, aligned and large enough; empty batch a no-op
+    # backward: d = 64 or 128; workspace present, aligned and large enough; empty batch a no-op
     ws = 1 << 24
-    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 64, 0, 0.1, 0, ws, 1 << 20,
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 256, 0, 0.1, 0, ws, 1 << 20,
                          None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 2, 2, 64, 64, 96, 0, 0.1, 0, ws, 1 << 20,
                          None) == fa.FA_ERR_UNSUPPORTED
@@ -133,6 +133,8 @@ def test_host_argument_checks(fa_lib):
                          None, 0, None) == fa.FA_OK
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_OK
     assert nbytes.value == 2 * 4 * 100 * 128 * 4 + 2 * 4 * 2 * 512
+    assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 64, ctypes.byref(nbytes)) == fa.FA_OK
+    assert nbytes.value == 2 * 4 * 100 * 64 * 4 + 2 * 4 * 2 * 512  # one 128-row step = two records
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 96, ctypes.byref(nbytes)) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_bwd_workspace_bytes(-1, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_ERR_INVALID_ARG
 

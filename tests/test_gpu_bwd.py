@@ -81,6 +81,7 @@ def _check(got, ref, dtype, what):
             f"{what} {name}: rms error {math.sqrt((e ** 2).mean()) / rrms:.3e} of rms(ref)"
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk", [
@@ -93,18 +94,17 @@ def _check(got, ref, dtype, what):
     (1, 1, 1, 1, 1),        # smallest
     (1, 2, 1, 37, 1000),    # short queries against a long sequence
 ])
-def test_bwd_parity(fa, dtype, causal, B, Hq, Hkv, Nq, Nk):
-    d = 128
+def test_bwd_parity(fa, d, dtype, causal, B, Hq, Hkv, Nq, Nk):
     scale = 1.0 / math.sqrt(d)
-    q, k, v, do = _inputs(B, Hq, Hkv, Nq, Nk, d, 900 + Nq + 7 * Nk + Hkv, dtype)
+    q, k, v, do = _inputs(B, Hq, Hkv, Nq, Nk, d, 900 + Nq + 7 * Nk + Hkv + d, dtype)
     got = _gpu_grads(fa, q, k, v, do, causal, scale)
     ref = oracle.attn_bwd(q, k, v, do, causal=causal, scale=scale)
-    _check(got, ref, dtype, f"B={B} Hq={Hq} Hkv={Hkv} Nq={Nq} Nk={Nk} causal={causal} {dtype}")
+    _check(got, ref, dtype, f"d={d} B={B} Hq={Hq} Hkv={Hkv} Nq={Nq} Nk={Nk} causal={causal} {dtype}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("scale", [0.0, -0.2, 0.3])
-def test_bwd_scales(fa, scale):
-    d = 128
+def test_bwd_scales(fa, d, scale):
     q, k, v, do = _inputs(1, 2, 2, 192, 192, d, 77, torch.bfloat16)
     for causal in (False, True):
         got = _gpu_grads(fa, q, k, v, do, causal, scale)
@@ -112,23 +112,23 @@ def test_bwd_scales(fa, scale):
         _check(got, ref, torch.bfloat16, f"scale={scale} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_end_to_end(fa, dtype, causal):
+def test_bwd_end_to_end(fa, d, dtype, causal):
     """GPU forward -> GPU backward at the usual scale 1/sqrt(d)."""
-    d = 128
     q, k, v, do = _inputs(2, 4, 2, 333, 333, d, 4242, dtype)
     got = _gpu_grads(fa, q, k, v, do, causal, 1.0 / math.sqrt(d), forward="gpu")
     ref = oracle.attn_bwd(q, k, v, do, causal=causal, scale=1.0 / math.sqrt(d))
     _check(got, ref, dtype, f"end to end causal={causal} {dtype}")
 
 
+@pytest.mark.parametrize("B,H,N,d", [(4, 16, 2048, 128), (4, 32, 2048, 64)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_mid_sampled_heads(fa, causal):
-    """The benchmark's backward workload (B=4, H=16, N=2048, d=128, bf16) in
-    one call; the oracle checks whole heads (every gradient entry of the
-    head), the first and the last."""
-    B, H, N, d = 4, 16, 2048, 128
+def test_bwd_mid_sampled_heads(fa, B, H, N, d, causal):
+    """The benchmark's backward workloads (N=2048, bf16; d=128 with H=16,
+    d=64 with H=32) in one call; the oracle checks whole heads (every
+    gradient entry of the head), the first and the last."""
     scale = 1.0 / math.sqrt(d)
     q, k, v, do = _inputs(B, H, H, N, N, d, 1234, torch.bfloat16)
     dq, dk, dv = _gpu_grads(fa, q, k, v, do, causal, scale, forward="gpu")
@@ -138,13 +138,41 @@ def test_bwd_mid_sampled_heads(fa, causal):
         _check((dq[sl], dk[sl], dv[sl]), ref, torch.bfloat16, f"mid head ({b},{h}) causal={causal}")
 
 
-def test_bwd_repeatable_dk_dv(fa):
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_repeatable_dk_dv(fa, d):
     """dK and dV are summed in a fixed order inside one CTA: bit-identical
     over repeated calls (dQ is added across CTAs in any order)."""
-    q, k, v, do = _inputs(1, 4, 2, 320, 320, 128, 55, torch.bfloat16)
+    q, k, v, do = _inputs(1, 4, 2, 320, 320, d, 55, torch.bfloat16)
     a = _gpu_grads(fa, q, k, v, do, True, 0.1)
     b = _gpu_grads(fa, q, k, v, do, True, 0.1)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_cuda_graph(fa, d):
+    """fa_bwd is capturable: a replayed graph gives the eager result (dK, dV
+    bit for bit; dQ within fp32 reduce-add reordering)."""
+    q, k, v, do = (t.cuda() for t in _inputs(2, 4, 4, 256, 256, d, 66, torch.bfloat16))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ws = torch.empty(fa.bwd_workspace_bytes(2, 4, 256, d), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    ref = (dq.clone(), dk.clone(), dv.clone())
+    for t in (dq, dk, dv):
+        t.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fa.bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
 
 
 def test_bwd_no_query(fa):
@@ -161,7 +189,7 @@ def test_bwd_no_query(fa):
 
 
 def test_bwd_rejects(fa):
-    q = torch.randn(1, 1, 64, 64, device="cuda").to(torch.bfloat16)
+    q = torch.randn(1, 1, 64, 256, device="cuda").to(torch.bfloat16)
     o, lse = fa.fwd(q, q, q)
     with pytest.raises(fa.FaError) as ei:
         fa.bwd(q, q, q, o, lse, q)
