@@ -60,7 +60,7 @@ struct BwdCfg {
   static constexpr int Q_PANEL = BQ * 128;         // one panel of a Q or dO tile
   static constexpr int KV_BYTES = NCH * KV_PANEL;
   static constexpr int QT_BYTES = NCH * Q_PANEL;
-  static constexpr int NST = 4;                    // Q/dO stages
+  static constexpr int NST = (D == 64) ? 3 : 4;    // Q/dO stages
   static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q, then dO
   static constexpr int REC = BQ / kRec;            // LSE / D records per step
   static constexpr int VEC_FLOATS = REC * 2 * kRec;
@@ -69,7 +69,11 @@ struct BwdCfg {
   static constexpr int OFF_ST = OFF_V + KV_BYTES;
   static constexpr int OFF_DS = OFF_ST + NST * STAGE_BYTES;   // dS [key][query], BQ / 64 panels
   static constexpr int OFF_VEC = OFF_DS + kBK * BQ * 2;       // per stage: REC x (-LSE log2 e [64], -D [64])
-  static constexpr int OFF_BAR = OFF_VEC + NST * VEC_FLOATS * 4;
+  // d = 64: the dQ tile (BQ rows x 64 fp32) staged for the tensor
+  // reduce-add, two 32-column boxes with the 128-byte swizzle
+  static constexpr int DQ_STAGE_BYTES = (D == 64) ? BQ * D * 4 : 0;
+  static constexpr int OFF_DQST = OFF_VEC + NST * VEC_FLOATS * 4;
+  static constexpr int OFF_BAR = OFF_DQST + DQ_STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemCap, "shared memory budget");
   static constexpr bool DS_TMEM = (D == 128);      // dS in TMEM as dK's left operand
@@ -101,7 +105,7 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t st_full[4];
+  uint64_t st_full[4];   // NST <= 4
   uint64_t st_empty[4];
   uint64_t s_full;
   uint64_t s_free;
@@ -132,7 +136,7 @@ template <int ELEM, int D, bool CAUSAL>
 __global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams prm) {
   using C = BwdCfg<ELEM, D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -375,7 +379,6 @@ __global__ void __launch_bounds__(448, 1)
         lim = key - koff - q0 - cb;
         need_mask = (k0 + kBK - 1 - koff - q0 - cb) > 0;  // same for the whole warpgroup
       }
-      uint32_t pp[16 * C::NSUB], dd[16 * C::NSUB];
 #pragma unroll
       for (int sub = 0; sub < C::NSUB; ++sub) {
         const int c0 = cb + 32 * sub;  // first query column of this piece
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(448, 1)
         // the piece's -LSE * log2(e) and -D values (record c0 / 64)
         const float* nl2 = vec + s * C::VEC_FLOATS + (c0 / kRec) * (2 * kRec) + (c0 % kRec);
         const float* nd = nl2 + kRec;
+        uint32_t pp[16], dd[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);
@@ -414,36 +418,33 @@ __global__ void __launch_bounds__(448, 1)
                                   make_float2(d4.z, d4.w));
           const float2 s01 = mul2(make_float2(p0, p1), g01);
           const float2 s23 = mul2(make_float2(p2, p3), g23);
-          const int w = 16 * sub + i / 2;
-          pp[w] = pack2<ELEM>(p0, p1);
-          pp[w + 1] = pack2<ELEM>(p2, p3);
-          dd[w] = pack2<ELEM>(s01.x, s01.y);
-          dd[w + 1] = pack2<ELEM>(s23.x, s23.y);
+          pp[i / 2] = pack2<ELEM>(p0, p1);
+          pp[i / 2 + 1] = pack2<ELEM>(p2, p3);
+          dd[i / 2] = pack2<ELEM>(s01.x, s01.y);
+          dd[i / 2 + 1] = pack2<ELEM>(s23.x, s23.y);
+        }
+        // P and dS of the previous step have been consumed (checked once,
+        // before this step's first store)
+        if (sub == 0 && t > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free, (uint32_t)((t - 1) & 1), abort_flag, prm.err));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // P (and for d = 128 dS) into TMEM, 16-bit pairs: left operands of
+        // dV (and dK) ...
+        tmem_st16(tmem + lane_addr + C::COL_P + c0 / 2, pp);
+        if constexpr (C::DS_TMEM) tmem_st16(tmem + lane_addr + C::COL_DSM + c0 / 2, dd);
+        // ... and dS into row r of shared memory ([key][query], 64-query
+        // panels, 128-byte swizzle: 16-byte chunk c of a row at c ^ (r % 8))
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int c8 = c0 / 8 + ch;  // 8-query chunk index within the step
+          uint8_t* row = smem + C::OFF_DS + (c8 / 8) * C::KV_PANEL + r * 128;
+          *reinterpret_cast<uint4*>(row + (((c8 % 8) ^ (r & 7)) * 16)) =
+              make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
         }
       }
-
-      // P and dS of the previous step have been consumed
-      if (t > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free, (uint32_t)((t - 1) & 1), abort_flag, prm.err));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // P (and for d = 128 dS) into TMEM, 16-bit pairs: left operands of dV (and dK) ...
-      if constexpr (C::NSUB == 1) {
-        tmem_st16(tmem + lane_addr + C::COL_P + cb / 2, pp);
-        if constexpr (C::DS_TMEM) tmem_st16(tmem + lane_addr + C::COL_DSM + cb / 2, dd);
-      } else {
-        tmem_st32(tmem + lane_addr + C::COL_P + cb / 2, pp);
-      }
-      // ... and dS into row r of shared memory ([key][query], 64-query
-      // panels, 128-byte swizzle: 16-byte chunk c of a row at c ^ (r % 8))
-#pragma unroll
-      for (int ch = 0; ch < C::HALF_Q / 8; ++ch) {
-        const int c8 = cb / 8 + ch;  // 8-query chunk index within the step
-        uint8_t* row = smem + C::OFF_DS + (c8 / 8) * C::KV_PANEL + r * 128;
-        *reinterpret_cast<uint4*>(row + (((c8 % 8) ^ (r & 7)) * 16)) =
-            make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
-      }
+      if (!ok) break;
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
@@ -492,22 +493,24 @@ __global__ void __launch_bounds__(448, 1)
     // d = 128: thread c holds column c of the dQ^T tile (TMEM lane c) and
     // adds it to the fp32 accumulator: per query row, a warp adds 32
     // consecutive floats.  d = 64: thread r holds query row r of the dQ
-    // tile and adds its 64 floats four at a time.
+    // tile; the tile is staged in shared memory (two 32-column boxes,
+    // 128-byte swizzle, so the row-per-thread writes are conflict-free) and
+    // added by two TMA tensor reduce-adds (rows past Nq are clipped).
     const int c = threadIdx.x - 32 * C::DQ_WARP0;
     const uint32_t lane_addr = (uint32_t)((warp - C::DQ_WARP0) * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      int bhq, q0;
-      step_of(t, bhq, q0);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err))) break;
-      tc_fence_after();
-      uint32_t a[32], b[32];
-      tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
-      tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      const int rows = Nq - q0 < C::BQ ? Nq - q0 : C::BQ;
-      if constexpr (D == 128) {
+    if constexpr (D == 128) {
+      for (int t = 0; t < T; ++t) {
+        int bhq, q0;
+        step_of(t, bhq, q0);
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err))) break;
+        tc_fence_after();
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
+        tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free);
+        const int rows = Nq - q0 < C::BQ ? Nq - q0 : C::BQ;
         float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0) * D + c;
 #pragma unroll
         for (int q = 0; q < 32; ++q)
@@ -515,19 +518,45 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q)
           if (q + 32 < rows) red_add_f32(dst + (size_t)(q + 32) * D, __uint_as_float(b[q]));
-      } else {
-        if (c < rows) {
-          float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0 + c) * D;
+      }
+    } else {
+      uint8_t* stg = smem + C::OFF_DQST;
+      if (c == 0) tma_prefetch_desc(&tm_dq);
+      for (int t = 0; t < T; ++t) {
+        int bhq, q0;
+        step_of(t, bhq, q0);
+        const bool w_ok =
+            __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err));
+        uint32_t a[32], b[32];
+        if (w_ok) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
+          tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
+        }
+        // the staging tile is free once the previous reduce has read it
+        if (c == 0 && t > 0) bulk_wait_read_all();
+        if (!bar_and(1, 128, w_ok)) break;
+        // row c: box 0 holds columns 0-31, box 1 columns 32-63; 16-byte
+        // chunk k of a row at position k ^ (row % 8)
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4_f32(dst + i, __uint_as_float(a[i]), __uint_as_float(a[i + 1]), __uint_as_float(a[i + 2]),
-                           __uint_as_float(a[i + 3]));
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4_f32(dst + 32 + i, __uint_as_float(b[i]), __uint_as_float(b[i + 1]), __uint_as_float(b[i + 2]),
-                           __uint_as_float(b[i + 3]));
+        for (int k = 0; k < 8; ++k) {
+          const int pos = ((k ^ (c & 7)) * 16);
+          *reinterpret_cast<uint4*>(stg + c * 128 + pos) = make_uint4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+          *reinterpret_cast<uint4*>(stg + C::BQ * 128 + c * 128 + pos) =
+              make_uint4(b[4 * k], b[4 * k + 1], b[4 * k + 2], b[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        bar_sync_n(1, 128);
+        if (c == 0) {
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, bhq);
+          tma_reduce_add_3d(&tm_dq, stg + C::BQ * 128, 32, q0, bhq);
+          bulk_commit_group();
         }
       }
+      if (c == 0) bulk_wait_all();
     }
   }
 
@@ -660,7 +689,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& L) {
   }
   const long long nkt = (L.prm.Nk + kBK - 1) / kBK;
   const long long ctas = (long long)L.prm.BHkv * nkt;
-  kern<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.dout, L.k, L.v, L.prm);
+  kern<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.dout, L.k, L.v, L.dq_acc, L.prm);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ struct BwdParams {
 struct BwdLaunch {
   CUtensorMap q, dout;  // [BHq, Nq, D], 64-row boxes
   CUtensorMap k, v;     // [BHkv, Nk, D], 128-row boxes
+  CUtensorMap dq_acc;   // fp32 [BHq, Nq, D], 32-column x step-row boxes, 128-byte swizzle (d = 64)
   BwdParams prm;
   cudaStream_t stream;
 };

@@ -133,6 +133,16 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// Tiled 3-D shared -> global element-wise fp32 add through a tensor map
+// (box layout as the map's swizzle mode), tracked by the issuing thread's
+// bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* ssrc, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(ssrc)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared-memory sources of this thread's committed bulk groups may be reused
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
