@@ -60,7 +60,7 @@ struct BwdCfg {
   static constexpr int Q_PANEL = BQ * 128;         // one panel of a Q or dO tile
   static constexpr int KV_BYTES = NCH * KV_PANEL;
   static constexpr int QT_BYTES = NCH * Q_PANEL;
-  static constexpr int NST = (D == 64) ? 3 : 4;    // Q/dO stages
+  static constexpr int NST = 3;                    // Q/dO stages
   static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q, then dO
   static constexpr int REC = BQ / kRec;            // LSE / D records per step
   static constexpr int VEC_FLOATS = REC * 2 * kRec;
@@ -69,10 +69,11 @@ struct BwdCfg {
   static constexpr int OFF_ST = OFF_V + KV_BYTES;
   static constexpr int OFF_DS = OFF_ST + NST * STAGE_BYTES;   // dS [key][query], BQ / 64 panels
   static constexpr int OFF_VEC = OFF_DS + kBK * BQ * 2;       // per stage: REC x (-LSE log2 e [64], -D [64])
-  // d = 64: the dQ tile (BQ rows x 64 fp32) staged for the tensor
-  // reduce-add, two 32-column boxes with the 128-byte swizzle
-  static constexpr int DQ_STAGE_BYTES = (D == 64) ? BQ * D * 4 : 0;
-  static constexpr int OFF_DQST = OFF_VEC + NST * VEC_FLOATS * 4;
+  // the dQ tile (BQ rows x D fp32) staged for the tensor reduce-add, in
+  // 32-column boxes with the 128-byte swizzle
+  static constexpr int DQ_STAGE_BYTES = BQ * D * 4;
+  static constexpr int OFF_DQST = (OFF_VEC + NST * VEC_FLOATS * 4 + 1023) / 1024 * 1024;  // swizzled boxes: 1024-aligned
+  static_assert(OFF_DS % 1024 == 0 && OFF_DQST % 1024 == 0 && (BQ * 128) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static constexpr int OFF_BAR = OFF_DQST + DQ_STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemCap, "shared memory budget");
@@ -499,26 +500,43 @@ __global__ void __launch_bounds__(448, 1)
     const int c = threadIdx.x - 32 * C::DQ_WARP0;
     const uint32_t lane_addr = (uint32_t)((warp - C::DQ_WARP0) * 32) << 16;
     if constexpr (D == 128) {
+      // column c of the dQ^T tile = column c of the dQ tile: element (q, c)
+      // goes to box c / 32, row q, float c % 32 (chunk (c % 32) / 4 at
+      // position chunk ^ (q % 8)); a warp writes one whole 128-byte row
+      uint8_t* stg = smem + C::OFF_DQST;
+      if (c == 0) tma_prefetch_desc(&tm_dq);
+      const int box = c / 32, ch = (c % 32) / 4, within = (c % 4) * 4;
       for (int t = 0; t < T; ++t) {
         int bhq, q0;
         step_of(t, bhq, q0);
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err))) break;
-        tc_fence_after();
+        const bool w_ok =
+            __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (uint32_t)(t & 1), abort_flag, prm.err));
         uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
-        tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->dq_free);
-        const int rows = Nq - q0 < C::BQ ? Nq - q0 : C::BQ;
-        float* dst = prm.dq_acc + ((size_t)bhq * Nq + q0) * D + c;
+        if (w_ok) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_addr + C::COL_DQ, a);
+          tmem_ld32(tmem + lane_addr + C::COL_DQ + 32, b);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
+        }
+        if (c == 0 && t > 0) bulk_wait_read_all();
+        if (!bar_and(1, 128, w_ok)) break;
+        uint8_t* base = stg + box * (C::BQ * 128) + within;
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (q < rows) red_add_f32(dst + (size_t)q * D, __uint_as_float(a[q]));
+        for (int q = 0; q < 32; ++q) {
+          *reinterpret_cast<uint32_t*>(base + q * 128 + ((ch ^ (q & 7)) * 16)) = a[q];
+          *reinterpret_cast<uint32_t*>(base + (q + 32) * 128 + ((ch ^ (q & 7)) * 16)) = b[q];
+        }
+        fence_proxy_async_smem();
+        bar_sync_n(1, 128);
+        if (c == 0) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (q + 32 < rows) red_add_f32(dst + (size_t)(q + 32) * D, __uint_as_float(b[q]));
+          for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_3d(&tm_dq, stg + bx * (C::BQ * 128), 32 * bx, q0, bhq);
+          bulk_commit_group();
+        }
       }
+      if (c == 0) bulk_wait_all();
     } else {
       uint8_t* stg = smem + C::OFF_DQST;
       if (c == 0) tma_prefetch_desc(&tm_dq);
