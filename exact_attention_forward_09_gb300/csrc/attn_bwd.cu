@@ -22,10 +22,12 @@
 // f16), written back to TMEM (dS also to shared memory); the MMA warp then
 // accumulates dV += P^T dO and dK += dS^T Q with the left operand read from
 // TMEM, and computes dQ^T = K^T dS^T for the tile, which a second warpgroup
-// (one thread per head-dim column) adds to an fp32 dQ accumulator in global
-// memory with coalesced reduce-adds.  Shared-memory bandwidth is the scarce
-// resource of this kernel (the tensor core reads its shared-memory operands
-// through it), so nothing that can stay in TMEM or registers goes through it.
+// (one thread per head-dim column) stages in shared memory and adds to an
+// fp32 dQ accumulator in global memory with TMA tensor reduce-adds (d = 64
+// uses 128-query steps and a row-major dQ tile; see BwdCfg).  Shared-memory
+// bandwidth is the scarce resource of this kernel (the tensor core reads its
+// shared-memory operands through it), so nothing that can stay in TMEM or
+// registers goes through it.
 // S^T / dP^T of tile t+1 are issued as soon as tile t's rows are read out,
 // so the tensor core runs them while the compute warpgroup works on tile t.
 // A preprocessing kernel forms D and clears the dQ accumulator; a last

@@ -8,7 +8,7 @@
 namespace fa {
 
 struct BwdParams {
-  float* dq_acc;       // [BHq, Nq, D] fp32, zeroed by the preprocessing kernel
+  float* dq_acc;       // [BHq, Nq, D] fp32, zeroed by the preprocessing kernel (added to through tm dq_acc)
   void* dk;            // [BHkv, Nk, D] bf16 / f16
   void* dv;            // [BHkv, Nk, D]
   // [BHq, nrec, 2, 64]: per 64-row record, -LSE_i * log2(e) (-inf for a
@@ -26,7 +26,7 @@ struct BwdParams {
 struct BwdLaunch {
   CUtensorMap q, dout;  // [BHq, Nq, D], 64-row boxes
   CUtensorMap k, v;     // [BHkv, Nk, D], 128-row boxes
-  CUtensorMap dq_acc;   // fp32 [BHq, Nq, D], 32-column x step-row boxes, 128-byte swizzle (d = 64)
+  CUtensorMap dq_acc;   // fp32 [BHq, Nq, D], 32-column x step-row boxes, 128-byte swizzle
   BwdParams prm;
   cudaStream_t stream;
 };

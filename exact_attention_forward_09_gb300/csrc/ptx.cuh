@@ -124,15 +124,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-// Contiguous shared -> global element-wise fp32 add of `bytes` (multiple of
-// 16, both addresses 16-byte aligned), tracked by the issuing thread's bulk
-// async-group.
-__device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(gdst)),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
 // Tiled 3-D shared -> global element-wise fp32 add through a tensor map
 // (box layout as the map's swizzle mode), tracked by the issuing thread's
 // bulk async-group.
@@ -148,16 +139,6 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // this thread's committed bulk groups have completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Fire-and-forget fp32 add to global memory.
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
-// Fire-and-forget add of four consecutive fp32 values (16-byte aligned).
-__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads, bulk copies).
