@@ -132,6 +132,10 @@ struct AttnParams {
   int nblk_k;           // ceil(Nk / 128): K/V descale blocks per head
   float scale_log2;     // scale * log2(e)
   int drop_pos;         // test hook: ring position CTA 0 never fills (-1: none)
+  // Units [0, pair_units) hold NQT Q tiles each; when pair_units is below
+  // the number of such groups, each remaining group is run as NQT units of
+  // one Q tile (shorter units for a last, partial wave of SMs).
+  int pair_units;
   int o_vec32;          // 1: o is 32-byte aligned (rows are stored 32 bytes at a time)
   // Row r of a head sits at sequence position r % q_period (q_period = N,
   // or Nq when the query heads of a key/value group are packed into one
@@ -163,7 +167,7 @@ struct Bars {
   uint64_t unit_full[2];   // queue of next-unit ids (load warp -> others)
   uint64_t unit_empty[2];
   alignas(16) uint32_t clc_resp[4];
-  alignas(16) int unit_q[2][8];  // decoded units: {bh (-1: none), kvh, q_base, Jt0 | Jt1 << 16, split, tb}
+  alignas(16) int unit_q[2][8];  // decoded units: {bh (-1: none), kvh, q_base, Jt0 | Jt1 << 16, split, tb, active mask}
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -210,7 +214,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   const int n_groups = (N + C::NQT * kBM - 1) / (C::NQT * kBM);
   const int koff = Nk - N;                 // causal diagonal offset (unpacked rows)
   const int S = SPLIT ? prm.splits : 1;  // key splits
-  const int U = prm.BH * n_groups * S;  // work units: (head, group of NQT Q tiles, key split)
+  const int U_groups = prm.BH * n_groups * S;  // (head, group of NQT Q tiles, key split)
+  // work units: every group, or pair_units groups and the rest as single Q tiles
+  const int U = U_groups + (C::NQT - 1) * (U_groups - prm.pair_units);
   const int G = (int)gridDim.x;
 
   // Work units are launched one CTA each, in this order: non-causal,
@@ -233,7 +239,13 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     Unit w;
     int group;
     w.split = SPLIT ? u % S : 0;
-    const int v = SPLIT ? u / S : u;
+    int v = SPLIT ? u / S : u;
+    int single = -1;  // which Q tile of its group a single-tile unit runs
+    if (!CAUSAL && !SPLIT && C::NQT == 2 && v >= prm.pair_units) {
+      const int x = v - prm.pair_units;
+      v = prm.pair_units + x / 2;
+      single = x % 2;
+    }
     if constexpr (CAUSAL) {
       group = n_groups - 1 - v / prm.BH;
       w.bh = v % prm.BH;
@@ -241,12 +253,12 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       w.bh = v / n_groups;
       group = v % n_groups;
     }
-    w.q_base = group * (C::NQT * kBM);
+    w.q_base = group * (C::NQT * kBM) + (single > 0 ? kBM : 0);
     w.tb = SPLIT ? w.split * prm.split_tiles : 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int q0 = w.q_base + t * kBM;
-      w.active[t] = (t < C::NQT) && (q0 < N);
+      w.active[t] = (t < C::NQT) && (q0 < N) && (single < 0 || t == 0);
       int tiles = 0;
       if (w.active[t]) {
         if constexpr (CAUSAL && SPLIT) {
@@ -317,6 +329,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     const int4 v = make_int4(qv[0], qv[1], qv[2], qv[3]);
     w.split = SPLIT ? qv[4] : 0;
     w.tb = SPLIT ? qv[5] : 0;
+    const int act = qv[6];
     if (arrive) mbar_arrive(&bars->unit_empty[slot]);
     w.bh = okr ? v.x : -1;
     w.kvh = v.y;
@@ -324,8 +337,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     w.Jt[0] = v.w & 0xffff;
     w.Jt[1] = (v.w >> 16) & 0xffff;
     w.J = w.Jt[0] > w.Jt[1] ? w.Jt[0] : w.Jt[1];
-    w.active[0] = true;
-    w.active[1] = (C::NQT == 2) && (w.q_base + kBM < N);
+    w.active[0] = (act & 1) != 0;
+    w.active[1] = (act & 2) != 0;
     return w;
   };
   // the load warp's side: publish unit r (u < 0: no more units)
@@ -334,12 +347,13 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     if (r >= 2 && !mbar_wait(&bars->unit_empty[slot], (uint32_t)(((r - 2) >> 1) & 1), abort_flag, prm.err))
       return false;
     int4 v = make_int4(-1, 0, 0, 0);
-    int split = 0, tb = 0;
+    int split = 0, tb = 0, act = 0;
     if (u >= 0) {
       const Unit w = decode(u);
       v = make_int4(w.bh, w.kvh, w.q_base, w.Jt[0] | (w.Jt[1] << 16));
       split = w.split;
       tb = w.tb;
+      act = (w.active[0] ? 1 : 0) | (w.active[1] ? 2 : 0);
     }
     volatile int* qv = reinterpret_cast<volatile int*>(&bars->unit_q[slot][0]);
     qv[0] = v.x;
@@ -348,6 +362,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
     qv[3] = v.w;
     qv[4] = split;
     qv[5] = tb;
+    qv[6] = act;
     mbar_arrive(&bars->unit_full[slot]);
     return true;
   };
@@ -1021,8 +1036,17 @@ cudaError_t launch_attn(const AttnLaunch& L) {
   }
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 148;
   const long long groups = (L.prm.N + C::NQT * kBM - 1) / (C::NQT * kBM);
-  const long long units = (long long)L.BH * groups * (SPLIT ? L.prm.splits : 1);
-  (void)sms;
+  const long long n_groups_all = (long long)L.BH * groups * (SPLIT ? L.prm.splits : 1);
+  // Non-causal two-tile groups: when the groups leave a last, partial wave
+  // of at most half the SMs, run that wave's groups as single-tile units
+  // (twice as many, each about 3/4 as long), so the last wave ends sooner.
+  AttnParams prm = L.prm;
+  prm.pair_units = (int)n_groups_all;
+  if constexpr (!CAUSAL && !SPLIT && C::NQT == 2) {
+    const long long rem = n_groups_all % sms;
+    if (rem > 0 && 2 * rem <= sms) prm.pair_units = (int)(n_groups_all - rem);
+  }
+  const long long units = n_groups_all + (C::NQT - 1) * (n_groups_all - prm.pair_units);
   if constexpr (C::REALLOC) {
     // the register split must fit what the kernel is launched with, or the
     // growing warpgroups would wait for registers that never come
@@ -1049,7 +1073,7 @@ cudaError_t launch_attn(const AttnLaunch& L) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, L.q, L.k, L.v, L.prm);
+  e = cudaLaunchKernelEx(&cfg, kern, L.q, L.k, L.v, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
