@@ -480,6 +480,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   // fp32 dQ accumulator: 32-column (128-byte) x step-row boxes
   if ((st = encode_map(&L.dq_acc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B * Hq, Nq, d, step_rows)) != FA_OK)
     return st;
+  if ((st = encode_map(&L.dk, dk, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.dv, dv, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
   L.prm.dq_acc = dq_acc;
   L.prm.dk = dk;
   L.prm.dv = dv;

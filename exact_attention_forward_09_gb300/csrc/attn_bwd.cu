@@ -76,6 +76,7 @@ struct BwdCfg {
   static constexpr int DQ_STAGE_BYTES = BQ * D * 4;
   static constexpr int OFF_DQST = (OFF_VEC + NST * VEC_FLOATS * 4 + 1023) / 1024 * 1024;  // swizzled boxes: 1024-aligned
   static_assert(OFF_DS % 1024 == 0 && OFF_DQST % 1024 == 0 && (BQ * 128) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(OFF_ST % 1024 == 0 && 2 * KV_BYTES <= NST * STAGE_BYTES, "dK / dV staging in the stage area");
   static constexpr int OFF_BAR = OFF_DQST + DQ_STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemCap, "shared memory budget");
@@ -122,6 +123,15 @@ struct BwdBars {
   int abort_flag;
 };
 
+// Tiled 3-D shared -> global store through a tensor map (box layout as the
+// map's swizzle mode), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* ssrc, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(ssrc)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 template <int ELEM>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (ELEM == 0) return pack_bf16x2(lo, hi);
@@ -139,7 +149,8 @@ template <int ELEM, int D, bool CAUSAL>
 __global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const BwdParams prm) {
   using C = BwdCfg<ELEM, D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -453,42 +464,50 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
-    // epilogue: dV and scale * dK rows of this tile's keys
+    // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK.  Each thread
+    // converts its key's row and writes it into the (now idle) Q/dO stage
+    // area as 64-column panels with the 128-byte swizzle; one thread then
+    // stores the panels with TMA (rows past Nk are clipped).  The four warps
+    // of a warpgroup decide together whether to go on, so none of them
+    // waits at the named barrier for a warp that gave up.
+    bool have = ok;
     if (ok && T > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, prm.err));
-      if (ok) tc_fence_after();
+      have = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, prm.err));
+      if (have) tc_fence_after();
     }
-    if (ok) {
-      // warpgroup 0 stores dV, warpgroup 1 scale * dK
-      const bool store = key < Nk;
-      {
-        const int which = cg;
-        const uint32_t col = which ? C::COL_DK : C::COL_DV;
-        const float mult = which ? prm.scale : 1.0f;
-        uint8_t* dst = reinterpret_cast<uint8_t*>(which ? prm.dk : prm.dv) + ((size_t)bkv * Nk + key) * D * 2;
+    if (bar_and(2 + cg, 128, have)) {
+      const uint32_t col = cg ? C::COL_DK : C::COL_DV;
+      const float mult = cg ? prm.scale : 1.0f;
+      uint8_t* stg = smem + C::OFF_ST + cg * C::KV_BYTES;  // kBK rows x D, NCH panels
 #pragma unroll 1
-        for (int h = 0; h < D / 64; ++h) {
-          uint32_t a[32], b[32];
-          if (T > 0) {
-            tmem_ld32(tmem + lane_addr + col + h * 64, a);
-            tmem_ld32(tmem + lane_addr + col + h * 64 + 32, b);
-            tmem_wait_ld();
-          } else {
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t a[32], b[32];
+        if (T > 0) {
+          tmem_ld32(tmem + lane_addr + col + h * 64, a);
+          tmem_ld32(tmem + lane_addr + col + h * 64 + 32, b);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
-          }
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack2<ELEM>(__uint_as_float(a[2 * i]) * mult, __uint_as_float(a[2 * i + 1]) * mult);
-            w[16 + i] = pack2<ELEM>(__uint_as_float(b[2 * i]) * mult, __uint_as_float(b[2 * i + 1]) * mult);
-          }
-          if (store) {
-            uint4* o = reinterpret_cast<uint4*>(dst + h * 128);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
+          for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
         }
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          w[i] = pack2<ELEM>(__uint_as_float(a[2 * i]) * mult, __uint_as_float(a[2 * i + 1]) * mult);
+          w[16 + i] = pack2<ELEM>(__uint_as_float(b[2 * i]) * mult, __uint_as_float(b[2 * i + 1]) * mult);
+        }
+        uint8_t* row = stg + h * C::KV_PANEL + r * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<uint4*>(row + ((i ^ (r & 7)) * 16)) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+      fence_proxy_async_smem();
+      bar_sync_n(2 + cg, 128);
+      if (r == 0) {
+        const CUtensorMap* map = cg ? &tm_dk : &tm_dv;
+        for (int h = 0; h < D / 64; ++h) tma_store_3d(map, stg + h * C::KV_PANEL, h * 64, k0, bkv);
+        bulk_commit_group();
+        bulk_wait_all();  // the panels are read and the rows written before the CTA exits
       }
     }
   } else if (warp < C::LOAD_WARP) {
@@ -709,7 +728,8 @@ cudaError_t launch_attn_bwd(const BwdLaunch& L) {
   }
   const long long nkt = (L.prm.Nk + kBK - 1) / kBK;
   const long long ctas = (long long)L.prm.BHkv * nkt;
-  kern<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.dout, L.k, L.v, L.dq_acc, L.prm);
+  kern<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.q, L.dout, L.k, L.v, L.dq_acc, L.dk, L.dv,
+                                                               L.prm);
   return cudaGetLastError();
 }
 

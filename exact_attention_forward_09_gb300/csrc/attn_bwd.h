@@ -27,6 +27,7 @@ struct BwdLaunch {
   CUtensorMap q, dout;  // [BHq, Nq, D], 64-row boxes
   CUtensorMap k, v;     // [BHkv, Nk, D], 128-row boxes
   CUtensorMap dq_acc;   // fp32 [BHq, Nq, D], 32-column x step-row boxes, 128-byte swizzle
+  CUtensorMap dk, dv;   // [BHkv, Nk, D], 128-row boxes (epilogue stores)
   BwdParams prm;
   cudaStream_t stream;
 };
