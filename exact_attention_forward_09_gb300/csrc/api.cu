@@ -454,6 +454,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!q || !o || !lse || !dout || !dq) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq))
     return FA_ERR_INVALID_ARG;
+  // the preprocessing kernel runs one block per 8 padded query rows
+  if ((B * Hq * fa::bwd_records_per_head(Nq, (int)d) * 64 + 7) / 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   size_t need = 0;
   if ((st = fa_bwd_workspace_bytes(B, Hq, Nq, d, &need)) != FA_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)

@@ -131,6 +131,9 @@ def test_host_argument_checks(fa_lib):
                          None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_bwd(None, None, None, None, None, None, None, None, None, 0, 2, 2, 64, 64, 128, 0, 0.1, 0,
                          None, 0, None) == fa.FA_OK
+    # more query rows than the preprocessing grid can cover
+    assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 1 << 10, 1 << 10, 1 << 25, 64, 128, 0, 0.1, 0, ws, 1 << 62,
+                         None) == fa.FA_ERR_UNSUPPORTED
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 128, ctypes.byref(nbytes)) == fa.FA_OK
     assert nbytes.value == 2 * 4 * 100 * 128 * 4 + 2 * 4 * 2 * 512
     assert fa_lib.fa_bwd_workspace_bytes(2, 4, 100, 64, ctypes.byref(nbytes)) == fa.FA_OK
