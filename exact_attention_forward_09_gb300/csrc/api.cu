@@ -159,6 +159,7 @@ fa_status splitkv_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N
   const int64_t T = (nkv + S - 1) / S;
   S = (nkv + T - 1) / T;  // no empty run
   if (base * S > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((p->BHp * p->Np + 7) / 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;  // combine: one block per 8 rows
   p->S = (int)S;
   p->T = (int)T;
   p->o_bytes = S > 1 ? (((size_t)S * p->BHp * p->Np * d * 4 + 255) / 256) * 256 : 0;
