@@ -498,6 +498,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   L.prm.BHkv = (int)(B * Hkv);
   L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   L.prm.scale = scale;
+  L.prm.drop_step = (g_inject.exchange(0) & 1) ? 1 : -1;
   L.stream = stream;
   cudaError_t e;
   if (d == 64) {

@@ -242,6 +242,9 @@ __global__ void __launch_bounds__(448, 1)
           break;
         int bhq, q0;
         step_of(t, bhq, q0);
+        // failure-injection hook (tests only): this stage is never filled,
+        // so the waits on it run out and the kernel aborts
+        if (t == prm.drop_step && blockIdx.x == 0) continue;
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QT_BYTES + C::VEC_FLOATS * 4);
         uint8_t* st = smem + C::OFF_ST + s * C::STAGE_BYTES;
         for (int ch = 0; ch < C::NCH; ++ch) {

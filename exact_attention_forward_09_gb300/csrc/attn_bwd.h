@@ -21,6 +21,7 @@ struct BwdParams {
   int BHkv;            // batch x key/value heads
   float scale_log2;    // scale * log2(e)
   float scale;         // dK = scale * dS^T Q
+  int drop_step;       // test hook: step whose Q/dO stage CTA 0 never fills (-1: none)
 };
 
 struct BwdLaunch {

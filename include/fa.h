@@ -322,10 +322,12 @@ fa_status fa_check_device_error(cudaStream_t stream);
 /*
  * fa_debug_inject -- TEST HOOK for the failure path; not for production use.
  * flags = 1: the next fa_fwd / fa_fwd_fp8 launch has its first CTA leave
- * one K/V ring slot unfilled, so the MMA warp's bounded wait on it runs out
- * (about 2 s): the kernel then stops every role, frees its tensor memory
- * and ends, and fa_check_device_error() returns FA_ERR_TIMEOUT.  The output
- * of that launch is incomplete.  The flag is consumed by that launch.
+ * one K/V ring slot unfilled (the next fa_bwd launch: one Q/dO stage of its
+ * first CTA's second step), so the bounded waits on it run out (about 2 s):
+ * the kernel then stops every role, frees its tensor memory and ends, and
+ * fa_check_device_error() returns FA_ERR_TIMEOUT.  The output of that
+ * launch is incomplete.  The flag is consumed by the next fa_fwd*,
+ * fa_fwd_fp8* or fa_bwd call.
  * flags = 0 clears a pending injection.  Other values: FA_ERR_INVALID_ARG.
  */
 fa_status fa_debug_inject(int flags);

@@ -42,6 +42,28 @@ def test_pipeline_timeout_is_reported_and_context_survives(fa):
     assert_bf16_parity(errors(o, lse, o_ref, l_ref), "after the injected timeout")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_pipeline_timeout_is_reported_and_context_survives(fa, d):
+    """The same for fa_bwd: one Q/dO stage of the first CTA is never filled."""
+    q, k, v, do = (torch.randn(1, 2, 512, d, device="cuda").to(torch.bfloat16) for _ in range(4))
+    lib = fa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    o, lse = fa.fwd(q, k, v, causal=False)
+    ref = fa.bwd(q, k, v, o, lse, do)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert lib.fa_debug_inject(1) == fa.FA_OK
+    t0 = time.time()
+    fa.bwd(q, k, v, o, lse, do)
+    st = lib.fa_check_device_error(stream)
+    assert st == fa.FA_ERR_TIMEOUT, lib.fa_status_string(st)
+    assert time.time() - t0 < 30.0
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
+
+
 def test_inject_rejects_bad_flags(fa):
     assert fa.lib().fa_debug_inject(7) == fa.FA_ERR_INVALID_ARG
     assert fa.lib().fa_debug_inject(0) == fa.FA_OK
