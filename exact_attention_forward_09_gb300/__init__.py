@@ -17,7 +17,7 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["bwd", "bwd_workspace_bytes", "fwd_splitkv", "splitkv_workspace_bytes", "fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
+__all__ = ["fwd_host", "fwd_host_workspace_bytes", "bwd", "bwd_workspace_bytes", "fwd_splitkv", "splitkv_workspace_bytes", "fwd", "fwd_gqa", "fwd_fp8", "fwd_fp8_gqa", "quant_fp8", "quant_fp8_per_tensor_noalloc", "check_device_error", "lib",
            "FaError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_SCRATCH_LIMIT", "FA_DTYPE_BF16", "FA_DTYPE_FP16", "FP8_BLOCK_ROWS",
            "FA_ROPE_INTERLEAVED", "FA_ROPE_HALF",
@@ -68,6 +68,11 @@ def _lib():
         lib.fa_quant_fp8_rope.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
         lib.fa_quant_fp8_per_tensor_noalloc.restype = i32
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32, vp,
+                                    ctypes.c_size_t, vp]
+        lib.fa_fwd_host.restype = i32
+        lib.fa_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_fwd_host_workspace_bytes.restype = i32
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32,
                                vp, ctypes.c_size_t, vp]
         lib.fa_bwd.restype = i32
@@ -166,6 +171,51 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool 
                                    B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), dt, int(num_splits),
                                    wp, wb, _stream(q))
     _check(st, "fa_fwd_splitkv")
+    return out, lse
+
+
+def fwd_host_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    """Bytes of device workspace ``fa_fwd_host`` needs for this shape."""
+    n = ctypes.c_size_t(0)
+    _check(_lib().fa_fwd_host_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, ctypes.byref(n)), "fa_fwd_host_workspace_bytes")
+    return int(n.value)
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, scale: float | None = None,
+             out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, device=None):
+    """``fa_fwd_host``: q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] in HOST memory
+    (page-locked for overlapped copies); the call copies them to the device,
+    runs the kernel and copies O and LSE back, asynchronously on the current
+    stream of ``device`` (default: the current CUDA device).  Returns
+    (O, LSE) as host tensors, complete once that stream has synchronised."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D host tensor")
+        if t.dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError(f"{name} has dtype {t.dtype}; expected bf16 or fp16")
+    B, Hq, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or q.dtype != k.dtype or k.dtype != v.dtype:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's batch, head dimension and dtype")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=pin)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    dt = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    with torch.cuda.device(dev):
+        need = fwd_host_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+        if workspace is None:
+            workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        st = _lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), dt,
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                torch.cuda.current_stream(dev).cuda_stream)
+    _check(st, "fa_fwd_host")
     return out, lse
 
 

@@ -37,6 +37,24 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Streams and events of the host-buffer path (fa_fwd_host), created once
+// per device on first use: two host->device copy streams, a compute stream
+// and a device->host copy stream, fanned out from and joined back into the
+// caller's stream with events on every call.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d[2] = {nullptr, nullptr};
+  cudaStream_t comp = nullptr;
+  cudaStream_t d2h = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t copied[kHostChunks] = {};
+  cudaEvent_t computed[kHostChunks] = {};
+  cudaEvent_t done[4] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
 std::atomic<int> g_inject{0};  // one-shot failure injection for the next attention launch
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -287,6 +305,122 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   L.prm.split_tiles = (int)((Nk + 127) / 128);
   L.stream = stream;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
+}
+
+fa_status fa_fwd_host_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                                     size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (Hkv == 0 || Hq % Hkv != 0) {
+    if (B == 0 || Hq == 0) {
+      *bytes = 0;
+      return FA_OK;
+    }
+    return FA_ERR_INVALID_ARG;
+  }
+  auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t qo = B * Hq * Nq * d * 2, kv = B * Hkv * Nk * d * 2;
+  *bytes = (size_t)(2 * up(qo) + 2 * up(kv) + up(B * Hq * Nq * 4));  // q, o, k, v, lse
+  return FA_OK;
+}
+
+fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                      int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                      int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  size_t need = 0;
+  fa_status st = fa_fwd_host_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, &need);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (Nk == 0) return FA_ERR_INVALID_ARG;
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host) return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return FA_ERR_INVALID_ARG;
+  const int64_t lim = 0x7fffffffLL - 256;
+  if (Nq > lim || Nk > lim || B * Hq > 0x7fffffffLL || B * Hq * ((Nq + 127) / 128) > 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& P = g_pipe[dev];
+  if (!P.ready) {
+    bool ok = true;
+    for (auto* sp : {&P.h2d[0], &P.h2d[1], &P.comp, &P.d2h})
+      ok = ok && cudaStreamCreateWithFlags(sp, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < kHostChunks; ++i) {
+      ok = ok && cudaEventCreateWithFlags(&P.copied[i], cudaEventDisableTiming) == cudaSuccess;
+      ok = ok && cudaEventCreateWithFlags(&P.computed[i], cudaEventDisableTiming) == cudaSuccess;
+    }
+    for (int i = 0; i < 4; ++i) ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return FA_ERR_CUDA;
+    P.ready = true;
+  }
+  // device copies inside the workspace: q, o, k, v, lse
+  auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t g = Hq / Hkv;
+  const int64_t q_row = g * Nq * d * 2;   // bytes of one key/value head's query rows (= its o rows)
+  const int64_t kv_row = Nk * d * 2;      // bytes of one key/value head's K (or V)
+  const int64_t BHkv = B * Hkv;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* qd = w;
+  uint8_t* od = qd + up(BHkv * q_row);
+  uint8_t* kd = od + up(BHkv * q_row);
+  uint8_t* vd = kd + up(BHkv * kv_row);
+  float* ld = reinterpret_cast<float*>(vd + up(BHkv * kv_row));
+  const uint8_t* qh = static_cast<const uint8_t*>(q_host);
+  const uint8_t* kh = static_cast<const uint8_t*>(k_host);
+  const uint8_t* vh = static_cast<const uint8_t*>(v_host);
+  uint8_t* oh = static_cast<uint8_t*>(o_host);
+
+  // fan out from the caller's stream
+  if (cudaEventRecord(P.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  for (cudaStream_t s : {P.h2d[0], P.h2d[1], P.comp, P.d2h})
+    if (cudaStreamWaitEvent(s, P.start, 0) != cudaSuccess) return FA_ERR_CUDA;
+  // chunks of whole key/value heads (each with its g query heads): the
+  // copies of chunk c+1 run while chunk c computes and chunk c-1 copies back
+  // chunk boundaries at multiples of `step` key/value heads, so that every
+  // chunk's LSE rows start 16-byte aligned (g * Nq * step rows of 4 bytes)
+  const int64_t rows = g * Nq;
+  const int64_t step = (rows % 4 == 0) ? 1 : (rows % 2 == 0) ? 2 : 4;
+  const int64_t nch = BHkv < kHostChunks ? BHkv : kHostChunks;
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t j0 = (BHkv * c / nch) / step * step;
+    const int64_t j1 = (c + 1 == nch) ? BHkv : (BHkv * (c + 1) / nch) / step * step;
+    const int64_t nj = j1 - j0;
+    if (nj <= 0) continue;
+    cudaStream_t hs = P.h2d[c & 1];
+    if (cudaMemcpyAsync(qd + j0 * q_row, qh + j0 * q_row, (size_t)(nj * q_row), cudaMemcpyHostToDevice, hs) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(kd + j0 * kv_row, kh + j0 * kv_row, (size_t)(nj * kv_row), cudaMemcpyHostToDevice, hs) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(vd + j0 * kv_row, vh + j0 * kv_row, (size_t)(nj * kv_row), cudaMemcpyHostToDevice, hs) !=
+            cudaSuccess ||
+        cudaEventRecord(P.copied[c], hs) != cudaSuccess || cudaStreamWaitEvent(P.comp, P.copied[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    // the chunk as nj batches of one key/value head and its g query heads
+    st = fa_fwd_gqa(qd + j0 * q_row, kd + j0 * kv_row, vd + j0 * kv_row, od + j0 * q_row, ld + j0 * g * Nq, nj, g,
+                    1, Nq, Nk, d, causal, scale, dtype, P.comp);
+    if (st != FA_OK) return st;
+    if (cudaEventRecord(P.computed[c], P.comp) != cudaSuccess ||
+        cudaStreamWaitEvent(P.d2h, P.computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(oh + j0 * q_row, od + j0 * q_row, (size_t)(nj * q_row), cudaMemcpyDeviceToHost, P.d2h) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(lse_host + j0 * g * Nq, ld + j0 * g * Nq, (size_t)(nj * g * Nq * 4), cudaMemcpyDeviceToHost,
+                        P.d2h) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  // join back into the caller's stream
+  cudaStream_t all[4] = {P.h2d[0], P.h2d[1], P.comp, P.d2h};
+  for (int i = 0; i < 4; ++i)
+    if (cudaEventRecord(P.done[i], all[i]) != cudaSuccess || cudaStreamWaitEvent(stream, P.done[i], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t N,

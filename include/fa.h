@@ -133,6 +133,45 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
                          cudaStream_t stream);
 
 /*
+ * fa_fwd_host -- fa_fwd_gqa on HOST buffers: the call copies q, k, v to the
+ * device, runs the attention kernel and copies o and lse back, in chunks of
+ * whole key/value heads (each with its query heads), so that the copies of
+ * one chunk overlap the kernel of the previous one and the copies back of
+ * the one before (two host->device streams, a compute stream and a
+ * device->host stream, created once per device and joined to `stream` with
+ * events; nothing is allocated per call).
+ *   q_host, o_host  [B, Hq, Nq, d]   bf16 or fp16 (dtype), HOST memory
+ *   k_host, v_host  [B, Hkv, Nk, d]  same dtype, HOST memory
+ *   lse_host        [B, Hq, Nq] fp32, HOST memory
+ *                   Page-locked memory (cudaHostAlloc / cudaHostRegister)
+ *                   lets the copies run asynchronously and overlap; with
+ *                   pageable memory the results are the same but the copies
+ *                   do not overlap.
+ *   workspace       DEVICE pointer, 256-byte aligned, owned by the caller,
+ *                   at least fa_fwd_host_workspace_bytes(...) bytes (device
+ *                   copies of q, o, k, v, lse); overwritten
+ * Asynchronous on `stream` like cudaMemcpyAsync: o_host and lse_host hold
+ * the results once `stream` has synchronised; the host buffers must stay
+ * valid until then.  Results are bit-identical to fa_fwd_gqa on device
+ * copies of the same inputs.  Errors: as fa_fwd_gqa (host pointers need no
+ * alignment), plus FA_ERR_INVALID_ARG for a missing, misaligned or too
+ * small workspace.
+ */
+fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                      int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                      int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/*
+ * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs:
+ * 2*B*Hq*Nq*d*2 + 2*B*Hkv*Nk*d*2 + B*Hq*Nq*4 bytes, each part rounded up to
+ * 256.  Writes *bytes (0 for an empty batch).  Same size checks as
+ * fa_fwd_host.
+ */
+fa_status fa_fwd_host_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                                      size_t* bytes);
+
+/*
  * fa_fwd_splitkv -- the forward pass of fa_fwd_gqa for decode-like shapes
  * (few query rows against a long key/value sequence), where batch x heads x
  * query tiles leave most SMs idle ("FlashAttention-3: async pipelines on

@@ -131,6 +131,23 @@ def test_host_argument_checks(fa_lib):
                          None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_bwd(None, None, None, None, None, None, None, None, None, 0, 2, 2, 64, 64, 128, 0, 0.1, 0,
                          None, 0, None) == fa.FA_OK
+    # host-buffer forward: workspace present, aligned and large enough; empty batch a no-op
+    assert fa_lib.fa_fwd_host(p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, None, 1 << 20,
+                              None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_host(p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws + 16, 1 << 20,
+                              None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_host(p, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws, 1000, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_host(None, p, p, p, p, 1, 2, 2, 64, 64, 128, 0, 0.1, 0, ws, 1 << 20,
+                              None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_host(p, p, p, p, p, 1, 2, 2, 64, 64, 96, 0, 0.1, 0, ws, 1 << 20,
+                              None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_fwd_host(p, p, p, p, p, 1, 3, 2, 64, 64, 128, 0, 0.1, 0, ws, 1 << 20,
+                              None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_fwd_host(None, None, None, None, None, 0, 2, 2, 64, 64, 128, 0, 0.1, 0, None, 0,
+                              None) == fa.FA_OK
+    assert fa_lib.fa_fwd_host_workspace_bytes(2, 4, 2, 100, 300, 128, ctypes.byref(nbytes)) == fa.FA_OK
+    up = lambda x: (x + 255) // 256 * 256
+    assert nbytes.value == 2 * up(2 * 4 * 100 * 128 * 2) + 2 * up(2 * 2 * 300 * 128 * 2) + up(2 * 4 * 100 * 4)
     # more query rows than the preprocessing grid can cover
     assert fa_lib.fa_bwd(p, p, p, p, p, p, p, p, p, 1, 1 << 10, 1 << 10, 1 << 25, 64, 128, 0, 0.1, 0, ws, 1 << 62,
                          None) == fa.FA_ERR_UNSUPPORTED
