@@ -53,7 +53,7 @@ constexpr int kSmemCap = 232448;
 // d = 64: 128-query steps (S^T, dP^T with N = 128); dQ = dS K has M = 128
 // queries, so it comes out row-major per thread; dK reads dS from shared
 // memory (no TMEM left for it).
-template <int ELEM, int D>
+template <int ELEM, int D, bool CAUSAL = false>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "the backward kernel covers head dimensions 64 and 128");
   static constexpr int BQ = (D == 64) ? 128 : 64;  // queries per step
@@ -95,16 +95,23 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_KV = instr_desc(FMT, FMT, 0, 1, kBK, D);  // dV, dK
   // dQ^T (M = d = 128, N = 64 queries) or dQ (M = 128 queries, N = d = 64)
   static constexpr uint32_t IDESC_DQ = instr_desc(FMT, FMT, 1, 1, 128, 64);
-  // warps 0-7: compute, two warpgroups (thread = key) that split each
-  // step's BQ query columns in halves; 8-11: dQ (thread = head-dim column
-  // for d = 128, query row for d = 64)
-  static constexpr int COMPUTE_WARPS = 8;
-  static constexpr int HALF_Q = BQ / 2;   // query columns per compute warpgroup
-  static constexpr int NSUB = HALF_Q / 32;  // 32-column pieces per warpgroup and step
-  static constexpr int DQ_WARP0 = 8;
-  static constexpr int LOAD_WARP = 12;
-  static constexpr int MMA_WARP = 13;
-  static constexpr int THREADS = 448;
+  // compute warpgroups (thread = key), each taking HALF_Q of a step's BQ
+  // query columns in pieces of PIECE: two warpgroups with 32-column pieces,
+  // or four with 16-column pieces for non-causal d = 64, whose 128-query
+  // steps are bound by this work (more warps per sub-partition, few live
+  // registers; the causal instance measured slower that way); then the dQ
+  // warpgroup (thread = head-dim column for d = 128, query row for d = 64),
+  // the load warp and the MMA warp
+  static constexpr int NCWG = (D == 64 && !CAUSAL) ? 4 : 2;
+  static constexpr int COMPUTE_WARPS = 4 * NCWG;
+  static constexpr int HALF_Q = BQ / NCWG;   // query columns per compute warpgroup
+  static constexpr int PIECE = (NCWG == 4) ? 16 : 32;
+  static constexpr int NSUB = HALF_Q / PIECE;  // pieces per warpgroup and step
+  static_assert(NSUB >= 1 && HALF_Q % PIECE == 0, "whole pieces");
+  static constexpr int DQ_WARP0 = COMPUTE_WARPS;
+  static constexpr int LOAD_WARP = DQ_WARP0 + 4;
+  static constexpr int MMA_WARP = LOAD_WARP + 1;
+  static constexpr int THREADS = 32 * (MMA_WARP + 1);
 };
 
 struct BwdBars {
@@ -122,6 +129,27 @@ struct BwdBars {
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// 32 lanes x 32 bit, 16 consecutive columns (thread i: lane quarter base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+  if constexpr (W == 32) tmem_ld32(taddr, r);
+  else tmem_ld16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[W]) {
+  if constexpr (W == 16) tmem_st16(taddr, r);
+  else tmem_st8(taddr, r);
+}
 
 // Tiled 3-D shared -> global store through a tensor map (box layout as the
 // map's swizzle mode), tracked by the issuing thread's bulk async-group.
@@ -146,12 +174,12 @@ __device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity) {
 }
 
 template <int ELEM, int D, bool CAUSAL>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(BwdCfg<ELEM, D, CAUSAL>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
                     const __grid_constant__ CUtensorMap tm_dv, const BwdParams prm) {
-  using C = BwdCfg<ELEM, D>;
+  using C = BwdCfg<ELEM, D, CAUSAL>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
@@ -370,7 +398,7 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp < C::COMPUTE_WARPS) {
     // --------------------------------------------------------- compute --
     // Warpgroup g handles query columns [g * HALF_Q, (g + 1) * HALF_Q) of
-    // each step, in pieces of 32; thread r of a warpgroup owns key r (TMEM
+    // each step, in pieces of PIECE columns; thread r of a warpgroup owns key r (TMEM
     // lane r).
     const int cg = warp / 4;
     const int r = threadIdx.x & 127;
@@ -396,12 +424,13 @@ __global__ void __launch_bounds__(448, 1)
         lim = key - koff - q0 - cb;
         need_mask = (k0 + kBK - 1 - koff - q0 - cb) > 0;  // same for the whole warpgroup
       }
+      constexpr int PW = C::PIECE;
 #pragma unroll
       for (int sub = 0; sub < C::NSUB; ++sub) {
-        const int c0 = cb + 32 * sub;  // first query column of this piece
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_addr + C::COL_S + c0, sr);
-        tmem_ld32(tmem + lane_addr + C::COL_DP + c0, dr);
+        const int c0 = cb + PW * sub;  // first query column of this piece
+        uint32_t sr[PW], dr[PW];
+        tmem_ld_cols<PW>(tmem + lane_addr + C::COL_S + c0, sr);
+        tmem_ld_cols<PW>(tmem + lane_addr + C::COL_DP + c0, dr);
         tmem_wait_ld();
         if (sub == C::NSUB - 1) {
           tc_fence_before();
@@ -410,9 +439,9 @@ __global__ void __launch_bounds__(448, 1)
         // the piece's -LSE * log2(e) and -D values (record c0 / 64)
         const float* nl2 = vec + s * C::VEC_FLOATS + (c0 / kRec) * (2 * kRec) + (c0 % kRec);
         const float* nd = nl2 + kRec;
-        uint32_t pp[16], dd[16];
+        uint32_t pp[PW / 2], dd[PW / 2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
+        for (int i = 0; i < PW; i += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(nl2 + i);
           const float4 d4 = *reinterpret_cast<const float4*>(nd + i);
           // P = 2^(s * scale * log2 e - LSE * log2 e), in pairs
@@ -422,7 +451,7 @@ __global__ void __launch_bounds__(448, 1)
                                   make_float2(l4.z, l4.w));
           float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
           if (CAUSAL && need_mask) {
-            const int c = 32 * sub + i;
+            const int c = PW * sub + i;
             p0 = (c < lim) ? 0.0f : p0;
             p1 = (c + 1 < lim) ? 0.0f : p1;
             p2 = (c + 2 < lim) ? 0.0f : p2;
@@ -449,12 +478,12 @@ __global__ void __launch_bounds__(448, 1)
         }
         // P (and for d = 128 dS) into TMEM, 16-bit pairs: left operands of
         // dV (and dK) ...
-        tmem_st16(tmem + lane_addr + C::COL_P + c0 / 2, pp);
-        if constexpr (C::DS_TMEM) tmem_st16(tmem + lane_addr + C::COL_DSM + c0 / 2, dd);
+        tmem_st_cols<PW / 2>(tmem + lane_addr + C::COL_P + c0 / 2, pp);
+        if constexpr (C::DS_TMEM) tmem_st_cols<PW / 2>(tmem + lane_addr + C::COL_DSM + c0 / 2, dd);
         // ... and dS into row r of shared memory ([key][query], 64-query
         // panels, 128-byte swizzle: 16-byte chunk c of a row at c ^ (r % 8))
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < PW / 8; ++ch) {
           const int c8 = c0 / 8 + ch;  // 8-query chunk index within the step
           uint8_t* row = smem + C::OFF_DS + (c8 / 8) * C::KV_PANEL + r * 128;
           *reinterpret_cast<uint4*>(row + (((c8 % 8) ^ (r & 7)) * 16)) =
@@ -467,7 +496,8 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
-    // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK.  Each thread
+    // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK (any further
+    // compute warpgroups are done).  Each thread
     // converts its key's row and writes it into the (now idle) Q/dO stage
     // area as 64-column panels with the 128-byte swizzle; one thread then
     // stores the panels with TMA (rows past Nk are clipped).  The four warps
@@ -478,7 +508,7 @@ __global__ void __launch_bounds__(448, 1)
       have = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, prm.err));
       if (have) tc_fence_after();
     }
-    if (bar_and(2 + cg, 128, have)) {
+    if (cg < 2 && bar_and(2 + cg, 128, have)) {
       const uint32_t col = cg ? C::COL_DK : C::COL_DV;
       const float mult = cg ? prm.scale : 1.0f;
       uint8_t* stg = smem + C::OFF_ST + cg * C::KV_BYTES;  // kBK rows x D, NCH panels
@@ -718,7 +748,7 @@ unsigned stride_grid(long long n) {
 
 template <int ELEM, int D, bool CAUSAL>
 cudaError_t launch_attn_bwd(const BwdLaunch& L) {
-  using C = BwdCfg<ELEM, D>;
+  using C = BwdCfg<ELEM, D, CAUSAL>;
   auto kern = attn_bwd_kernel<ELEM, D, CAUSAL>;
   static bool attr_done[64] = {};
   int dev = 0;
