@@ -35,13 +35,18 @@
  *                    ["FlashAttention-3: async pipelines on Hopper", section
  *                    "how incoherent processing flattens outliers": random +-1
  *                    diagonal combined with a Hadamard matrix, O(d log d)].
- *                    The quantised code is an integer decided by floating
- *                    point, so this routine works in fp32 like the kernel does:
- *                    the rotation is the fast Walsh-Hadamard butterfly with
- *                    strides 1, 2, 4, ... in fp32, the 1/sqrt(d) factor is
- *                    carried in the stored descale, codes are
- *                    round-to-nearest-even of y * RN(1 / s) with saturation at
- *                    448 (one rounded reciprocal per block, then products).
+ *                    The rotated value y is fp32 (the fast Walsh-Hadamard
+ *                    butterfly with strides 1, 2, 4, ..., the textbook in-place
+ *                    order, in fp32), the 1/sqrt(d) factor is carried in the
+ *                    stored descale, s = amax / 448 rounded to fp32, and the
+ *                    code is the E4M3 value nearest to the exact quotient y / s
+ *                    (ties to even, saturated at 448): one rounding, from the
+ *                    real number to E4M3, with no fp32 quotient in between.
+ *                    The quotient is formed in fp64, which decides that
+ *                    rounding exactly: an E4M3 midpoint has at most 5
+ *                    significant bits, so y - m s (y and s of 24 bits) is
+ *                    either 0 or at least about 2^-30 |y| away from it, far
+ *                    beyond fp64's 2^-53 relative rounding of y / s.
  *
  *                    With a rotary position embedding requested, each row is
  *                    first turned pairwise by the caller's angles (the pages
@@ -270,11 +275,12 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
 /* FP8 E4M3 codec.                                                           */
 /* ------------------------------------------------------------------------ */
 
-uint8_t oracle_e4m3_encode(float x)
+/* Nearest E4M3 value to x (ties to even), saturated at +-448. */
+uint8_t oracle_e4m3_encode_f64(double x)
 {
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
     if (isnan(x)) return (uint8_t)(sign | 0x7F);
-    const double a = fabs((double)x);
+    const double a = fabs(x);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);          /* saturate     */
     if (a < 0.015625) {                                      /* < 2^-6       */
         /* subnormal spacing 2^-9; a*512 is exact; nearbyint rounds half to
@@ -291,6 +297,11 @@ uint8_t oracle_e4m3_encode(float x)
     const int field = E + 7;
     if (field > 15 || (field == 15 && (int)qn - 8 > 6)) return (uint8_t)(sign | 0x7E);
     return (uint8_t)(sign | (uint8_t)((field << 3) | ((int)qn - 8)));
+}
+
+uint8_t oracle_e4m3_encode(float x)
+{
+    return oracle_e4m3_encode_f64((double)x);
 }
 
 float oracle_e4m3_decode(uint8_t c)
@@ -399,8 +410,7 @@ int oracle_quant_e4m3(const float* x, uint8_t* codes, float* descale,
             else for (int64_t i = 0; i < cnt; ++i) { float a = fabsf(yb[i]); if (a > amax) amax = a; }
             const float s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
             uint8_t* cb = codes + (bh * N + r0) * d;
-            const float rs = 1.0f / s;
-            for (int64_t i = 0; i < cnt; ++i) cb[i] = oracle_e4m3_encode(yb[i] * rs);
+            for (int64_t i = 0; i < cnt; ++i) cb[i] = oracle_e4m3_encode_f64((double)yb[i] / (double)s);
             descale[bh * nblk + blk] = s * rinv;
         }
     }

@@ -19,7 +19,10 @@ Sources of truth used here:
   * the tiled online recurrence equals the two-pass result (wmrh.cn article,
     sec. 2.1: the tiled result is the same as the global one);
   * torch.float8_e4m3fn for the E4M3 codec, and 448 as its maximum (wmrh.cn
-    article, sec. 3.3);
+    article, sec. 3.3); exact rational arithmetic (``fractions``) and a brute
+    force search of torch's E4M3 grid for the quantiser's rounding of y / s
+    next to E4M3 midpoints, and torch's fp32 division and float8 cast where
+    the scale is a power of two (the quotient is then exact in fp32);
   * for the backward pass: torch autograd through CPU float64 SDPA, central
     finite differences of the pinned forward, and the sums fixed by the
     softmax (rows of dS sum to zero, rows of P to one);
@@ -378,6 +381,114 @@ def pin_quantiser(oracle):
                 assert oracle.e4m3_decode(codes & 0x7F).max() == 448.0
 
 
+def _e4m3_grid():
+    """The non-negative finite E4M3 values, decoded by torch (ascending)."""
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return np.unique(np.abs(vals[np.isfinite(vals)]))
+
+
+def _nearest_e4m3_code(q, grid, codes_of):
+    """E4M3 code of the exact rational q: the nearest grid value, ties to the
+    even code, saturated at the largest finite value (brute force)."""
+    from fractions import Fraction
+    a = abs(q)
+    top = Fraction(float(grid[-1]))
+    if a >= top:
+        best = grid[-1]
+    else:
+        i = int(np.searchsorted(grid, float(a), side="right")) - 1
+        while i + 1 < len(grid) and Fraction(float(grid[i + 1])) <= a:
+            i += 1
+        while i > 0 and Fraction(float(grid[i])) > a:
+            i -= 1
+        lo, hi = Fraction(float(grid[i])), Fraction(float(grid[i + 1]))
+        dlo, dhi = a - lo, hi - a
+        if dlo < dhi:
+            best = grid[i]
+        elif dhi < dlo:
+            best = grid[i + 1]
+        else:
+            best = grid[i] if codes_of[float(grid[i])] % 2 == 0 else grid[i + 1]
+    code = codes_of[float(best)]
+    return code | (0x80 if q < 0 else 0)
+
+
+def _near_midpoint_block(d=64, rows=128):
+    """One block whose elements sit within a few fp32 ulps of s * m for E4M3
+    midpoints m, with s = amax / 448 (fp32) not a power of two, plus its
+    expected codes from exact rational arithmetic.  Also returns how many
+    elements two other readings (y * RN(1/s) rounded to fp32 first, and the
+    fp32 quotient RN(y / s) first) would encode differently, so that the pin
+    is known to tell them apart."""
+    from fractions import Fraction
+    grid = _e4m3_grid()
+    codes_of = {}
+    for c in range(0x7F):
+        v = float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64))
+        codes_of.setdefault(v, c)
+    amax = np.float32(1.7731) * np.float32(448.0)
+    s = np.float32(amax) / np.float32(448.0)
+    assert math.frexp(float(s))[0] != 0.5                            # not a power of two
+    mids = (grid[1:] + grid[:-1]) / 2.0
+    mids = mids[mids < 440.0]
+    vals, exp_codes = [], []
+    n_recip = n_div32 = 0
+    r32 = np.float32(1.0) / s
+    for m in mids:
+        y0 = np.float32(float(Fraction(float(m)) * Fraction(float(s))))
+        for k in range(-3, 4):
+            y = y0
+            for _ in range(abs(k)):
+                y = np.nextafter(y, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+            for sgn in (1.0, -1.0):
+                yy = np.float32(sgn * y)
+                want = _nearest_e4m3_code(Fraction(float(yy)) / Fraction(float(s)), grid, codes_of)
+                recip = _nearest_e4m3_code(Fraction(float(np.float32(yy * r32))), grid, codes_of)
+                div32 = _nearest_e4m3_code(Fraction(float(np.float32(yy / s))), grid, codes_of)
+                n_recip += recip != want
+                n_div32 += div32 != want
+                vals.append(yy)
+                exp_codes.append(want)
+    n = len(vals)
+    assert n + 1 <= rows * d
+    x = np.zeros(rows * d, dtype=np.float32)
+    x[:n] = vals
+    x[n] = amax                                     # the block's largest magnitude
+    exp = np.zeros(rows * d, dtype=np.uint8)
+    exp[:n] = exp_codes
+    exp[n] = 0x7E
+    exp[n + 1:] = 0                                 # +0 encodes to code 0
+    return x.reshape(1, 1, rows, d), exp.reshape(1, 1, rows, d), float(s), n_recip, n_div32
+
+
+def pin_quantiser_exact_rounding(oracle):
+    # codes are the E4M3 value nearest to the exact quotient y / s (ties to
+    # even), s = fp32(amax / 448): checked with rational arithmetic on values
+    # crafted within a few ulps of s times every E4M3 midpoint, where rounding
+    # y / s to fp32 first, or multiplying by a rounded reciprocal, would
+    # change some codes
+    x, exp, s, n_recip, n_div32 = _near_midpoint_block()
+    assert n_recip > 0 and n_div32 > 0, "crafted block does not separate the readings"
+    codes, ds = oracle.quant_e4m3(x, block_rows=128)
+    assert ds.reshape(-1)[0] == np.float32(s)
+    assert np.array_equal(codes, exp), f"{int((codes != exp).sum())} codes differ from exact rounding of y / s"
+
+
+def pin_quantiser_power_of_two_scale(oracle):
+    # with amax = 448 * 2^k the scale is exactly 2^k, so y / s is exact in
+    # fp32 and torch's float8_e4m3fn cast of it is the single correct rounding
+    rng = np.random.Generator(np.random.PCG64(71))
+    for k in (-3, 0, 5):
+        x = rng.standard_normal((1, 2, 128, 64)).astype(np.float32)
+        for h in range(2):
+            x[0, h] *= np.float32(448.0 * 2.0 ** k / 4.0) / np.abs(x[0, h]).max() * np.float32(0.999)
+            x[0, h, 7, 3] = np.float32(448.0 * 2.0 ** k)
+        codes, ds = oracle.quant_e4m3(x, block_rows=128)
+        assert np.all(ds == np.float32(2.0 ** k))
+        ref = (torch.from_numpy(x) / np.float32(2.0 ** k)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(codes, ref), k
+
+
 def _rope_pairs(d, layout):
     half = d // 2
     if layout == 1:
@@ -471,7 +582,8 @@ def pin_flop_convention(oracle):
 ALL_PINS = [
     pin_library_cross_check, pin_zero_query, pin_causal_row0, pin_special_cases,
     pin_rotation_invariance, pin_online_recurrence, pin_row_subset,
-    pin_e4m3_decode, pin_e4m3_encode, pin_fwht, pin_quantiser, pin_flop_convention,
+    pin_e4m3_decode, pin_e4m3_encode, pin_fwht, pin_quantiser, pin_quantiser_exact_rounding,
+    pin_quantiser_power_of_two_scale, pin_flop_convention,
     pin_rope_complex, pin_rope_layouts, pin_rope_relative_position, pin_rope_quantiser,
     pin_bwd_autograd, pin_bwd_finite_difference, pin_bwd_invariants, pin_bwd_empty_rows,
 ]

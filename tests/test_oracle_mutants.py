@@ -26,6 +26,10 @@ MUTANTS = {
     "e4m3_ties_away": ("double qn = nearbyint(ldexp(a, 3 - E));", "double qn = round(ldexp(a, 3 - E));"),
     "e4m3_bias": ("const int field = E + 7;", "const int field = E + 8;"),
     "quant_xmax_127": ("amax / 448.0f", "amax / 127.0f"),
+    "quant_reciprocal_product": ("oracle_e4m3_encode_f64((double)yb[i] / (double)s)",
+                                 "oracle_e4m3_encode(yb[i] * (1.0f / s))"),
+    "quant_fp32_quotient_first": ("oracle_e4m3_encode_f64((double)yb[i] / (double)s)",
+                                  "oracle_e4m3_encode(yb[i] / s)"),
     "fwht_sign": ("y[c + h] = a - b;", "y[c + h] = b - a;"),
     "signs_ignored": ("(signs && signs[c] < 0) ? -x[c] : x[c]", "x[c]"),
     "rotation_norm_missing": ("(float)(1.0 / sqrt((double)d))", "1.0f"),
