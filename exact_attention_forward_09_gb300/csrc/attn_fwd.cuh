@@ -831,7 +831,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
             mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
           }
         }
-        const float mx2 = mx * cj;
+        // a row whose keys in this tile are all masked keeps -inf (for a zero
+        // scale mx * cj would be inf * 0 = NaN)
+        const float mx2 = (mx == mask_val) ? -INFINITY : mx * cj;
         float alpha = 1.0f;
         // (a row that has seen no key yet keeps m = -inf until it does)
         const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY && mx2 != -INFINITY);

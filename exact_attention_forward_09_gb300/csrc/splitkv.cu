@@ -40,7 +40,11 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
   if (m != -INFINITY) {
     for (int s = 0; s < S; ++s) {
       const float ls = lse_part[(long long)s * rows + row];
-      const float w = expf(ls - m);  // 0 for a run without visible keys
+      // a run without visible keys (LSE -inf) has weight 0 and is skipped;
+      // a run's LSE is never NaN, but a NaN would be skipped the same way
+      // rather than spread to the row
+      if (!(ls > -INFINITY)) continue;
+      const float w = expf(ls - m);
       wsum += w;
       const float* src = o_part + ((long long)s * rows + row) * D + lane * E;
 #pragma unroll

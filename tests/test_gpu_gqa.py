@@ -43,6 +43,24 @@ def _check(o, lse, o_ref, l_ref, what):
         assert math.sqrt((diff ** 2).mean()) <= O_RMSE, what
         assert np.abs(lse[~empty] - l_ref[~empty]).max() <= LSE_ABS, what
 
+def _check_scaled(o, lse, o_ref, l_ref, v_absmax, what):
+    """Rows without keys exactly O = 0, LSE = -inf; the others within the
+    element-wise bound derived from the arithmetic (a scale other than
+    1/sqrt(d) makes the softmax flatter or peakier than the N(0,1)
+    tolerance assumes: P rounded to bf16 costs at most 2^-9 max|V| on O, the
+    output rounding 2^-9 |O|; twice that plus 1e-4), LSE within 1e-3."""
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: rows without keys must have LSE = -inf"
+    assert np.all(o[empty] == 0.0), f"{what}: rows without keys must have O = 0"
+    assert np.isfinite(o).all() and np.isfinite(lse[~empty]).all(), what
+    tol = 2.0 ** -8 * (np.abs(o_ref[~empty]) + v_absmax) + 1e-4
+    excess = np.abs(o[~empty] - o_ref[~empty]) - tol
+    assert (excess <= 0).all(), f"{what}: {int((excess > 0).sum())} elements beyond the bound"
+    assert np.abs(lse[~empty] - l_ref[~empty]).max() <= LSE_ABS, what
+
+
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (8, 1)])
 @pytest.mark.parametrize("Nq,Nk", [(300, 300), (128, 700), (700, 128), (1, 513), (513, 1)])
@@ -91,3 +109,43 @@ def test_gqa_fp8(fa, causal):
     qd, kd, vd = oracle.dequant_e4m3(qc, qs), oracle.dequant_e4m3(kc, ks), oracle.dequant_e4m3(vc, vs)
     _, l_dq = oracle.attn_fwd(qd, kd, vd, causal=causal, scale=1 / math.sqrt(d))
     assert np.abs(lse.cpu().numpy() - l_dq).max() <= 1e-3
+
+
+# Zero and negative scales on rows that see no key in a tile (causal with
+# Nq > Nk leaves the first Nq - Nk rows without any key; the others see a
+# ragged prefix of the last tile).  For a zero scale a fully masked tile's
+# row maximum times the scale is inf * 0, so these cases guard that such a
+# row keeps m = -inf: rows without keys must come out O = 0, LSE = -inf, and
+# every other row must match the oracle.
+@pytest.mark.parametrize("scale", [0.0, -0.2])
+@pytest.mark.parametrize("Nq,Nk,d", [(700, 128, 128), (513, 1, 128), (300, 260, 64), (400, 150, 256)])
+def test_gqa_rows_without_keys_zero_and_negative_scale(fa, scale, Nq, Nk, d):
+    q, k, v = _inputs(1, 4, 2, Nq, Nk, d, 950 + Nq + d, torch.bfloat16)
+    o, lse = fa.fwd_gqa(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale)
+    fa.check_device_error()
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=True, scale=scale)
+    assert np.isneginf(l_ref).any()
+    _check_scaled(o, lse, o_ref, l_ref, float(v.float().abs().max()), f"Nq={Nq} Nk={Nk} d={d} scale={scale}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2])
+def test_gqa_fp8_rows_without_keys_zero_and_negative_scale(fa, scale):
+    B, Hq, Hkv, Nq, Nk, d = 1, 4, 2, 640, 300, 128
+    q, k, v = (a.numpy().astype(np.float32) for a in _inputs(B, Hq, Hkv, Nq, Nk, d, 960, torch.float32))
+    qc, qs = oracle.quant_e4m3(q)
+    kc, ks = oracle.quant_e4m3(k)
+    vc, vs = oracle.quant_e4m3(v)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o, lse = fa.fwd_fp8_gqa(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=True, scale=scale)
+    fa.check_device_error()
+    qd, kd, vd = oracle.dequant_e4m3(qc, qs), oracle.dequant_e4m3(kc, ks), oracle.dequant_e4m3(vc, vs)
+    o_ref, l_ref = oracle.attn_fwd(qd, kd, vd, causal=True, scale=scale)
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(l_ref)
+    assert empty.any()
+    assert np.array_equal(np.isneginf(lse), empty)
+    assert np.all(o[empty] == 0.0)
+    assert np.isfinite(o).all() and np.isfinite(lse[~empty]).all()
+    assert math.sqrt(((o[~empty] - o_ref[~empty]) ** 2).mean()) <= FP8_O_RMSE
+    assert np.abs(lse[~empty] - l_ref[~empty]).max() <= 1e-3

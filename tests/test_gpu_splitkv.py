@@ -46,6 +46,24 @@ def _check(o, lse, o_ref, l_ref, what):
         assert math.sqrt((diff ** 2).mean()) <= O_RMSE, what
         assert np.abs(lse[~empty] - l_ref[~empty]).max() <= LSE_ABS, what
 
+def _check_scaled(o, lse, o_ref, l_ref, v_absmax, what):
+    """Rows without keys exactly O = 0, LSE = -inf; the others within the
+    element-wise bound derived from the arithmetic (a scale other than
+    1/sqrt(d) makes the softmax flatter or peakier than the N(0,1)
+    tolerance assumes: P rounded to bf16 costs at most 2^-9 max|V| on O, the
+    output rounding 2^-9 |O|; twice that plus 1e-4), LSE within 1e-3."""
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: rows without keys must have LSE = -inf"
+    assert np.all(o[empty] == 0.0), f"{what}: rows without keys must have O = 0"
+    assert np.isfinite(o).all() and np.isfinite(lse[~empty]).all(), what
+    tol = 2.0 ** -8 * (np.abs(o_ref[~empty]) + v_absmax) + 1e-4
+    excess = np.abs(o[~empty] - o_ref[~empty]) - tol
+    assert (excess <= 0).all(), f"{what}: {int((excess > 0).sum())} elements beyond the bound"
+    assert np.abs(lse[~empty] - l_ref[~empty]).max() <= LSE_ABS, what
+
+
 
 CASES = [
     # B, Hq, Hkv, Nq, Nk, d, causal
@@ -99,3 +117,29 @@ def test_splitkv_matches_unsplit_closely(fa):
     torch.cuda.synchronize()
     assert (o1.float() - o2.float()).abs().max().item() <= 8e-3
     assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+# Runs beyond a row's last key: with causal masks and Nq close to Nk the
+# first rows see no key of the last runs, whose LSE must then be -inf (not
+# NaN) so that the merge gives those runs weight 0.  A zero scale makes a
+# fully masked tile's maximum times the scale inf * 0; a negative scale
+# flips which score is the largest.
+SCALE_CASES = [
+    # B, Hq, Hkv, Nq, Nk, d
+    (1, 4, 2, 600, 700, 128),   # rows 0..411 see no key of the last of 3 runs
+    (1, 4, 4, 300, 1100, 64),
+    (1, 8, 2, 4, 3000, 128),    # decode-like, packed rows
+    (1, 4, 2, 8, 5, 128),       # Nq > Nk: rows without any key
+]
+
+
+@pytest.mark.parametrize("case", SCALE_CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_d{}".format(*c))
+@pytest.mark.parametrize("splits", [3, 64])
+@pytest.mark.parametrize("scale", [0.0, -0.2])
+def test_splitkv_zero_and_negative_scale(fa, case, splits, scale):
+    B, Hq, Hkv, Nq, Nk, d = case
+    q, k, v = _inputs(B, Hq, Hkv, Nq, Nk, d, 970 + Nq + d, torch.bfloat16)
+    o, lse = fa.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale, num_splits=splits)
+    fa.check_device_error()
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=True, scale=scale)
+    _check_scaled(o, lse, o_ref, l_ref, float(v.float().abs().max()), f"{case} splits={splits} scale={scale}")
