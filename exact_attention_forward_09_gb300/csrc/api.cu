@@ -56,6 +56,7 @@ struct HostPipe {
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
 std::atomic<int> g_inject{0};  // one-shot failure injection for the next attention launch
+std::atomic<int> g_inject_quant{0};  // ... and for the next quantiser call
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fa_status device_setup(int* dev_out, int** err_out) {
@@ -494,7 +495,8 @@ fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_
   if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x8) || ((uintptr_t)descale & 3u)) return FA_ERR_INVALID_ARG;
   if (per_tensor && (!workspace || ((uintptr_t)workspace & 3u))) return FA_ERR_INVALID_ARG;
-  if (B * H > 65535 || N > ((int64_t)1 << 31) - 128) return FA_ERR_UNSUPPORTED;
+  // 128-row blocks are numbered with int
+  if (N > ((int64_t)1 << 31) - 128 || B * H > 0x7fffffffLL / ((N + 127) / 128)) return FA_ERR_UNSUPPORTED;
   int dev = 0;
   int* err = nullptr;
   fa_status st = device_setup(&dev, &err);
@@ -528,9 +530,26 @@ fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_
   L.rope_cos = rope_cos;
   L.rope_sin = rope_sin;
   L.stream = stream;
+  if ((st = fa::internal_encode_quant_map(&L.map, x, B * H, N, d)) != FA_OK) return st;
+  L.drop_pos = fa::internal_take_quant_inject();
   return fa::launch_quant(L) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 }  // namespace
+
+}  // extern "C"
+
+namespace fa {
+fa_status internal_device_setup(int* dev, int** err) { return device_setup(dev, err); }
+
+fa_status internal_encode_quant_map(CUtensorMap* map, const float* x, int64_t BH, int64_t N, int64_t d) {
+  // 32-float (128-byte) x 64-row boxes, 128-byte swizzle, rows past N read as 0
+  return encode_map(map, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 64);
+}
+
+int internal_take_quant_inject() { return g_inject_quant.exchange(0) ? 1 : -1; }
+}  // namespace fa
+
+extern "C" {
 
 fa_status fa_quant_fp8(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
                        const int8_t* hadamard_signs, int per_tensor, float* workspace, cudaStream_t stream) {
@@ -678,8 +697,9 @@ fa_status fa_check_device_error(cudaStream_t stream) {
 }
 
 fa_status fa_debug_inject(int flags) {
-  if (flags != 0 && flags != 1) return FA_ERR_INVALID_ARG;
-  g_inject.store(flags);
+  if (flags < 0 || flags > 3) return FA_ERR_INVALID_ARG;
+  g_inject.store(flags & 1);
+  g_inject_quant.store((flags >> 1) & 1);
   return FA_OK;
 }
 

@@ -13,289 +13,572 @@
 // each product rounded before the sum; the caller supplies the cos / sin
 // tables and picks the pairing, (2i, 2i+1) or (i, i + d/2).
 //
-// One CTA per (head, 128-row block).  The block's rows are contiguous in
-// memory, so one bulk copy (cp.async.bulk, completion on an mbarrier) brings
-// the whole block into shared memory; then one warp per row at a time.  Each lane
-// holds d/32 consecutive elements; the Walsh-Hadamard butterfly runs inside
-// the lane for strides below d/32 and across lanes (shuffle) above, stride
-// 1, 2, 4, ... in fp32, so every element sees the same sequence of fp32
-// additions as the plain in-place butterfly.  The rotated rows stay in shared
-// memory between the amax pass and the encode pass.  The 1/sqrt(d) factor is
-// folded into the stored descale, so the codes are RNE(y * r) with
-// r = RN(1 / s), s = amax(y) / 448 of the unnormalised rotated block y (one
-// correctly rounded reciprocal per block instead of a division per element).
+// Arithmetic.  y is the rotated row in fp32: sign flip, then the in-place
+// Walsh-Hadamard butterfly with strides 1, 2, 4, ... (a + b, a - b), every
+// element seeing the same sequence of fp32 additions whatever lane holds it.
+// The block scale is s = amax(y) / 448 in fp32 (1 for an all-zero block) and
+// the 1/sqrt(d) factor is folded into the stored descale.  The code is the
+// E4M3 value nearest to the exact quotient y / s (ties to even, saturated at
+// 448): one rounding, from the real number.  It is decided exactly without a
+// division: with r = RN(1/s), the products y * RN(r (1 + 2^-20)) and
+// y * RN(r (1 - 2^-20)) bracket y / s strictly, so when both convert to the
+// same code that code is the answer; otherwise y / s lies next to the one
+// E4M3 midpoint m between the two codes, and the sign of y - m s -- exact
+// from a single fused multiply-add, the FMA residual of the Handbook of
+// Floating-Point Arithmetic (Muller et al.) -- picks the side, a zero residual
+// being a tie.  That happens for about one element in 2^15.
+//
+// Kernel organisation (persistent, one CTA per SM).  A load warp streams the
+// input through a ring of shared-memory slots with TMA (each slot is half a
+// 128-row block: 32-float x 64-row boxes, 128-byte swizzle, rows past N read
+// as zero), with full / empty mbarriers; sixteen consumer warps take 8 rows
+// each, so a block is one pass.  A row is spread over 4 lanes (lane / 8 picks
+// the quarter, lane % 8 the row), chosen so that the 8 lanes of each
+// shared-memory phase read 8 different rows and the swizzle puts them in
+// different banks.  The rotated rows stay in registers: each warp frees its
+// slot as soon as it has read it, takes the block maximum across the 16 warps
+// through a predicate-AND barrier (which also lets a warp that gave up stop
+// the others), and encodes from registers.  HBM-bound: 4 bytes read and 1
+// written per element.
+#include <climits>
 #include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
 #include "quant_fp8.h"
 
 namespace fa {
+namespace {
 
 template <int D>
-__device__ __forceinline__ void rotate_row(float (&v)[D / 32], int lane, const SignBits& sg, bool rot) {
-  constexpr int E = D / 32;
-  if (!rot) return;
+struct QCfg {
+  static constexpr int NW = 16;                  // warps per CTA
+  static constexpr int THREADS = 32 * NW;
+  // Two groups of 8 warps work on alternate blocks, each with its own ring
+  // and barrier, so that one group's wait for its block maximum overlaps
+  // the other group's work (d = 256: one group; its rows do not fit twice).
+  static constexpr int NG = (D == 256) ? 1 : 2;
+  static constexpr int WG = NW / NG;             // warps per group
+  static constexpr int RS = NG;                  // 8-row sets per warp and block
+  static constexpr int E = D / 4;                // elements of a row per lane
+  static constexpr int G = E < 32 ? E : 32;      // contiguous run of a lane's elements
+  static constexpr int BOXES = D / 32;           // 32-float boxes per row
+  static constexpr int SLOT_ROWS = 64;           // half a block per slot
+  static constexpr int BOX_BYTES = SLOT_ROWS * 128;
+  static constexpr int SLOT_BYTES = BOXES * BOX_BYTES;
+  // Slots per group.  With one group each slot must serve one half of the
+  // block only, so the count is even: position q goes to slot q % NSG and to
+  // half q % 2.  (An odd count would let a slot alternate between the
+  // halves, and a half running a block ahead could wait on a slot two phases
+  // ahead of its last fill, which an mbarrier's phase parity cannot tell
+  // from the previous phase.)  With two groups every warp of a group reads
+  // both halves, in order, so any count works.
+  static constexpr int NSG_RAW = 196608 / SLOT_BYTES / NG;
+  static constexpr int NSG_CAP = NSG_RAW > 8 ? 8 : NSG_RAW;
+  static constexpr int NSG = (NG == 1) ? (NSG_CAP & ~1) : NSG_CAP;
+  static_assert(NSG >= 2 && (NG == 2 || NSG % 2 == 0), "ring too shallow or odd");
+  static constexpr int NSLOT = NG * NSG;
+  static constexpr int SMEM_BYTES = NSLOT * SLOT_BYTES + 1024 + 1024;  // ring + barriers + alignment
+};
+
+template <int NS>
+struct QShared {
+  uint64_t full[NS];
+  uint64_t empty[NS];
+  float red[2][2][8];  // [group][block parity][warp of group] (one group: [0][parity][16])
+  int last_pos[NS];
+  int abort_flag;
+  int first_bad;       // first block iteration (of the CTA) some warp could not finish
+};
+
+struct QuantParams {
+  uint8_t* x8;
+  float* descale;
+  float* ws;          // MODE 1: one float (atomic max); MODE 2: the tensor maximum; MODE 3: per-block maxima
+  int* err;
+  const float* rcos;
+  const float* rsin;
+  SignBits sg;
+  int N, nblk, total;  // rows per head, blocks per head, blocks in all
+  int rot;
+  float rinv;
+  int rope;
+  int drop_pos;
+};
+
+// Index within the row of a lane's local element e (quarter p of the row).
+template <int D>
+__device__ __forceinline__ int elem_of(int e, int p) {
+  constexpr int G = QCfg<D>::G;
+  return (e & (G - 1)) + G * p + 128 * (e >> 5);
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  // RN(a - b) per half: a fused multiply-add whose product b * -1 is exact
+  return fma2(b, make_float2(-1.0f, -1.0f), a);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float2 lo, float2 hi) {
+  uint16_t a, b;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(a) : "f"(lo.y), "f"(lo.x));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(hi.y), "f"(hi.x));
+  return (uint32_t)a | ((uint32_t)b << 16);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)code));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// The bracketing codes of four values differ: settle each differing byte by
+// the sign of y - m s (m the E4M3 midpoint between the two candidates).
+__device__ __noinline__ uint32_t settle4(float y0, float y1, float y2, float y3, uint32_t chi, uint32_t clo, float s) {
+  const float y[4] = {y0, y1, y2, y3};
+  uint32_t out = 0;
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int i = lane * E + e;
-    if ((sg.w[i >> 5] >> (i & 31)) & 1u) v[e] = -v[e];
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t ch = (chi >> (8 * b)) & 0xffu, cl = (clo >> (8 * b)) & 0xffu;
+    uint32_t c = ch;
+    if (ch != cl) {
+      const float m = 0.5f * (fabsf(e4m3_value(ch)) + fabsf(e4m3_value(cl)));
+      const float rem = fmaf(-m, s, fabsf(y[b]));
+      c = rem > 0.0f ? ch : (rem < 0.0f ? cl : ((ch & 1u) ? cl : ch));
+    }
+    out |= c << (8 * b);
   }
+  return out;
+}
+
+// Four codes of y / s; rh, rl bracket 1/s from above and below.
+__device__ __forceinline__ uint32_t encode4(const float* v, float2 rh, float2 rl, float s) {
+  const float2 a = make_float2(v[0], v[1]), b = make_float2(v[2], v[3]);
+  const uint32_t ch = cvt_e4m3x4(mul2(a, rh), mul2(b, rh));
+  const uint32_t cl = cvt_e4m3x4(mul2(a, rl), mul2(b, rl));
+  if (ch == cl) return ch;
+  return settle4(v[0], v[1], v[2], v[3], ch, cl, s);
+}
+
+template <int D>
+__device__ __forceinline__ void rope_row(float (&v)[QCfg<D>::E], int p, const float* __restrict__ c,
+                                         const float* __restrict__ s, int mode) {
+  constexpr int E = QCfg<D>::E;
+  if (mode == 1) {
+    // pairs (2i, 2i+1): adjacent elements of one lane, angle elem / 2
 #pragma unroll
-  for (int h = 1; h < E; h <<= 1) {
+    for (int e0 = 0; e0 < E; e0 += 8) {
+      const int a0 = elem_of<D>(e0, p) >> 1;
+      const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
+      const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+      const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      if (!(e & h)) {
-        const float a = v[e], b = v[e + h];
-        v[e] = __fadd_rn(a, b);
-        v[e + h] = __fsub_rn(a, b);
+      for (int k = 0; k < 4; ++k) {
+        const float x = v[e0 + 2 * k], y = v[e0 + 2 * k + 1];
+        v[e0 + 2 * k] = __fsub_rn(__fmul_rn(x, cv[k]), __fmul_rn(y, sv[k]));
+        v[e0 + 2 * k + 1] = __fadd_rn(__fmul_rn(x, sv[k]), __fmul_rn(y, cv[k]));
+      }
+    }
+  } else if (mode == 2) {
+    if constexpr (D == 256) {
+      // pairs (i, i + 128): local elements e and e + 32 of one lane
+#pragma unroll
+      for (int e0 = 0; e0 < 32; e0 += 4) {
+        const int a0 = elem_of<D>(e0, p);
+        const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
+        const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+        const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x = v[e0 + k], y = v[e0 + k + 32];
+          v[e0 + k] = __fsub_rn(__fmul_rn(x, cv[k]), __fmul_rn(y, sv[k]));
+          v[e0 + k + 32] = __fadd_rn(__fmul_rn(x, sv[k]), __fmul_rn(y, cv[k]));
+        }
+      }
+    } else {
+      // pairs (i, i + D/2): quarters p and p ^ 2 of the row, lanes 16 apart
+      const bool first = (p & 2) == 0;
+#pragma unroll
+      for (int e0 = 0; e0 < E; e0 += 4) {
+        const int a0 = elem_of<D>(e0, p & 1);
+        const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
+        const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+        const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[e0 + k], 16);
+          const float x = first ? v[e0 + k] : o, y = first ? o : v[e0 + k];
+          v[e0 + k] = first ? __fsub_rn(__fmul_rn(x, cv[k]), __fmul_rn(y, sv[k]))
+                            : __fadd_rn(__fmul_rn(x, sv[k]), __fmul_rn(y, cv[k]));
+        }
       }
     }
   }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float p = __shfl_xor_sync(0xffffffffu, v[e], m);
-      v[e] = (lane & m) ? __fsub_rn(p, v[e]) : __fadd_rn(v[e], p);
-    }
-  }
 }
 
-// n consecutive floats (16-byte aligned when n >= 4, 8-byte when n == 2)
-template <int n>
-__device__ __forceinline__ void load_row_f32(float (&out)[n], const float* __restrict__ p) {
-  if constexpr (n % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < n; i += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(p + i);
-      out[i] = t.x; out[i + 1] = t.y; out[i + 2] = t.z; out[i + 3] = t.w;
-    }
-  } else if constexpr (n == 2) {
-    const float2 t = *reinterpret_cast<const float2*>(p);
-    out[0] = t.x; out[1] = t.y;
-  } else {
-#pragma unroll
-    for (int i = 0; i < n; ++i) out[i] = p[i];
-  }
-}
-
-// Rotary embedding of one row (lane holds channels lane*E .. lane*E+E-1);
-// c, s: this row's cos / sin tables (d/2 entries each).
+// Sign flip and Walsh-Hadamard butterfly of a row spread over the 4 lanes
+// lane % 8 + 8 * {0, 1, 2, 3}; strides in ascending order.
 template <int D>
-__device__ __forceinline__ void rope_row(float (&v)[D / 32], int lane, const float* __restrict__ c,
-                                         const float* __restrict__ s, int mode) {
-  constexpr int E = D / 32;
-  if (mode == 1) {
-    // pairs (2i, 2i+1), both in this lane: angles lane*E/2 .. +E/2
-    float cv[E / 2], sv[E / 2];
-    load_row_f32<E / 2>(cv, c + lane * (E / 2));
-    load_row_f32<E / 2>(sv, s + lane * (E / 2));
+__device__ __forceinline__ void rotate_row(float (&v)[QCfg<D>::E], int p, const uint32_t (&smask)[2]) {
+  constexpr int E = QCfg<D>::E, G = QCfg<D>::G;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    v[e] = __uint_as_float(__float_as_uint(v[e]) ^ ((smask[e >> 5] << (31 - (e & 31))) & 0x80000000u));
+  // stride 1 (inside a lane, scalar)
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const float a = v[e], b = v[e + 1];
+    v[e] = __fadd_rn(a, b);
+    v[e + 1] = __fsub_rn(a, b);
+  }
+  // strides 2 .. G/2 (inside a lane, packed pairs)
+#pragma unroll
+  for (int h = 2; h < G; h <<= 1) {
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
-      const float cs = cv[e / 2], sn = sv[e / 2];
-      const float a = v[e], b = v[e + 1];
-      v[e] = __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn));
-      v[e + 1] = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
+      if (!(e & h)) {
+        const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + h], v[e + h + 1]);
+        const float2 s = add2(a, b), d = sub2(a, b);
+        v[e] = s.x; v[e + 1] = s.y;
+        v[e + h] = d.x; v[e + h + 1] = d.y;
+      }
     }
-  } else if (mode == 2) {
-    // pairs (i, i + D/2): lane L < 16 holds i = L*E + e, lane L + 16 its partner
-    const bool first = lane < 16;
-    float cv[E], sv[E];
-    load_row_f32<E>(cv, c + (lane & 15) * E);
-    load_row_f32<E>(sv, s + (lane & 15) * E);
+  }
+  // strides G and 2G: the other quarters of the row (lanes 8 and 16 apart);
+  // the lower index takes a + b, the upper b' - a' as RN(partner - own)
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float cs = cv[e], sn = sv[e];
-      const float o = __shfl_xor_sync(0xffffffffu, v[e], 16);
-      const float a = first ? v[e] : o, b = first ? o : v[e];
-      v[e] = first ? __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)) : __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs));
+  for (int m = 8; m <= 16; m <<= 1) {
+    const bool upper = (p & (m >> 3)) != 0;
+    const float2 sg2 = make_float2(upper ? -1.0f : 1.0f, upper ? -1.0f : 1.0f);
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], m), __shfl_xor_sync(0xffffffffu, v[e + 1], m));
+      const float2 r = fma2(make_float2(v[e], v[e + 1]), sg2, o);
+      v[e] = r.x; v[e + 1] = r.y;
+    }
+  }
+  if constexpr (D == 256) {
+    // stride 128: local elements e and e + 32
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + 32], v[e + 33]);
+      const float2 s = add2(a, b), d = sub2(a, b);
+      v[e] = s.x; v[e + 1] = s.y;
+      v[e + 32] = d.x; v[e + 33] = d.y;
     }
   }
 }
 
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// MODE 0: per-block scale.  MODE 1: per-tensor amax into *amax_ws (atomic).
-// MODE 2: per-tensor encode with the amax in *amax_ws.
-// MODE 3: per-block amax stored to amax_ws[bh * nblk + blk] (no atomics).
-// ROPE: rotary embedding first (pairing `rope`, 1 or 2); separate instances
-// keep the plain path's code unchanged.
+// MODE 0: per-block scale.  MODE 1: per-tensor maximum into *ws (one atomic
+// max per CTA).  MODE 2: per-tensor encode with the maximum in *ws.
+// MODE 3: per-block maxima to ws[block] (no atomics).
 template <int D, int MODE, bool ROPE>
-__global__ void __launch_bounds__(256) quant_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ x8,
-                                                         float* __restrict__ descale, int N, int nblk,
-                                                         SignBits sg, int rot, float rinv,
-                                                         const float* __restrict__ rcos, const float* __restrict__ rsin,
-                                                         int rope, float* __restrict__ amax_ws, int* err) {
-  constexpr int E = D / 32;
-  constexpr int ROWS = 128;
-  extern __shared__ __align__(128) float ys[];  // [ROWS][D]: the block, rotated in place
-  __shared__ float red[8];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int failed;
-  const int blk = blockIdx.x;
-  const int bh = blockIdx.y;
+__global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
+    quant_e4m3_kernel(const __grid_constant__ CUtensorMap map, const QuantParams prm) {
+  using C = QCfg<D>;
+  constexpr int E = C::E, RS = C::RS, NSG = C::NSG;
+  extern __shared__ __align__(1024) uint8_t qsmem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+  QShared<C::NSLOT>* sh = reinterpret_cast<QShared<C::NSLOT>*>(ring + C::NSLOT * C::SLOT_BYTES);
+  volatile int* abort_flag = &sh->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blk * ROWS;
-  const int nrows = min(ROWS, N - r0);
-  const size_t base = ((size_t)bh * N + r0) * D;
+  const int G = (int)gridDim.x;
+  const int grp = warp / C::WG;     // group of this warp
+  const int wg = warp % C::WG;      // warp within the group
+  const int p = lane >> 3;          // quarter of the row held by this lane
+  const int rl = lane & 7;          // row within the warp's 8-row set
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    failed = 0;
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 8);  // the 8 warps that read a slot's rows
+      sh->last_pos[s] = -1;
+    }
+    sh->abort_flag = 0;
+    sh->first_bad = INT_MAX;
     fence_barrier_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t bytes = (uint32_t)(nrows * D * sizeof(float));
-    mbar_arrive_expect_tx(&bar, bytes);
-    bulk_load(ys, x + base, bytes, &bar);
-    // bounded wait for the block
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&bar, 0)) {
-      if (globaltimer() - t0 > FA_WAIT_LIMIT_NS) {
-        failed = 1;
-        if (err) atomicExch(err, FA_DEVERR_TIMEOUT);
+
+  // Block iteration `it` of this CTA is blockIdx.x + it * G; group g takes
+  // it = g, g + NG, g + 2 NG, ...  Its j-th block fills group positions 2j
+  // (rows 0..63) and 2j + 1 (rows 64..127) of the group's ring of NSG slots.
+  // Row set k of this warp: half hk, row r_slot within the half.
+  auto half_of = [&](int k) -> int { return (C::NG == 2) ? k : wg / 8; };
+  const int r_slot = (wg % 8) * 8 + rl;
+  uint8_t* gring = ring + grp * NSG * C::SLOT_BYTES;
+  uint64_t* gfull = &sh->full[grp * NSG];
+  uint64_t* gempty = &sh->empty[grp * NSG];
+  int* glast = &sh->last_pos[grp * NSG];
+
+  // Loads: lane 0 of the group's first warp keeps the group's ring full,
+  // issuing group position q once the slot's previous position was released.
+  int issued = 0;
+  bool more = true;
+  const bool issuer = (wg == 0 && lane == 0);
+  auto issue_upto = [&](int limit) -> bool {
+    bool ok = true;
+    if (issuer) {
+      for (; more && issued < limit; ++issued) {
+        const int q = issued;
+        const int it = C::NG * (q >> 1) + grp;
+        const int b = blockIdx.x + it * G;
+        if (b >= prm.total) { more = false; break; }
+        const int bh = b / prm.nblk, blk = b - bh * prm.nblk;
+        const int slot = q % NSG;
+        if (!mbar_wait(&gempty[slot], (uint32_t)(((q / NSG) & 1) ^ 1), abort_flag, prm.err)) {
+          ok = false;
+          break;
+        }
+        // test hook: this position is never filled, so its consumers' wait runs out
+        if (q == prm.drop_pos && blockIdx.x == 0 && grp == 0) continue;
+        const int row0 = blk * 128 + (q & 1) * C::SLOT_ROWS;
+        if (row0 >= prm.N) {
+          mbar_arrive(&gfull[slot]);  // nothing to load: rows past N are zeros
+        } else {
+          mbar_arrive_expect_tx(&gfull[slot], C::SLOT_BYTES);
+          uint8_t* dst = gring + slot * C::SLOT_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::BOXES; ++k) tma_load_3d(dst + k * C::BOX_BYTES, &map, &gfull[slot], 32 * k, row0, bh);
+        }
+        glast[slot] = q;
+      }
+    }
+    return ok;
+  };
+  if (issuer) tma_prefetch_desc(&map);
+
+  // sign bits of this lane's elements (selected, not indexed, so that the
+  // parameter block stays out of local memory)
+  uint32_t smask[2] = {0u, 0u};
+  if (prm.rot) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t w = prm.sg.w[k];
+      if constexpr (D == 64) {
+        if (k == (p >> 1)) smask[0] = (w >> (16 * (p & 1))) & 0xffffu;
+      } else {
+        if (k == p) smask[0] = w;
+        if (D == 256 && k == p + 4) smask[1] = w;
+      }
+    }
+  }
+  float s_t = 1.0f;  // MODE 2: the tensor's scale
+  if constexpr (MODE == 2) {
+    const float am = *prm.ws;
+    s_t = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+  }
+  float cta_max = 0.0f;  // MODE 1
+  const int N = prm.N, nblk = prm.nblk, total = prm.total;
+
+  for (int j = 0;; ++j) {
+    const int it = C::NG * j + grp;
+    const int b = blockIdx.x + it * G;
+    if (b >= total) break;
+    const int bh = b / nblk, blk = b - bh * nblk;
+    bool ok = __shfl_sync(0xffffffffu, (int)issue_upto(2 * j + NSG), 0) != 0;
+    float v[RS][E];
+    float am = 0.0f;
+#pragma unroll
+    for (int k = 0; k < RS; ++k) {
+      const int hk = half_of(k);
+      const int pos = 2 * j + hk;
+      const int slot = pos % NSG;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&gfull[slot], (uint32_t)((pos / NSG) & 1), abort_flag, prm.err));
+      if (ok) {
+        const uint8_t* src = gring + slot * C::SLOT_BYTES + r_slot * 128;
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const int i = elem_of<D>(e, p);
+          const int ch = (i & 31) >> 2;
+          const float4 t = *reinterpret_cast<const float4*>(src + (i >> 5) * C::BOX_BYTES + ((ch ^ rl) << 4));
+          v[k][e] = t.x; v[k][e + 1] = t.y; v[k][e + 2] = t.z; v[k][e + 3] = t.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&gempty[slot]);
+        // refill the slot as soon as the group has read it (a failure here
+        // shows up at the next block's issue)
+        (void)__shfl_sync(0xffffffffu, (int)issue_upto(2 * j + NSG + hk + 1), 0);
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int k = 0; k < RS; ++k) {
+        const int n = blk * 128 + half_of(k) * C::SLOT_ROWS + r_slot;
+        if (n >= N) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[k][e] = 0.0f;
+        }
+        if constexpr (ROPE) {
+          const size_t nr = (size_t)(n < N ? n : N - 1) * (D / 2);
+          rope_row<D>(v[k], p, prm.rcos + nr, prm.rsin + nr, prm.rope);
+        }
+        if (prm.rot) rotate_row<D>(v[k], p, smask);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) am = max3f(am, fabsf(v[k][e]), fabsf(v[k][e + 1]));
+      }
+    }
+
+    float s = 1.0f;
+    if constexpr (MODE == 1) {
+      if (!ok) {
+        if (lane == 0) atomicMin(&sh->first_bad, it);
         break;
       }
-    }
-  }
-  __syncthreads();
-  if (failed) return;
-
-  float amax = 0.0f;
-  for (int r = warp; r < nrows; r += 8) {
-    float v[E];
-    float* yrow = ys + r * D + lane * E;
-    if constexpr (E == 2) {
-      const float2 t = *reinterpret_cast<const float2*>(yrow);
-      v[0] = t.x; v[1] = t.y;
-    } else {
-#pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        const float4 t = reinterpret_cast<const float4*>(yrow)[q];
-        v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
-      }
-    }
-    if constexpr (ROPE) rope_row<D>(v, lane, rcos + (size_t)(r0 + r) * (D / 2), rsin + (size_t)(r0 + r) * (D / 2), rope);
-    rotate_row<D>(v, lane, sg, rot != 0);
-#pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
-    if constexpr (MODE == 0) {
-      if (rot || ROPE) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) yrow[e] = v[e];
-      }
+      cta_max = fmaxf(cta_max, am);
+      continue;
     } else if constexpr (MODE == 2) {
-      // per-tensor encode: scale known up front
-      const float am = *amax_ws;
-      const float s = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
-      const float rs = __frcp_rn(s);
-      uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
-      if constexpr (E == 2) {
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fmul_rn(v[0], rs), __fmul_rn(v[1], rs));
-      } else {
+      if (!ok) {
+        if (lane == 0) atomicMin(&sh->first_bad, it);
+        break;
+      }
+      s = s_t;
+    } else {
+      // block maximum over the group's warps; the barrier also ends the loop
+      // for every warp of the group as soon as one of them could not read
 #pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          const uint32_t lo = e4m3x2(__fmul_rn(v[4 * q], rs), __fmul_rn(v[4 * q + 1], rs));
-          const uint32_t hi = e4m3x2(__fmul_rn(v[4 * q + 2], rs), __fmul_rn(v[4 * q + 3], rs));
-          reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
-        }
+      for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
+      float* red = &sh->red[0][0][0] + (grp * 2 + (j & 1)) * 8;   // one group: 16 entries over [0][parity]
+      if (C::NG == 1) red = &sh->red[0][0][0] + (j & 1) * 16;
+      if (lane == 0) red[wg] = am;
+      if (!bar_and(1 + grp, 32 * C::WG, ok)) {
+        if (lane == 0) atomicMin(&sh->first_bad, it);
+        break;
+      }
+      float bm = red[lane & (C::WG - 1)];
+#pragma unroll
+      for (int m = C::WG / 2; m >= 1; m >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, m));
+      if constexpr (MODE == 3) {
+        if (wg == 0 && lane == 0) prm.ws[b] = bm;
+        continue;
+      }
+      s = (bm > 0.0f) ? __fdiv_rn(bm, 448.0f) : 1.0f;
+    }
+    // encode: a scale too small for its reciprocal to stay finite is
+    // handled with y and s both scaled by 2^64 (exact)
+    float se = s;
+    if (s < 0x1p-64f) {
+      se = s * 0x1p64f;
+#pragma unroll
+      for (int k = 0; k < RS; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] *= 0x1p64f;
+    }
+    const float r = __frcp_rn(se);
+    const float rh = __fmul_rn(r, 0x1.00001p0f), rl_ = __fmul_rn(r, 0x1.ffffep-1f);
+    const float2 rh2 = make_float2(rh, rh), rl2 = make_float2(rl_, rl_);
+#pragma unroll
+    for (int k = 0; k < RS; ++k) {
+      uint32_t words[E / 4];
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) words[q] = encode4(&v[k][4 * q], rh2, rl2, se);
+      const int n = blk * 128 + half_of(k) * C::SLOT_ROWS + r_slot;
+      if (n < N) {
+        uint8_t* row = prm.x8 + ((size_t)bh * N + n) * D;
+#pragma unroll
+        for (int jj = 0; jj < E / 16; ++jj)
+          *reinterpret_cast<uint4*>(row + elem_of<D>(16 * jj, p)) =
+              make_uint4(words[4 * jj], words[4 * jj + 1], words[4 * jj + 2], words[4 * jj + 3]);
+      }
+    }
+    if (wg == 0 && lane == 0) prm.descale[b] = __fmul_rn(s, prm.rinv);
+  }
+  // never leave with copies in flight: after a timeout, each issuer waits
+  // (bounded) for the last fill of every slot of its group that was filled
+  if (issuer && *abort_flag) {
+    for (int sl = 0; sl < NSG; ++sl) {
+      const int q = glast[sl];
+      if (q < 0) continue;
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&gfull[sl], (uint32_t)((q / NSG) & 1)) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
       }
     }
   }
-  if constexpr (MODE == 2) {
-    if (threadIdx.x == 0) {
-      const float am = *amax_ws;
-      const float s = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
-      descale[(size_t)bh * nblk + blk] = __fmul_rn(s, rinv);
-    }
-    return;
-  }
-  // block amax
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  if (lane == 0) red[warp] = amax;
+  // the CTA's maximum (MODE 1) and, after a timeout, marks on every block
+  // from the first one some warp could not finish, so that no caller reads
+  // a stale or unwritten scale without the error word being set
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float a = (lane < 8) ? red[lane] : 0.0f;
-#pragma unroll
-    for (int m = 4; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
-    if (lane == 0) red[0] = a;
-  }
-  __syncthreads();
-  amax = red[0];
   if constexpr (MODE == 1) {
-    if (threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(amax_ws), __float_as_int(amax));
-    return;
-  } else if constexpr (MODE == 3) {
-    if (threadIdx.x == 0) amax_ws[(size_t)bh * nblk + blk] = amax;
-    return;
-  } else {
-    const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    const float rs = __frcp_rn(s);
-    for (int r = warp; r < nrows; r += 8) {
-      uint8_t* dst = x8 + base + (size_t)r * D + lane * E;
-      const float* y = ys + r * D + lane * E;
-      if constexpr (E == 2) {
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e4m3x2(__fmul_rn(y[0], rs), __fmul_rn(y[1], rs));
-      } else {
 #pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          const uint32_t lo = e4m3x2(__fmul_rn(y[4 * q], rs), __fmul_rn(y[4 * q + 1], rs));
-          const uint32_t hi = e4m3x2(__fmul_rn(y[4 * q + 2], rs), __fmul_rn(y[4 * q + 3], rs));
-          reinterpret_cast<uint32_t*>(dst)[q] = lo | (hi << 16);
-        }
+    for (int m = 16; m >= 1; m >>= 1) cta_max = fmaxf(cta_max, __shfl_xor_sync(0xffffffffu, cta_max, m));
+    if (lane == 0) (&sh->red[0][0][0])[warp] = cta_max;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mx = 0.0f;
+      for (int w = 0; w < C::NW; ++w) mx = fmaxf(mx, (&sh->red[0][0][0])[w]);
+      if (sh->first_bad != INT_MAX) mx = INFINITY;
+      atomicMax(reinterpret_cast<int*>(prm.ws), __float_as_int(mx));
+    }
+  } else {
+    if (threadIdx.x == 0 && sh->first_bad != INT_MAX) {
+      for (int bb = blockIdx.x + sh->first_bad * G; bb < total; bb += G) {
+        if constexpr (MODE == 3) prm.ws[bb] = INFINITY;
+        else prm.descale[bb] = __int_as_float(0x7fc00000);
       }
     }
-    if (threadIdx.x == 0) descale[(size_t)bh * nblk + blk] = __fmul_rn(s, rinv);
   }
 }
 
-// Dynamic shared memory of one block (128 rows x D fp32), set once per
-// device for each instance.
+int sm_count_cached() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (sms[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    sms[dev] = v;
+  }
+  return sms[dev];
+}
+
 template <int D, int MODE, bool ROPE>
-static cudaError_t prep_quant() {
+cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
+  using C = QCfg<D>;
+  auto kern = quant_e4m3_kernel<D, MODE, ROPE>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(quant_e4m3_kernel<D, MODE, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(128u * D * sizeof(float)));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  return cudaSuccess;
-}
-
-template <int D, int MODE, bool ROPE>
-static cudaError_t launch_mode_r(const QuantLaunch& L, float* ws) {
-  cudaError_t e = prep_quant<D, MODE, ROPE>();
-  if (e != cudaSuccess) return e;
-  const dim3 grid(L.nblk, L.BH, 1);
-  quant_e4m3_kernel<D, MODE, ROPE><<<grid, 256, 128u * D * sizeof(float), L.stream>>>(
-      L.x, L.x8, L.descale, L.N, L.nblk, L.signs, L.rot, L.rinv, L.rope_cos, L.rope_sin, L.rope, ws, L.err);
+  QuantParams prm;
+  prm.x8 = L.x8;
+  prm.descale = L.descale;
+  prm.ws = ws;
+  prm.err = L.err;
+  prm.rcos = L.rope_cos;
+  prm.rsin = L.rope_sin;
+  prm.sg = L.signs;
+  prm.N = L.N;
+  prm.nblk = L.nblk;
+  prm.total = L.BH * L.nblk;
+  prm.rot = L.rot;
+  prm.rinv = L.rinv;
+  prm.rope = L.rope;
+  prm.drop_pos = drop_pos;
+  const int sms = sm_count_cached();
+  const int grid = prm.total < sms ? prm.total : sms;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.map, prm);
   return cudaGetLastError();
 }
 
 template <int D, int MODE>
-static cudaError_t launch_mode(const QuantLaunch& L, float* ws) {
-  return L.rope ? launch_mode_r<D, MODE, true>(L, ws) : launch_mode_r<D, MODE, false>(L, ws);
+cudaError_t launch_mode(const QuantLaunch& L, float* ws, int drop_pos) {
+  return L.rope ? launch_one<D, MODE, true>(L, ws, drop_pos) : launch_one<D, MODE, false>(L, ws, drop_pos);
 }
 
 template <int D>
-static cudaError_t launch_quant_d(const QuantLaunch& L) {
-  if (!L.per_tensor) return launch_mode<D, 0>(L, nullptr);
+cudaError_t launch_quant_d(const QuantLaunch& L) {
+  if (!L.per_tensor) return launch_mode<D, 0>(L, nullptr, L.drop_pos);
   cudaError_t e = cudaMemsetAsync(L.amax_ws, 0, sizeof(float), L.stream);
   if (e != cudaSuccess) return e;
-  e = launch_mode<D, 1>(L, L.amax_ws);
+  e = launch_mode<D, 1>(L, L.amax_ws, L.drop_pos);
   if (e != cudaSuccess) return e;
-  return launch_mode<D, 2>(L, L.amax_ws);
+  return launch_mode<D, 2>(L, L.amax_ws, -1);
 }
 
 // Maximum of n partial maxima -> *out (one CTA).
@@ -317,14 +600,16 @@ __global__ void __launch_bounds__(1024) reduce_max_kernel(const float* __restric
 }
 
 template <int D>
-static cudaError_t launch_quant_partials_d(const QuantLaunch& L, float* partials, float* amax_out) {
-  cudaError_t e = launch_mode<D, 3>(L, partials);
+cudaError_t launch_quant_partials_d(const QuantLaunch& L, float* partials, float* amax_out) {
+  cudaError_t e = launch_mode<D, 3>(L, partials, L.drop_pos);
   if (e != cudaSuccess) return e;
   reduce_max_kernel<<<1, 1024, 0, L.stream>>>(partials, L.BH * L.nblk, amax_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_mode<D, 2>(L, amax_out);
+  return launch_mode<D, 2>(L, amax_out, -1);
 }
+
+}  // namespace
 
 cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partials, float* amax_out) {
   switch (L.d) {

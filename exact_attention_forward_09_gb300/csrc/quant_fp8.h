@@ -1,8 +1,12 @@
-// quant_fp8.h -- launch interface of the FP8 E4M3 quantisation kernel.
+// quant_fp8.h -- launch interface of the FP8 E4M3 quantisation kernel, and
+// the library internals its C-ABI entry points share with api.cu.
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include "fa.h"
 
 namespace fa {
 
@@ -12,6 +16,7 @@ struct SignBits {
 };
 
 struct QuantLaunch {
+  CUtensorMap map;  // x as [BH, N, d] fp32: 32-float x 64-row boxes, 128-byte swizzle
   const float* x;   // [BH, N, d] fp32
   uint8_t* x8;      // [BH, N, d] E4M3 codes
   float* descale;   // [BH, nblk]
@@ -28,6 +33,9 @@ struct QuantLaunch {
   const float* rope_cos;
   const float* rope_sin;
   int rope;
+  // test hook: the first CTA of the first launch of this call never fills
+  // this slot position (-1: none), so the bounded waits on it run out
+  int drop_pos;
   cudaStream_t stream;
 };
 
@@ -35,7 +43,18 @@ cudaError_t launch_quant(const QuantLaunch& L);
 
 // Per-tensor mode with caller-provided scratch: per-block maxima go to
 // partials[BH * nblk], their maximum to *amax_out, then the encode pass runs.
-// Every partial is written before it is read, so nothing needs clearing.
+// Every partial is written before it is read, so nothing needs clearing (a
+// block whose load timed out writes +inf, never leaves an old value).
 cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partials, float* amax_out);
+
+// Library internals defined in api.cu.
+// Once per device: architecture check, the device error word's address and
+// the tensor-map encoder; then the current device and its error word.
+fa_status internal_device_setup(int* dev, int** err);
+// Tensor map of a contiguous fp32 [BH, N, d] tensor for the quantiser.
+fa_status internal_encode_quant_map(CUtensorMap* map, const float* x, int64_t BH, int64_t N, int64_t d);
+// Consume a pending quantiser failure injection (fa_debug_inject flag 2):
+// the slot position to leave unfilled, or -1.
+int internal_take_quant_inject();
 
 }  // namespace fa

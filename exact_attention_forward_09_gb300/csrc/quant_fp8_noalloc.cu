@@ -15,10 +15,12 @@
 // maximum, so a call is limited to FA_QUANT_NOALLOC_MAX_BLOCKS blocks
 // (B * H * ceil(N / 128)); larger calls are rejected with
 // FA_ERR_SCRATCH_LIMIT before anything is launched.  Every partial a call
-// reads was written earlier in the same call, so nothing has to be cleared;
-// but all calls share the one array, so two calls that overlap on the GPU
-// (different streams, or different host threads on one device) race and may
-// produce wrong scales.  Serialise them.
+// reads was written earlier in the same call, so nothing has to be cleared:
+// a block whose input load timed out writes +inf (and the library's error
+// word is set, reported by fa_check_device_error), never leaves an earlier
+// call's value in place.  But all calls share the one array, so two calls
+// that overlap on the GPU (different streams, or different host threads on
+// one device) race and may produce wrong scales.  Serialise them.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -72,6 +74,7 @@ extern "C" fa_status fa_quant_fp8_per_tensor_noalloc(const float* x, void* x8, f
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   const int64_t nblk = (N + 127) / 128;
+  if (N > ((int64_t)1 << 31) - 128) return FA_ERR_UNSUPPORTED;
   if (B * H > FA_QUANT_NOALLOC_MAX_BLOCKS || B * H * nblk > FA_QUANT_NOALLOC_MAX_BLOCKS)
     return FA_ERR_SCRATCH_LIMIT;
   if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
@@ -94,9 +97,13 @@ extern "C" fa_status fa_quant_fp8_per_tensor_noalloc(const float* x, void* x8, f
     L.rinv = 1.0f;
   }
 
-  float* scratch = nullptr;
-  const fa_status st = scratch_for_current_device(&scratch);
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = fa::internal_device_setup(&dev, &err);
   if (st != FA_OK) return st;
+  float* scratch = nullptr;
+  if ((st = scratch_for_current_device(&scratch)) != FA_OK) return st;
+  if ((st = fa::internal_encode_quant_map(&L.map, x, B * H, N, d)) != FA_OK) return st;
 
   L.x = x;
   L.x8 = static_cast<uint8_t*>(x8);
@@ -107,6 +114,8 @@ extern "C" fa_status fa_quant_fp8_per_tensor_noalloc(const float* x, void* x8, f
   L.d = (int)d;
   L.nblk = (int)nblk;
   L.per_tensor = 1;
+  L.err = err;
+  L.drop_pos = fa::internal_take_quant_inject();
   L.stream = stream;
   return fa::launch_quant_per_tensor_partials(L, scratch, scratch + FA_QUANT_NOALLOC_MAX_BLOCKS) == cudaSuccess
              ? FA_OK

@@ -279,9 +279,19 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, s
  *   workspace      per_tensor = 1: DEVICE pointer to one float of scratch
  *                  (overwritten; calls sharing it must not overlap on the GPU);
  *                  per_tensor = 0: ignored, may be NULL
- * Codes are round-to-nearest-even of y * RN(1 / scale) in fp32 (the scale's
- * correctly rounded reciprocal, then one product per element), saturated at
- * 448.
+ * The rotated value y is fp32 (sign flip, then the Walsh-Hadamard butterfly
+ * with strides 1, 2, 4, ...), scale = amax(y) / 448 rounded to fp32, and each
+ * code is the E4M3 value nearest to the exact quotient y / scale (ties to
+ * even, saturated at 448): a single rounding, decided exactly.
+ * Errors: FA_ERR_INVALID_ARG for negative sizes, null or misaligned pointers
+ * (x, x8 16-byte aligned), signs other than +-1, per_tensor not 0 / 1 or a
+ * missing workspace; FA_ERR_UNSUPPORTED for d not in {64, 128, 256}, more
+ * than 2^31 - 1 blocks, or a device other than sm_103; FA_ERR_CUDA for a
+ * launch error.  B*H*N = 0 is a no-op.  A bounded wait inside the kernel that
+ * runs out (about 2 s) sets the library's error word (fa_check_device_error
+ * then returns FA_ERR_TIMEOUT) and marks the blocks it could not finish with
+ * a NaN descale (per-tensor mode: an infinite scale) instead of leaving old
+ * values.
  */
 fa_status fa_quant_fp8(const float* x, void* x8, float* descale,
                        int64_t B, int64_t H, int64_t N, int64_t d,
@@ -339,8 +349,11 @@ fa_status fa_quant_fp8_rope(const float* x, void* x8, float* descale,
  *   stream capture.
  *   All calls share the one scratch array and it keeps the last call's
  *   contents (each call writes every entry it reads, so nothing needs
- *   clearing): calls that overlap on the GPU -- other streams, other host
- *   threads on the same device -- race and can produce wrong scales.
+ *   clearing; a block whose input load timed out writes +inf and sets the
+ *   library's error word, see fa_check_device_error): calls that overlap on
+ *   the GPU -- other streams, other host threads on the same device -- race
+ *   and can produce wrong scales.
+ *   Errors: as fa_quant_fp8 (per_tensor = 1), plus FA_ERR_SCRATCH_LIMIT.
  */
 #define FA_QUANT_NOALLOC_MAX_BLOCKS 65536
 fa_status fa_quant_fp8_per_tensor_noalloc(const float* x, void* x8, float* descale,
@@ -360,14 +373,20 @@ fa_status fa_check_device_error(cudaStream_t stream);
 
 /*
  * fa_debug_inject -- TEST HOOK for the failure path; not for production use.
- * flags = 1: the next fa_fwd / fa_fwd_fp8 launch has its first CTA leave
+ * flags bit 0: the next fa_fwd / fa_fwd_fp8 launch has its first CTA leave
  * one K/V ring slot unfilled (the next fa_bwd launch: one Q/dO stage of its
  * first CTA's second step), so the bounded waits on it run out (about 2 s):
  * the kernel then stops every role, frees its tensor memory and ends, and
  * fa_check_device_error() returns FA_ERR_TIMEOUT.  The output of that
  * launch is incomplete.  The flag is consumed by the next fa_fwd*,
  * fa_fwd_fp8* or fa_bwd call.
- * flags = 0 clears a pending injection.  Other values: FA_ERR_INVALID_ARG.
+ * flags bit 1: the same for the next quantiser call (fa_quant_fp8,
+ * fa_quant_fp8_rope or fa_quant_fp8_per_tensor_noalloc): the first CTA of its
+ * first launch leaves one input slot unfilled; the blocks it cannot finish
+ * get a NaN descale (per-tensor: an infinite maximum) and the error word is
+ * set.
+ * flags = 0 clears pending injections.  Values outside 0..3:
+ * FA_ERR_INVALID_ARG.
  */
 fa_status fa_debug_inject(int flags);
 

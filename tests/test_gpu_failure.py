@@ -6,8 +6,12 @@ usable for the next, correct call."""
 import math
 import time
 
+import numpy as np
 import pytest
 import torch
+
+import attn_inputs as gen
+import oracle
 
 from gpu_util import assert_bf16_parity, errors, make_qkv, oracle_rows
 
@@ -64,6 +68,37 @@ def test_backward_pipeline_timeout_is_reported_and_context_survives(fa, d):
     assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
 
 
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quantiser_timeout_is_reported_and_next_call_exact(fa, per_tensor):
+    """The quantiser's first CTA never gets one input slot: the bounded waits
+    run out, FA_ERR_TIMEOUT is reported, the blocks that CTA could not finish
+    carry a NaN descale (per tensor: an infinite maximum, so every descale is
+    infinite) instead of old values, and the next call is bit-exact."""
+    x = gen.outliers((2, 4, 1000, 128), 33)
+    xd = torch.from_numpy(x).cuda()
+    lib = fa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert lib.fa_debug_inject(2) == fa.FA_OK
+    t0 = time.time()
+    _, ds = fa.quant_fp8(xd, per_tensor=per_tensor)
+    st = lib.fa_check_device_error(stream)
+    assert st == fa.FA_ERR_TIMEOUT, lib.fa_status_string(st)
+    assert time.time() - t0 < 30.0
+    ds = ds.cpu().numpy()
+    if per_tensor:
+        assert np.isinf(ds).all()
+    else:
+        assert np.isnan(ds.reshape(-1)[0])
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    codes, ds = fa.quant_fp8(xd, per_tensor=per_tensor)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    codes_ref, ds_ref = oracle.quant_e4m3(x, per_tensor=per_tensor)
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+    assert np.array_equal(ds.cpu().numpy(), ds_ref)
+
+
 def test_inject_rejects_bad_flags(fa):
     assert fa.lib().fa_debug_inject(7) == fa.FA_ERR_INVALID_ARG
+    assert fa.lib().fa_debug_inject(-1) == fa.FA_ERR_INVALID_ARG
     assert fa.lib().fa_debug_inject(0) == fa.FA_OK

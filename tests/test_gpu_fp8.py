@@ -49,6 +49,20 @@ def test_quant_bit_exact(fa, d, N, rot, per_tensor):
     assert np.array_equal(ds.view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_quant_many_blocks_per_cta(fa, d):
+    # about seven 128-row blocks per CTA of the persistent grid, so the
+    # shared-memory ring wraps several times, in every mode
+    x = gen.outliers((1, 17, 8192, d), 63 + d)    # 1088 blocks
+    signs = gen.hadamard_signs(d, 4)
+    for sg, per_tensor in ((None, False), (signs, False), (None, True), (signs, True)):
+        codes_ref, ds_ref = oracle.quant_e4m3(x, signs=sg, per_tensor=per_tensor)
+        codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=sg, per_tensor=per_tensor)
+        fa.check_device_error()
+        assert np.array_equal(codes.cpu().numpy(), codes_ref), (sg is None, per_tensor)
+        assert np.array_equal(ds.cpu().numpy(), ds_ref), (sg is None, per_tensor)
+
+
 def test_quant_zero_block(fa):
     x = np.zeros((1, 1, 200, 128), dtype=np.float32)
     x[0, 0, 150, 3] = 2.0  # second block non-zero, first all zero
@@ -57,6 +71,49 @@ def test_quant_zero_block(fa):
     assert np.array_equal(codes.cpu().numpy(), codes_ref)
     assert np.array_equal(ds.cpu().numpy(), ds_ref)
     assert ds_ref[0, 0, 0] == 1.0 and codes_ref[0, 0, 150, 3] == 0x7E
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quant_exact_rounding_near_midpoints(fa, d, per_tensor):
+    # values within a few ulps of s times every E4M3 midpoint: the code must
+    # be the rounding of the exact quotient y / s, as rational arithmetic
+    # gives it (neither the fp32 quotient nor a product with a rounded
+    # reciprocal would match every one of these)
+    import oracle_pins as P
+    x, exp, s, _, _ = P._near_midpoint_block(d=d)
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), per_tensor=per_tensor)
+    fa.check_device_error()
+    got = codes.cpu().numpy()
+    assert np.array_equal(got, exp), f"{int((got != exp).sum())} codes differ from exact rounding"
+    assert ds.cpu().numpy().reshape(-1)[0] == np.float32(s)
+
+
+@pytest.mark.parametrize("mag", [1e-20, 1e-30, 1e-38, 1e-41])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quant_tiny_scales(fa, mag, per_tensor):
+    # block maxima far below 1: the scale's reciprocal leaves the fp32 range
+    # for the smallest ones (subnormal inputs and scales), which the kernel
+    # handles exactly; bit-exact against the oracle
+    x = (gen.normal((1, 2, 300, 128), 61) * np.float32(mag)).astype(np.float32)
+    signs = gen.hadamard_signs(128, 4)
+    for sg in (None, signs):
+        codes_ref, ds_ref = oracle.quant_e4m3(x, signs=sg, per_tensor=per_tensor)
+        codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=sg, per_tensor=per_tensor)
+        fa.check_device_error()
+        assert np.array_equal(codes.cpu().numpy(), codes_ref), (mag, sg is None)
+        assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32)), (mag, sg is None)
+
+
+def test_quant_many_heads(fa):
+    # 65536 heads of one row: more blocks than a 2-D grid could index by head
+    x = gen.outliers((4, 16384, 1, 64), 62)
+    for per_tensor in (False, True):
+        codes_ref, ds_ref = oracle.quant_e4m3(x, per_tensor=per_tensor)
+        codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), per_tensor=per_tensor)
+        fa.check_device_error()
+        assert np.array_equal(codes.cpu().numpy(), codes_ref)
+        assert np.array_equal(ds.cpu().numpy(), ds_ref)
 
 
 def _fp8_case(fa, B, H, N, d, causal, rot, per_tensor, seed, rows=None, sigma=10.0):

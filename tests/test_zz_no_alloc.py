@@ -12,6 +12,7 @@ This file sorts last so that a run stopping at the first failure has run
 every other test first; it also passes alone in a fresh process.
 """
 import ctypes
+import time
 
 import numpy as np
 import pytest
@@ -79,3 +80,49 @@ def test_noalloc_binding_and_limit(fa):
     assert st == fa.FA_ERR_SCRATCH_LIMIT
     st = fa.lib().fa_quant_fp8_per_tensor_noalloc(p, p, p, 2, 1, 128 * (lim // 2 + 1), 128, None, None)
     assert st == fa.FA_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_smaller_call_after_larger(fa):
+    # a large call leaves 16 * 16 * 8 partial maxima behind; a following call
+    # with one block and a far smaller maximum must not see any of them
+    big = torch.from_numpy(gen.outliers((16, 16, 1024, 128), 910, sigma=10.0)).cuda()
+    small = torch.from_numpy((gen.normal((1, 1, 129, 64), 911) * np.float32(1e-3)).astype(np.float32)).cuda()
+    for x, signs in ((big, gen.hadamard_signs(128, 4)), (small, None), (big, None), (small, None)):
+        ref8, ref_ds = fa.quant_fp8(x, signs=signs, per_tensor=True)
+        got8, got_ds = _noalloc_c(fa, x, signs)
+        torch.cuda.synchronize()
+        assert torch.equal(got8, ref8) and torch.equal(got_ds.view(torch.int32), ref_ds.view(torch.int32))
+    fa.check_device_error()
+
+
+def test_noalloc_many_heads_at_the_limit(fa):
+    # B * H = 65536 heads of one row: exactly the scratch limit, accepted
+    x = torch.from_numpy(gen.outliers((4, 16384, 1, 64), 912)).cuda()
+    ref8, ref_ds = fa.quant_fp8(x, per_tensor=True)
+    got8, got_ds = _noalloc_c(fa, x, None)
+    torch.cuda.synchronize()
+    assert torch.equal(got8, ref8) and torch.equal(got_ds, ref_ds)
+    fa.check_device_error()
+
+
+def test_noalloc_timeout_is_reported_and_next_call_exact(fa):
+    """A bounded wait that runs out (the test hook leaves one input slot of
+    the first CTA unfilled) sets the library's error word, and the blocks it
+    could not finish write +inf partials rather than keep the previous
+    call's: every descale comes out infinite, and the next call is exact."""
+    x = torch.from_numpy(gen.outliers((2, 4, 1000, 128), 913)).cuda()
+    lib = fa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    ref8, ref_ds = fa.quant_fp8(x, per_tensor=True)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert lib.fa_debug_inject(2) == fa.FA_OK
+    t0 = time.time()
+    _, ds = _noalloc_c(fa, x, None)
+    st = lib.fa_check_device_error(stream)
+    assert st == fa.FA_ERR_TIMEOUT, lib.fa_status_string(st)
+    assert time.time() - t0 < 30.0
+    assert torch.isinf(ds).all()
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    got8, got_ds = _noalloc_c(fa, x, None)
+    assert lib.fa_check_device_error(stream) == fa.FA_OK
+    assert torch.equal(got8, ref8) and torch.equal(got_ds, ref_ds)
