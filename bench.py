@@ -1,15 +1,21 @@
 """Benchmark of the fused attention forward on one GB300 (or N replicas).
 
-One step = one fa_fwd call on the workload (every step of the hot path runs
-inside that one kernel launch).  Default workload ("mid"): B=4, H=16,
-N=2048, d=128, bf16 Q/K/V drawn from N(0,1), non-causal, scale 1/sqrt(128).
+One step = one pass of the hot path over one batch.  Default workload
+("long"): B=1, H=16, N=65536, d=128, bf16 Q/K/V drawn from N(0,1), causal,
+scale 1/sqrt(128) -- the largest single-GPU configuration of the
+attention-forward benchmark, one fa_fwd launch per step.  The FP8 workloads
+("fp8_1k", "fp8_4k", "fp8_16k") make a step the whole FP8 path: quantise Q
+and K (block scales + Hadamard) and V (block scales), then fa_fwd_fp8.
 
-Timing: W untimed warm-up steps, then K timed steps; before each step a
-512 MB buffer is written to flush L2 (outside the timed events); each step is
-bracketed by CUDA events on the stream the kernel is launched on; the
-reported time is the sum over the K steps, the max over ranks.
+Timing: W untimed warm-up steps, then K timed steps; before each step L2 is
+flushed outside the timed events by writing a 512 MB buffer and then reading
+another 512 MB buffer (so the lines left in L2 are clean and no write-back of
+the flush lands inside the timed region); each step is bracketed by CUDA
+events on the stream the kernels are launched on; the reported time is the
+sum over the K steps, the max over ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra]
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 (independent problems, no data-path collective): weak scaling.
@@ -17,7 +23,6 @@ Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import math
@@ -38,6 +43,11 @@ METRIC = "attention fwd TFLOPS (BF16, FP8) and % of GB300 dense tensor peak, 1 G
 KERNEL_SOURCES = ["exact_attention_forward_09_gb300/csrc/attn_fwd.cuh",
                   "exact_attention_forward_09_gb300/csrc/ptx.cuh"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SHAPES = {"long": (1, 16, 65536, 128, True), "mid": (4, 16, 2048, 128, False),
+          "sweep4k": (4, 16, 4096, 128, False), "sweep16k": (1, 16, 16384, 128, False),
+          "fp8_1k": (16, 16, 1024, 128, False), "fp8_4k": (4, 16, 4096, 128, False),
+          "fp8_16k": (1, 16, 16384, 128, False)}
+FLUSH_BYTES = 512 * 1024 * 1024
 
 
 def kernel_source_hash() -> str:
@@ -74,7 +84,7 @@ def load_traffic(workload: str):
 # ---------------------------------------------------------------- clocks ----
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed
-    region (200 ms period)."""
+    region (50 ms period)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -89,7 +99,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -97,13 +107,13 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], 0.0, set()
+        sm, smax, power, reasons = [], 0.0, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -113,6 +123,7 @@ class ClockSampler:
                 try:
                     sm.append(float(parts[1]))
                     smax = max(smax, float(parts[2]))
+                    power.append(float(parts[3]))
                 except ValueError:
                     continue
                 for n, val in zip(names, parts[5:9]):
@@ -122,16 +133,32 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+class Flusher:
+    """Leaves L2 cold and clean: write a buffer larger than L2, then read
+    another one (the written lines are evicted, and written back, by the read,
+    outside the timed region)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, device=device, dtype=torch.float32)
+        self.r = torch.ones(FLUSH_BYTES // 4, device=device, dtype=torch.float32)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 # ------------------------------------------------------------ our arm -------
 def run_ours(args, rank, world, device):
+    import ctypes
+
     import torch
     import exact_attention_forward_09_gb300 as fa
 
-    B, H, N, d = args.B, args.H, args.N, args.d
-    causal = args.causal
+    B, H, N, d, causal = args.B, args.H, args.N, args.d, args.causal
     scale = 1.0 / math.sqrt(d)
     fp8 = args.fp8
     dtype = torch.float32 if fp8 else torch.bfloat16
@@ -142,10 +169,11 @@ def run_ours(args, rank, world, device):
     v = torch.randn((B, H, N, d), device=device, dtype=torch.float32, generator=g).to(dtype)
     o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
     lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
-    flush = torch.empty(512 * 1024 * 1024 // 4, device=device, dtype=torch.float32)
+    flush = Flusher(device)
     stream = torch.cuda.current_stream(device)
     flops = gen.flops(B, H, N, d, causal)
     signs = gen.hadamard_signs(d, 4)
+    keep = (ctypes.c_int8 * d)(*[int(x) for x in signs])
     if fp8:
         nb = (N + 127) // 128
         q8, k8, v8 = (torch.empty((B, H, N, d), device=device, dtype=torch.uint8) for _ in range(3))
@@ -159,7 +187,6 @@ def run_ours(args, rank, world, device):
         if fp8:
             lib = fa.lib()
             sp = torch.cuda.current_stream(device).cuda_stream
-            keep = (ctypes.c_int8 * d)(*[int(x) for x in signs])
             for x, c, ds, rot in ((qi, q8, qs, True), (ki, k8, ks, True), (vi, v8, vs, False)):
                 st = lib.fa_quant_fp8(x.data_ptr(), c.data_ptr(), ds.data_ptr(), B, H, N, d,
                                       ctypes.cast(keep, ctypes.c_void_p) if rot else None, 0, None, sp)
@@ -173,7 +200,7 @@ def run_ours(args, rank, world, device):
             fa.fwd(qi, ki, vi, causal=causal, scale=scale, out=o, lse=lse)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step(q, k, v)
     fa.check_device_error(device)
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
@@ -181,8 +208,9 @@ def run_ours(args, rank, world, device):
     _barrier(world)
     torch.cuda.synchronize(device)
     sampler.start()
+    time.sleep(0.1)
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         step(q, k, v, mid=ev[i][1])
         ev[i][2].record(stream)
@@ -233,14 +261,19 @@ def run_ours(args, rank, world, device):
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, device) / n_e2e
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    del qh, kh, vh, oh, lh
 
-    extra = {}
+    extra, fp8_point, short_n = {}, None, None
     if rank == 0 and not args.no_extra:
-        extra = run_extra(args, device)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+        fp8_point = run_fp8_point(device, flush)
+        short_n = run_short_n(device, flush)
+        extra = run_extra(device, flush)
 
     return dict(times_ms=times_ms, total_ms=total_ms, launch_ms=launch_ms, flops=flops, clocks=clocks,
-                launches_per_step=launches_per_step,
-                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, extra=extra)
+                launches_per_step=launches_per_step, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, extra=extra,
+                fp8_point=fp8_point, short_n=short_n)
 
 
 def _time_launches(fn, steps, device, flush):
@@ -248,7 +281,7 @@ def _time_launches(fn, steps, device, flush):
     stream = torch.cuda.current_stream(device)
     ts = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -258,14 +291,84 @@ def _time_launches(fn, steps, device, flush):
     return sum(ts) / len(ts)
 
 
-def run_extra(args, device):
-    """Secondary points (not the headline): causal and fp16 on the same
-    workload, the spec region N >= 4k at d = 128, and the FP8 path."""
+def run_fp8_point(device, flush):
+    """The FP8 half of the metric, on the largest FP8 configuration (B=1,
+    H=16, N=16384, d=128): attention alone against the FP8 peak, and the
+    whole FP8 step (three quantiser launches + attention)."""
+    import torch
+    import exact_attention_forward_09_gb300 as fa
+
+    peaks, src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * 2.0
+    B, H, N, d, _ = SHAPES["fp8_16k"]
+    g = torch.Generator(device=device)
+    g.manual_seed(11)
+    x = [torch.randn((B, H, N, d), device=device, generator=g) for _ in range(3)]
+    signs = gen.hadamard_signs(d, 4)
+    q8, qs = fa.quant_fp8(x[0], signs=signs)
+    k8, ks = fa.quant_fp8(x[1], signs=signs)
+    v8, vs = fa.quant_fp8(x[2])
+    o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+    attn = lambda: fa.fwd_fp8(q8, k8, v8, qs, ks, vs, out=o, lse=lse)
+
+    def whole():
+        fa.quant_fp8(x[0], signs=signs)
+        fa.quant_fp8(x[1], signs=signs)
+        fa.quant_fp8(x[2])
+        attn()
+
+    attn()
+    ms = _time_launches(attn, 10, device, flush)
+    ms_step = _time_launches(whole, 10, device, flush)
+    fl = gen.flops(B, H, N, d, False)
+    tf = fl / (ms * 1e-3) / 1e12
+    fa.check_device_error(device)
+    return {"workload": f"fp8_16k: B={B} H={H} N={N} d={d} non-causal, Q/K block scales + Hadamard, V block scales",
+            "value": tf, "unit": "TFLOPS", "ms": ms, "peak": fp8_peak, "frac": tf / fp8_peak,
+            "peak_source": f"{src} bf16 burst (cuBLAS GEMM) x 2, the nominal dense fp8:bf16 ratio",
+            "kernel": f"attn_fwd_kernel<e4m3,{d},non-causal>",
+            "step_ms": ms_step, "step_tflops": fl / (ms_step * 1e-3) / 1e12}
+
+
+def run_short_n(device, flush):
+    """Short sequences, where the forward sits at or below the ridge: HBM
+    GB/s on the algorithmic bytes (Q, K, V read once, O written once, LSE)
+    against the measured HBM bandwidth, beside TFLOPS."""
     import torch
     import exact_attention_forward_09_gb300 as fa
 
     peaks, _ = load_peaks()
-    flush = torch.empty(512 * 1024 * 1024 // 4, device=device, dtype=torch.float32)
+    g = torch.Generator(device=device)
+    g.manual_seed(12)
+    out = {}
+    for N, causal in ((512, False), (512, True), (1024, True)):
+        B, H, d = gen.TOTAL_TOKENS // N, 16, 128
+        q, k, v = (torch.randn((B, H, N, d), device=device, generator=g).to(torch.bfloat16) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+        fn = lambda: fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        fn()
+        ms = _time_launches(fn, 10, device, flush)
+        nbytes = 4 * q.numel() * 2 + lse.numel() * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tf = gen.flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        out[f"N{N}_d128{'_causal' if causal else ''}"] = {
+            "B": B, "H": H, "ms": round(ms, 4), "hbm_gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 3), "bytes": nbytes}
+    out["note"] = "algorithmic bytes = Q+K+V read + O written (bf16) + LSE (fp32); peak = measured HBM copy bandwidth"
+    return out
+
+
+def run_extra(device, flush):
+    """Secondary points (not the headline): the 16K-token sweep at every
+    (N, H, d) causal and not, the mid workload (bf16, fp16), FP8 at N=4096,
+    the quantiser's bandwidth, split-KV decode and the backward."""
+    import torch
+    import exact_attention_forward_09_gb300 as fa
+
+    peaks, _ = load_peaks()
     out = {}
     g = torch.Generator(device=device)
     g.manual_seed(7)
@@ -280,46 +383,45 @@ def run_extra(args, device):
         tf = gen.flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
         return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
 
-    out["mid_causal_bf16"] = bf(4, 16, 2048, 128, True)
+    out["mid"] = bf(4, 16, 2048, 128, False)
+    out["mid_causal"] = bf(4, 16, 2048, 128, True)
     out["mid_fp16"] = bf(4, 16, 2048, 128, False, torch.float16)
-    for N in (4096, 8192, 16384):
-        B = gen.TOTAL_TOKENS // N
-        out[f"sweep_N{N}_d128"] = bf(B, 16, N, 128, False)
-        out[f"sweep_N{N}_d128_causal"] = bf(B, 16, N, 128, True)
-    out["sweep_N8192_d64"] = bf(2, 32, 8192, 64, False)
-    out["sweep_N8192_d256"] = bf(2, 8, 8192, 256, False)
+    sweep = {}
+    for (_, B, H, N, d, _) in gen.sweep_configs():
+        for causal in (False, True):
+            r = bf(B, H, N, d, causal, reps=3)
+            sweep[f"N{N}_d{d}{'_causal' if causal else ''}"] = [r["tflops"], r["frac_of_bf16_peak"]]
+    out["sweep_16k_tokens"] = {"points": sweep, "format": "[TFLOPS, fraction of the bf16 peak]"}
 
-    # FP8: quantise (block scales + Hadamard on Q and K) then attention
+    # FP8 at N = 4096 (attention) and the quantiser's bandwidth on that input
     fp8_peak = peaks["bf16_tflops"] * 2.0
-    for N in (4096, 16384):
-        B = gen.TOTAL_TOKENS // N
-        x = [torch.randn((B, 16, N, 128), device=device, generator=g) for _ in range(3)]
-        signs = gen.hadamard_signs(128, 4)
-        q8, qs = fa.quant_fp8(x[0], signs=signs)
-        k8, ks = fa.quant_fp8(x[1], signs=signs)
-        v8, vs = fa.quant_fp8(x[2])
-        o = torch.empty((B, 16, N, 128), device=device, dtype=torch.bfloat16)
-        lse = torch.empty((B, 16, N), device=device, dtype=torch.float32)
-        fn = lambda: fa.fwd_fp8(q8, k8, v8, qs, ks, vs, out=o, lse=lse)
-        fn()
-        ms = _time_launches(fn, 5, device, flush)
-        tf = gen.flops(B, 16, N, 128, False) / (ms * 1e-3) / 1e12
-        qfn = lambda: fa.quant_fp8(x[0], signs=signs)
+    B, H, N, d = 4, 16, 4096, 128
+    x = [torch.randn((B, H, N, d), device=device, generator=g) for _ in range(3)]
+    signs = gen.hadamard_signs(d, 4)
+    q8, qs = fa.quant_fp8(x[0], signs=signs)
+    k8, ks = fa.quant_fp8(x[1], signs=signs)
+    v8, vs = fa.quant_fp8(x[2])
+    o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+    fn = lambda: fa.fwd_fp8(q8, k8, v8, qs, ks, vs, out=o, lse=lse)
+    fn()
+    ms = _time_launches(fn, 5, device, flush)
+    tf = gen.flops(B, H, N, d, False) / (ms * 1e-3) / 1e12
+    qbytes = x[0].numel() * 5  # 4 B read + 1 B written per element
+    quant = {}
+    cos, sin = (torch.from_numpy(t).to(device) for t in gen.rope_tables(N, d))
+    for name, qfn, extra_b in (("block", lambda: fa.quant_fp8(x[2]), 0),
+                               ("block_hadamard", lambda: fa.quant_fp8(x[0], signs=signs), 0),
+                               ("per_tensor", lambda: fa.quant_fp8(x[2], per_tensor=True), 0),
+                               ("rope_half_hadamard", lambda: fa.quant_fp8(x[0], signs=signs,
+                                                                          rope=(cos, sin, fa.FA_ROPE_HALF)),
+                                (cos.numel() + sin.numel()) * 4)):
         qms = _time_launches(qfn, 5, device, flush)
-        qbytes = x[0].numel() * 5  # 4 B read + 1 B written per element
-        # the same quantisation with the rotary embedding fused in (angle
-        # tables [N, d/2] cos + sin, shared by every head: 4 B each per pair)
-        cos, sin = (torch.from_numpy(t).to(device) for t in gen.rope_tables(N, 128))
-        rfn = lambda: fa.quant_fp8(x[0], signs=signs, rope=(cos, sin, fa.FA_ROPE_HALF))
-        rms = _time_launches(rfn, 5, device, flush)
-        rbytes = qbytes + (cos.numel() + sin.numel()) * 4
-        out[f"fp8_N{N}_d128"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
-                                 "frac_of_fp8_peak": round(tf / fp8_peak, 3),
-                                 "quant_ms_per_tensor": round(qms, 4),
-                                 "quant_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1),
-                                 "quant_rope_ms_per_tensor": round(rms, 4),
-                                 "quant_rope_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1)}
-    out["fp8_peak_note"] = "FP8 peak = measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"
+        gbs = (qbytes + extra_b) / (qms * 1e-3) / 1e9
+        quant[name] = {"us": round(qms * 1e3, 1), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
+    out["fp8_N4096_d128"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 3)}
+    out["quantiser_N4096_d128"] = quant
+    del x, q8, k8, v8, o, lse
 
     # decode-like: one query row per head against a long key/value cache,
     # GQA 4 (split-KV with the group's query heads packed), against the
@@ -342,6 +444,7 @@ def run_extra(args, device):
         dec[name] = {"ms": round(ms, 4), "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
     dec["workload"] = f"B={B} Hq={Hq} Hkv={Hkv} Nq=1 Nk={Nk} d={d} bf16, K/V {kv_bytes / 1e9:.2f} GB"
     out["decode"] = dec
+    del q, k, v, o, lse, ws
 
     # backward (dQ, dK, dV) from the forward's O and LSE; FLOPs counted as
     # 2.5x the forward's (five matrix products against two)
@@ -363,6 +466,7 @@ def run_extra(args, device):
     bwd["workload"] = ("bf16, 16K tokens per point; d=128: H=16, d=64: H=32; mid: B=4 N=2048, N8192: B=2; "
                        "dq, dk, dv from dO ~ N(0,1); one call per timed step after an L2 flush")
     out["backward"] = bwd
+    fa.check_device_error(device)
     return out
 
 
@@ -389,33 +493,51 @@ def _max_over_ranks(x, world, device):
 
 
 # ---------------------------------------------------- CPU oracle timing -----
-def time_oracle(B, H, N, d, causal, budget_s: float, max_heads: int | None = None):
+def sampled_rows(N: int, count: int) -> list:
+    """`count` query rows spread evenly over [0, N) (first and last included)."""
+    count = max(1, min(count, N))
+    if count == 1:
+        return [N - 1]
+    return sorted({round(i * (N - 1) / (count - 1)) for i in range(count)})
+
+
+def row_flops(rows, N: int, d: int, causal: bool) -> float:
+    """FLOPs of the sampled rows: 4 d per visible (query, key) pair."""
+    if causal:
+        return float(sum(4.0 * d * (r + 1) for r in rows))
+    return 4.0 * d * N * len(rows)
+
+
+def time_oracle(B, H, N, d, causal, budget_s: float):
     """Time the fp64 oracle as it stands on a bounded sample of the workload:
-    the first h heads (all rows), h chosen from a one-head calibration so the
-    run takes about `budget_s`.  Returns (TFLOPS, seconds, sample text, threads)."""
-    import numpy as np
+    R query rows of one head spread evenly over the sequence, R chosen from a
+    small calibration run so that the measured run takes about `budget_s`.
+    Returns (TFLOPS, seconds, sample text, threads)."""
     import oracle
 
     threads = oracle.max_threads()
-    shape = (1, 1, N, d)
-    q, k, v = gen.qkv_normal(shape, 99)
+    q, k, v = gen.qkv_normal((1, 1, N, d), 99)
+    scale = 1.0 / math.sqrt(d)
+    cal = sampled_rows(N, min(N, 64))
     t0 = time.perf_counter()
-    oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
-    t1 = time.perf_counter() - t0
-    heads = max(1, min(B * H, int(budget_s / max(t1, 1e-6))))
-    if max_heads:
-        heads = min(heads, max_heads)
-    q, k, v = gen.qkv_normal((1, heads, N, d), 98)
+    oracle.attn_fwd(q, k, v, causal=causal, scale=scale, rows=cal)
+    t1 = max(time.perf_counter() - t0, 1e-6)
+    per_flop = t1 / row_flops(cal, N, d, causal)
+    want = budget_s / per_flop
+    count = min(N, max(len(cal), int(len(cal) * want / row_flops(cal, N, d, causal))))
+    rows = sampled_rows(N, count)
     t0 = time.perf_counter()
-    oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+    oracle.attn_fwd(q, k, v, causal=causal, scale=scale, rows=rows)
     el = time.perf_counter() - t0
-    fl = gen.flops(1, heads, N, d, causal)
-    return fl / el / 1e12, el, f"{heads} of {B * H} heads, all {N} rows each, fp64", threads
+    fl = row_flops(rows, N, d, causal)
+    sample = (f"{len(rows)} of {N} query rows of 1 of {B * H} heads, spread evenly, fp64 C oracle; "
+              f"FLOPs counted as 4 d per visible (query, key) pair")
+    return fl / el / 1e12, el, sample, threads
 
 
 def run_reference(args, rank, world):
-    """The oracle timed as it stands: each step is a bounded sample (one head
-    of the workload, all rows).  Rank 0 only."""
+    """The oracle timed as it stands: each step is a bounded sample (query
+    rows of one head of the workload).  Rank 0 only."""
     import oracle
 
     if rank != 0:
@@ -423,15 +545,18 @@ def run_reference(args, rank, world):
     B, H, N, d, causal = args.B, args.H, args.N, args.d, args.causal
     threads = oracle.max_threads()
     q, k, v = gen.qkv_normal((1, 1, N, d), 97)
+    scale = 1.0 / math.sqrt(d)
+    rows = sampled_rows(N, 1024)
     for _ in range(args.warmup):
-        oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+        oracle.attn_fwd(q, k, v, causal=causal, scale=scale, rows=rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.attn_fwd(q, k, v, causal=causal, scale=1.0 / math.sqrt(d))
+        oracle.attn_fwd(q, k, v, causal=causal, scale=scale, rows=rows)
     el = time.perf_counter() - t0
-    fl = gen.flops(1, 1, N, d, causal) * args.steps
+    fl = row_flops(rows, N, d, causal) * args.steps
     val = fl / el / 1e12
-    sample = f"one head of {B * H} (all {N} rows) per step, fp64 C oracle"
+    sample = (f"{len(rows)} of {N} query rows (spread evenly) of 1 of {B * H} heads per step, fp64 C oracle; "
+              f"FLOPs counted as 4 d per visible (query, key) pair")
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
@@ -450,7 +575,8 @@ def _config(args):
     return {"workload": f"{args.workload}: B={args.B} H={args.H} N={args.N} d={args.d} {kind} "
                         f"{'causal' if args.causal else 'non-causal'} scale=1/sqrt(d)",
             "B": args.B, "H": args.H, "N": args.N, "d": args.d, "causal": bool(args.causal),
-            "l2": "flushed before every timed step (512 MB write, outside the timed events)",
+            "l2": "flushed before every timed step (512 MB write, then 512 MB read: cold, clean L2; "
+                  "outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
@@ -460,17 +586,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mid", choices=["mid", "sweep4k", "sweep16k", "long", "fp8_4k", "fp8_16k"])
-    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--workload", default="long", choices=sorted(SHAPES))
+    ap.add_argument("--causal", action="store_true", help="causal masks (the long workload is always causal)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
-    shapes = {"mid": (4, 16, 2048, 128), "sweep4k": (4, 16, 4096, 128), "sweep16k": (1, 16, 16384, 128),
-              "long": (1, 16, 65536, 128), "fp8_4k": (4, 16, 4096, 128), "fp8_16k": (1, 16, 16384, 128)}
     args.fp8 = args.workload.startswith("fp8")
-    args.B, args.H, args.N, args.d = shapes[args.workload]
-    if args.workload == "long":
-        args.causal = True
+    args.B, args.H, args.N, args.d, always_causal = SHAPES[args.workload]
+    args.causal = bool(args.causal or always_causal)
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -496,7 +619,7 @@ def main():
         e2e_tflops = res["flops"] * world / (res["e2e_ms"] * 1e-3) / 1e12
         cpu_tf, cpu_s, cpu_sample, cpu_threads = time_oracle(args.B, args.H, args.N, args.d, args.causal,
                                                               args.cpu_budget)
-        traffic = load_traffic(args.workload + ("_causal" if args.causal else ""))
+        traffic = load_traffic(args.workload + ("_causal" if args.causal and args.workload != "long" else ""))
         if args.fp8:
             peak = peaks["bf16_tflops"] * 2.0
             peak_source = f"{peak_src} bf16 burst (cuBLAS GEMM) x 2, the nominal dense fp8:bf16 ratio"
@@ -513,7 +636,9 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": peak_source, "kernel": kernel,
-                         "algorithmic_flops_per_launch": res["flops"]},
+                         "algorithmic_flops_per_launch": res["flops"],
+                         "frac_of_sustained": achieved / (peak * peaks.get("bf16_tflops_sustained", peak)
+                                                          / peaks["bf16_tflops"])},
             "cpu_baseline": {"value": cpu_tf, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
                              "sample": cpu_sample, "seconds": round(cpu_s, 2)},
             "e2e": {"value": e2e_tflops, "unit": "TFLOPS", "h2d_bytes_per_step": res["h2d"],
@@ -521,6 +646,8 @@ def main():
                     "call": "copies + quantiser + fa_fwd_fp8" if args.fp8 else "fa_fwd_host on pinned host buffers"},
             "gpu_launches": args.steps * res["launches_per_step"],
             "clocks": res["clocks"],
+            "fp8": res["fp8_point"],
+            "short_n_hbm": res["short_n"],
             "extra": res["extra"],
         }
         print(json.dumps(line), flush=True)

@@ -381,8 +381,9 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
 
   // fan out from the caller's stream
   if (cudaEventRecord(P.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  fa_status result = FA_OK;
   for (cudaStream_t s : {P.h2d[0], P.h2d[1], P.comp, P.d2h})
-    if (cudaStreamWaitEvent(s, P.start, 0) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, P.start, 0) != cudaSuccess) result = FA_ERR_CUDA;
   // chunks of whole key/value heads (each with its g query heads): the
   // copies of chunk c+1 run while chunk c computes and chunk c-1 copies back
   // chunk boundaries at multiples of `step` key/value heads, so that every
@@ -390,7 +391,7 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
   const int64_t rows = g * Nq;
   const int64_t step = (rows % 4 == 0) ? 1 : (rows % 2 == 0) ? 2 : 4;
   const int64_t nch = BHkv < kHostChunks ? BHkv : kHostChunks;
-  for (int64_t c = 0; c < nch; ++c) {
+  for (int64_t c = 0; c < nch && result == FA_OK; ++c) {
     const int64_t j0 = (BHkv * c / nch) / step * step;
     const int64_t j1 = (c + 1 == nch) ? BHkv : (BHkv * (c + 1) / nch) / step * step;
     const int64_t nj = j1 - j0;
@@ -402,26 +403,35 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
             cudaSuccess ||
         cudaMemcpyAsync(vd + j0 * kv_row, vh + j0 * kv_row, (size_t)(nj * kv_row), cudaMemcpyHostToDevice, hs) !=
             cudaSuccess ||
-        cudaEventRecord(P.copied[c], hs) != cudaSuccess || cudaStreamWaitEvent(P.comp, P.copied[c], 0) != cudaSuccess)
-      return FA_ERR_CUDA;
+        cudaEventRecord(P.copied[c], hs) != cudaSuccess || cudaStreamWaitEvent(P.comp, P.copied[c], 0) != cudaSuccess) {
+      result = FA_ERR_CUDA;
+      break;
+    }
     // the chunk as nj batches of one key/value head and its g query heads
     st = fa_fwd_gqa(qd + j0 * q_row, kd + j0 * kv_row, vd + j0 * kv_row, od + j0 * q_row, ld + j0 * g * Nq, nj, g,
                     1, Nq, Nk, d, causal, scale, dtype, P.comp);
-    if (st != FA_OK) return st;
+    if (st != FA_OK) {
+      result = st;
+      break;
+    }
     if (cudaEventRecord(P.computed[c], P.comp) != cudaSuccess ||
         cudaStreamWaitEvent(P.d2h, P.computed[c], 0) != cudaSuccess ||
         cudaMemcpyAsync(oh + j0 * q_row, od + j0 * q_row, (size_t)(nj * q_row), cudaMemcpyDeviceToHost, P.d2h) !=
             cudaSuccess ||
         cudaMemcpyAsync(lse_host + j0 * g * Nq, ld + j0 * g * Nq, (size_t)(nj * g * Nq * 4), cudaMemcpyDeviceToHost,
-                        P.d2h) != cudaSuccess)
-      return FA_ERR_CUDA;
+                        P.d2h) != cudaSuccess) {
+      result = FA_ERR_CUDA;
+      break;
+    }
   }
-  // join back into the caller's stream
+  // join back into the caller's stream -- after an error too, so that work
+  // the caller enqueues next never runs ahead of copies that still read or
+  // write its host buffers
   cudaStream_t all[4] = {P.h2d[0], P.h2d[1], P.comp, P.d2h};
   for (int i = 0; i < 4; ++i)
     if (cudaEventRecord(P.done[i], all[i]) != cudaSuccess || cudaStreamWaitEvent(stream, P.done[i], 0) != cudaSuccess)
-      return FA_ERR_CUDA;
-  return FA_OK;
+      if (result == FA_OK) result = FA_ERR_CUDA;
+  return result;
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H, int64_t N,

@@ -27,7 +27,7 @@ def test_reference_line_has_the_contract_keys():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
-    assert line["config"]["workload"].startswith("mid")
+    assert line["config"]["workload"].startswith("long")
 
 
 def test_reference_other_ranks_are_silent():
