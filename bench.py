@@ -15,7 +15,10 @@ events on the stream the kernels are launched on; the reported time is the
 sum over the K steps, the max over ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-extra]
+                    [--workload NAME] [--no-extra] [--ablate]
+
+--ablate times the kernel variants of libfa_ablate.so (one design choice of
+the attention kernel switched each) on a few workloads instead.
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 (independent problems, no data-path collective): weak scaling.
@@ -470,6 +473,72 @@ def run_extra(device, flush):
     return out
 
 
+ABLATE_VARIANTS = {0: "shipped kernel", 1: "split softmax (two warpgroups per Q tile, 64 keys each)",
+                   2: "eager rescale (no lazy threshold)", 4: "P handed over whole (not in two halves)",
+                   8: "one Q tile per CTA, S double-buffered (no two-tile alternation)",
+                   16: "no work stealing"}
+ABLATE_BUILT = {(False, False): (0, 1, 2, 4, 8, 16), (False, True): (0, 1, 8, 16), (True, False): (0, 1, 2, 4, 8, 16)}
+
+
+def run_ablate(args, device):
+    """Time the kernel variants of libfa_ablate.so (include/fa_ablate.h): each
+    switches one design choice of the attention kernel; TFLOPS and the ratio
+    to the shipped kernel, per workload."""
+    import ctypes
+
+    import torch
+    import exact_attention_forward_09_gb300 as fa
+    from exact_attention_forward_09_gb300 import build as fa_build
+
+    fa.lib()  # the product library must be present too (same build)
+    lib = ctypes.CDLL(fa_build.LIB_ABLATE)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.fa_ablate_fwd.argtypes = [i32, i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, f32, vp, vp, vp, vp]
+    lib.fa_ablate_fwd.restype = i32
+    flush = Flusher(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(13)
+    out = {}
+    for name, (B, H, N, causal, fp8) in (("N16384_bf16", (1, 16, 16384, False, False)),
+                                         ("mid_bf16", (4, 16, 2048, False, False)),
+                                         ("N16384_bf16_causal", (1, 16, 16384, True, False)),
+                                         ("mid_bf16_causal", (4, 16, 2048, True, False)),
+                                         ("N16384_fp8", (1, 16, 16384, False, True)),
+                                         ("N4096_fp8", (4, 16, 4096, False, True))):
+        d = 128
+        if fp8:
+            x = [torch.randn((B, H, N, d), device=device, generator=g) for _ in range(3)]
+            signs = gen.hadamard_signs(d, 4)
+            q, qs = fa.quant_fp8(x[0], signs=signs)
+            k, ks = fa.quant_fp8(x[1], signs=signs)
+            v, vs = fa.quant_fp8(x[2])
+            ds = (qs.data_ptr(), ks.data_ptr(), vs.data_ptr())
+        else:
+            q, k, v = (torch.randn((B, H, N, d), device=device, generator=g).to(torch.bfloat16) for _ in range(3))
+            ds = (None, None, None)
+        o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
+        lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
+        res = {}
+        for var in ABLATE_BUILT[(fp8, causal)]:
+            def fn(var=var):
+                st = lib.fa_ablate_fwd(var, int(fp8), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), B, H, N, d, int(causal), 1.0 / math.sqrt(d), *ds,
+                                       torch.cuda.current_stream(device).cuda_stream)
+                assert st == 0, st
+            fn()
+            ms = _time_launches(fn, args.steps, device, flush)
+            res[var] = {"variant": ABLATE_VARIANTS[var], "ms": round(ms, 4),
+                        "tflops": round(gen.flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12, 1)}
+        base = res[0]["tflops"]
+        for var in res:
+            res[var]["vs_shipped"] = round(res[var]["tflops"] / base, 3)
+        out[name] = {"shape": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'} "
+                              f"{'e4m3' if fp8 else 'bf16'}", "variants": res}
+        fa.check_device_error(device)
+    print(json.dumps({"ablation": out, "steps_per_point": args.steps,
+                      "l2": "flushed before every timed launch (512 MB write, then 512 MB read)"}), flush=True)
+
+
 def whole_job_tflops(flops_per_rank_step: float, world: int, total_ms_max: float, steps: int) -> float:
     """Whole-job throughput: every rank runs `steps` steps of `flops_per_rank_step`
     (independent problems); the job takes the slowest rank's time."""
@@ -590,6 +659,8 @@ def main():
     ap.add_argument("--causal", action="store_true", help="causal masks (the long workload is always causal)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ablate", action="store_true",
+                    help="time the kernel variants of libfa_ablate.so instead (one GPU, one JSON line)")
     args = ap.parse_args()
     args.fp8 = args.workload.startswith("fp8")
     args.B, args.H, args.N, args.d, always_causal = SHAPES[args.workload]
@@ -607,6 +678,10 @@ def main():
     import torch
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
+    if args.ablate:
+        if rank == 0:
+            run_ablate(args, device)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)

@@ -2,7 +2,9 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into
 ``libfa.so`` beside this file.  Only a GB300-class toolchain target is
-built: ``-gencode arch=compute_103a,code=sm_103a``.
+built: ``-gencode arch=compute_103a,code=sm_103a``.  The kernel variants of
+``ablate_*.cu`` make ``libfa_ablate.so`` (include/fa_ablate.h), linked
+against libfa.so; only the benchmark's ablation mode and its test load it.
 """
 from __future__ import annotations
 
@@ -17,9 +19,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
+LIB_ABLATE = os.path.join(HERE, "libfa_ablate.so")
 UNITS = ["api.cu", "attn_bf16.cu", "attn_fp16.cu", "attn_fp8.cu", "quant_fp8.cu", "quant_fp8_noalloc.cu",
          "splitkv.cu", "attn_split_bf16.cu", "attn_split_fp16.cu", "attn_bwd.cu"]
-HEADERS = ["ptx.cuh", "attn_fwd.cuh", "quant_fp8.h", "attn_bwd.h"]
+ABLATE_UNITS = ["ablate_api.cu", "ablate_bf16.cu", "ablate_bf16_causal.cu", "ablate_fp8.cu"]
+HEADERS = ["ptx.cuh", "attn_fwd.cuh", "quant_fp8.h", "attn_bwd.h", "splitkv.h", "ablate_inst.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,13 +48,14 @@ def _stale(out, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "fa.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("fa.h", "fa_ablate.h")]
     objs = []
+    ablate_objs = []
     jobs = []
-    for u in UNITS:
+    for u in UNITS + ABLATE_UNITS:
         src = os.path.join(CSRC, u)
         obj = os.path.join(BUILD, u.replace(".cu", ".o"))
-        objs.append(obj)
+        (objs if u in UNITS else ablate_objs).append(obj)
         if force or _stale(obj, [src] + hdrs):
             jobs.append([nvcc()] + _flags(extra_flags) + ["-c", src, "-o", obj])
     if jobs:
@@ -61,13 +66,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if force or jobs or _stale(LIB, objs):
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", LIB + ".tmp"] + objs
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-            raise RuntimeError("link of libfa.so failed")
-        os.replace(LIB + ".tmp", LIB)
+    # the ablation library holds only its kernel variants and links against
+    # libfa.so (found beside it), so no kernel is loaded twice in a process
+    for lib, lobjs, extra in ((LIB, objs, []),
+                              (LIB_ABLATE, ablate_objs, ["-L" + HERE, "-lfa", "-Xlinker", "-rpath,$ORIGIN"])):
+        if force or jobs or _stale(lib, lobjs + ([LIB] if extra else [])):
+            cmd = [nvcc()] + ARCH + ["-shared", "-o", lib + ".tmp"] + lobjs + extra
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+                raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+            os.replace(lib + ".tmp", lib)
     return LIB
 
 

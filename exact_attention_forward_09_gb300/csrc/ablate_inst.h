@@ -1,0 +1,13 @@
+// ablate_inst.h -- the kernel variants built into libfa_ablate.so
+// (include/fa_ablate.h lists what each code switches).  Variant 0, the
+// shipped kernel, is not among them: fa_ablate_fwd runs it through
+// libfa.so's own entry points, so no kernel is loaded twice in a process.
+#pragma once
+
+#include "attn_fwd.cuh"
+
+#define FA_ABLATE_BF16_NONCAUSAL(X) X(kBF16, false, 1) X(kBF16, false, 2) \
+  X(kBF16, false, 4) X(kBF16, false, 8) X(kBF16, false, 16)
+#define FA_ABLATE_BF16_CAUSAL(X) X(kBF16, true, 1) X(kBF16, true, 8) X(kBF16, true, 16)
+#define FA_ABLATE_FP8(X) X(kE4M3, false, 1) X(kE4M3, false, 2) X(kE4M3, false, 4) \
+  X(kE4M3, false, 8) X(kE4M3, false, 16)

@@ -18,10 +18,26 @@
 #include "quant_fp8.h"
 #include "attn_bwd.h"
 
+// The attention kernels are instantiated in their own translation units
+// (attn_bf16.cu, attn_fp16.cu, attn_fp8.cu, attn_split_*.cu), compiled in
+// parallel; this one only calls them.
 namespace fa {
-template <int ELEM, int D, bool CAUSAL, bool SPLIT>
-cudaError_t launch_attn(const AttnLaunch& L);
-}
+#define FA_EXTERN_ATTN(E, D, C, S) extern template cudaError_t launch_attn<E, D, C, S, 0>(const AttnLaunch&);
+#define FA_EXTERN_ATTN_DC(E, S) \
+  FA_EXTERN_ATTN(E, 64, false, S) FA_EXTERN_ATTN(E, 64, true, S) FA_EXTERN_ATTN(E, 128, false, S) \
+  FA_EXTERN_ATTN(E, 128, true, S) FA_EXTERN_ATTN(E, 256, false, S) FA_EXTERN_ATTN(E, 256, true, S)
+FA_EXTERN_ATTN_DC(kBF16, false)
+FA_EXTERN_ATTN_DC(kFP16, false)
+FA_EXTERN_ATTN_DC(kBF16, true)
+FA_EXTERN_ATTN_DC(kFP16, true)
+FA_EXTERN_ATTN(kE4M3, 128, false, false)
+FA_EXTERN_ATTN(kE4M3, 128, true, false)
+FA_EXTERN_ATTN(kE4M3, 256, false, false)
+FA_EXTERN_ATTN(kE4M3, 256, true, false)
+#undef FA_EXTERN_ATTN_DC
+#undef FA_EXTERN_ATTN
+}  // namespace fa
+
 
 namespace {
 
@@ -194,6 +210,60 @@ int device_sm_count(int dev) {
 
 }  // namespace
 
+namespace fa {
+fa_status internal_prepare_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                               int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                               int dtype, const float* q_descale, const float* k_descale, const float* v_descale,
+                               cudaStream_t stream, AttnLaunch* out, bool* empty) {
+  const bool fp8 = (dtype == kDtypeE4M3);
+  if (!fp8 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, empty);
+  if (st != FA_OK || *empty) return st;
+  if (fp8) {
+    if (d == 64) return FA_ERR_UNSUPPORTED;  // FP8 rows must span the 128-byte swizzle
+    if (!q_descale || !k_descale || !v_descale) return FA_ERR_INVALID_ARG;
+    if (((uintptr_t)k_descale & 3u) || ((uintptr_t)v_descale & 3u) || ((uintptr_t)q_descale & 3u))
+      return FA_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  AttnLaunch& L = *out;
+  std::memset(&L, 0, sizeof(L));
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : (dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  const int es = fp8 ? 1 : 2;
+  if ((st = encode_map(&L.q, q, dt, es, B * Hq, Nq, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.k, k, dt, es, B * Hkv, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.v, v, dt, es, B * Hkv, Nk, d)) != FA_OK) return st;
+  L.prm.o = o;
+  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  L.prm.lse = lse;
+  L.prm.q_ds = q_descale;
+  L.prm.k_ds = k_descale;
+  L.prm.v_ds = v_descale;
+  L.prm.err = err;
+  L.prm.N = (int)Nq;
+  L.prm.Nk = (int)Nk;
+  L.prm.Hq = (int)Hq;
+  L.prm.Hkv = (int)Hkv;
+  L.prm.nblk = (int)((Nq + 127) / 128);
+  L.prm.nblk_k = (int)((Nk + 127) / 128);
+  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  L.BH = (int)(B * Hq);
+  L.prm.BH = L.BH;
+  L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
+  L.prm.q_period = (int)Nq;
+  L.prm.splits = 1;
+  L.prm.split_tiles = (int)((Nk + 127) / 128);
+  L.stream = stream;
+  return FA_OK;
+}
+}  // namespace fa
+
 extern "C" {
 
 fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
@@ -271,40 +341,11 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t Hq,
                      int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, int dtype,
                      cudaStream_t stream) {
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  bool empty = false;
-  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, &empty);
-  if (st != FA_OK || empty) return st;
-  int dev = 0;
-  int* err = nullptr;
-  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
-
   fa::AttnLaunch L;
-  std::memset(&L, 0, sizeof(L));
-  const CUtensorMapDataType dt =
-      dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((st = encode_map(&L.q, q, dt, 2, B * Hq, Nq, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.k, k, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.v, v, dt, 2, B * Hkv, Nk, d)) != FA_OK) return st;
-  L.prm.o = o;
-  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
-  L.prm.lse = lse;
-  L.prm.err = err;
-  L.prm.N = (int)Nq;
-  L.prm.Nk = (int)Nk;
-  L.prm.Hq = (int)Hq;
-  L.prm.Hkv = (int)Hkv;
-  L.prm.nblk = (int)((Nq + 127) / 128);
-  L.prm.nblk_k = (int)((Nk + 127) / 128);
-  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
-  L.BH = (int)(B * Hq);
-  L.prm.BH = L.BH;
-  L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
-  L.prm.q_period = (int)Nq;
-  L.prm.splits = 1;
-  L.prm.split_tiles = (int)((Nk + 127) / 128);
-  L.stream = stream;
+  bool empty = false;
+  const fa_status st = fa::internal_prepare_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, dtype,
+                                                nullptr, nullptr, nullptr, stream, &L, &empty);
+  if (st != FA_OK || empty) return st;
   return dtype == FA_DTYPE_BF16 ? dispatch<fa::kBF16>(L, d, causal) : dispatch<fa::kFP16>(L, d, causal);
 }
 
@@ -443,44 +484,11 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
                          int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
                          const float* q_descale, const float* k_descale, const float* v_descale,
                          cudaStream_t stream) {
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  bool empty = false;
-  fa_status st = check_common(q8, k8, v8, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, &empty);
-  if (st != FA_OK || empty) return st;
-  if (d == 64) return FA_ERR_UNSUPPORTED;  // FP8 rows must span the 128-byte swizzle
-  if (!q_descale || !k_descale || !v_descale) return FA_ERR_INVALID_ARG;
-  if (((uintptr_t)k_descale & 3u) || ((uintptr_t)v_descale & 3u) || ((uintptr_t)q_descale & 3u))
-    return FA_ERR_INVALID_ARG;
-  int dev = 0;
-  int* err = nullptr;
-  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
-
   fa::AttnLaunch L;
-  std::memset(&L, 0, sizeof(L));
-  if ((st = encode_map(&L.q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hq, Nq, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.k, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
-  if ((st = encode_map(&L.v, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B * Hkv, Nk, d)) != FA_OK) return st;
-  L.prm.o = o;
-  L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
-  L.prm.lse = lse;
-  L.prm.q_ds = q_descale;
-  L.prm.k_ds = k_descale;
-  L.prm.v_ds = v_descale;
-  L.prm.err = err;
-  L.prm.N = (int)Nq;
-  L.prm.Nk = (int)Nk;
-  L.prm.Hq = (int)Hq;
-  L.prm.Hkv = (int)Hkv;
-  L.prm.nblk = (int)((Nq + 127) / 128);
-  L.prm.nblk_k = (int)((Nk + 127) / 128);
-  L.prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
-  L.BH = (int)(B * Hq);
-  L.prm.BH = L.BH;
-  L.prm.drop_pos = (g_inject.exchange(0) & 1) ? 3 : -1;
-  L.prm.q_period = (int)Nq;
-  L.prm.splits = 1;
-  L.prm.split_tiles = (int)((Nk + 127) / 128);
-  L.stream = stream;
+  bool empty = false;
+  const fa_status st = fa::internal_prepare_fwd(q8, k8, v8, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale,
+                                                fa::kDtypeE4M3, q_descale, k_descale, v_descale, stream, &L, &empty);
+  if (st != FA_OK || empty) return st;
   return dispatch<fa::kE4M3>(L, d, causal);
 }
 

@@ -44,6 +44,7 @@
 
 #include <type_traits>
 
+#include "fa.h"
 #include "ptx.cuh"
 
 namespace fa {
@@ -54,7 +55,18 @@ constexpr int kBM = 128;  // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kSmemLimit = 232448;
 
-template <int ELEM, int D, bool CAUSAL>
+// Variants (compile-time bits; 0 is the kernel the library ships).  Each
+// bit turns one design choice back into a simpler form, or tries an
+// alternative, for ablation builds that time what the choice is worth.
+enum : int {
+  kVarSplitSoftmax = 1,    // two softmax warpgroups per Q tile, 64 key columns each (measured slower)
+  kVarEagerRescale = 2,    // rescale O whenever a row maximum rises (no lazy threshold)
+  kVarWholeP = 4,          // hand P to the MMA warp in one piece instead of two halves
+  kVarOneTile = 8,         // one Q tile per CTA (S double-buffered) also for d <= 128
+  kVarNoSteal = 16,        // no work stealing: every CTA runs only the unit it was launched with
+};
+
+template <int ELEM, int D, bool CAUSAL, int VAR = 0>
 struct AttnCfg {
   static constexpr int ES = (ELEM == kE4M3) ? 1 : 2;           // bytes per element
   static constexpr int MMA_KIND = (ELEM == kE4M3) ? 1 : 0;     // kind::f16 or kind::f8f6f4
@@ -63,14 +75,20 @@ struct AttnCfg {
   static constexpr int CH_ELEMS = 128 / ES;                    // elements per 128-byte chunk
   static constexpr int NCH = ROW_BYTES / 128;                  // chunks per row
   static constexpr int CHUNK_BYTES = 128 * 128;                // 128 rows x 128 bytes
-  static constexpr int NQT = (D <= 128) ? 2 : 1;               // Q tiles per CTA
+  static constexpr int NQT = (D <= 128 && !(VAR & kVarOneTile)) ? 2 : 1;  // Q tiles per CTA
+  // Softmax warpgroups per Q tile: with two, each thread owns 64 of a row's
+  // 128 key columns and the two halves of a row exchange their maxima
+  // through shared memory (double-buffered on the tile count).
+  static constexpr int CSPLIT = (NQT == 2 && (VAR & kVarSplitSoftmax)) ? 2 : 1;
+  static constexpr int SCOLS = kBN / CSPLIT;                   // key columns per softmax thread
+  static constexpr int XCH_BYTES = (CSPLIT == 2) ? 2 * 2 * 2 * 128 * 4 : 0;  // [parity][tile][part][row]
   static constexpr int TILE_BYTES = kBN * ROW_BYTES;           // one K or V tile
   static constexpr int SLOT_BYTES = TILE_BYTES < 32768 ? TILE_BYTES : 32768;
   static constexpr int SPT = TILE_BYTES / SLOT_BYTES;          // ring slots per tile
   static constexpr int SLOT_CH = SLOT_BYTES / CHUNK_BYTES;     // chunks per slot
   static constexpr int SLOT_D = SLOT_CH * CH_ELEMS;            // head-dim columns per slot
   static constexpr int Q_BYTES = NQT * kBM * ROW_BYTES;
-  static constexpr int NS_MAX = (kSmemLimit - 1024 - 1024 - Q_BYTES) / SLOT_BYTES;
+  static constexpr int NS_MAX = (kSmemLimit - 1024 - 1024 - XCH_BYTES - Q_BYTES) / SLOT_BYTES;
   static constexpr int NS = NS_MAX > 8 ? 8 : NS_MAX;           // ring depth
   static_assert(NS >= 2 * SPT, "ring too shallow");
   static constexpr int KSTEP = 32 / ES;                        // MMA K per instruction (32 bytes)
@@ -78,11 +96,16 @@ struct AttnCfg {
   static constexpr int KSTEPS_PV = kBN / KSTEP;
   static_assert(KSTEPS_PV % 2 == 0, "P is handed over in two halves of the key tile");
   static constexpr int P_COLS = kBN * ES / 4;                  // TMEM columns of P per row
+  // P of key half h starts at column h * P_HALF_OFF of the S/P buffer: right
+  // after the first half normally; with the split softmax at column 64, the
+  // first column of the S columns its own warps read, so that no part's P
+  // lands on S columns the other part has still to read.
+  static constexpr int P_HALF_OFF = (CSPLIT == 2) ? 64 : P_COLS / 2;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0;                        // S/P buffers at 0 and 128
   static constexpr uint32_t O_COL0 = 256;                      // O accumulators from 256
   static_assert(O_COL0 + NQT * D <= TMEM_COLS, "TMEM budget");
-  static constexpr int SOFTMAX_WARPS = 4 * NQT;
+  static constexpr int SOFTMAX_WARPS = 4 * NQT * CSPLIT;
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
   static constexpr int LOAD_WARP = SOFTMAX_WARPS + 1;
   // Two Q tiles: a third, control warpgroup (MMA warp, load warp, two idle
@@ -93,15 +116,17 @@ struct AttnCfg {
   // kernels' warp-wide MMA loop spills below ~100 registers and their
   // softmax fits in 200 (measured fastest of 72/216, 88/208, 104/200); the
   // FP8 softmax is the tighter side and keeps 216.
-  static constexpr bool REALLOC = (NQT == 2);
+  static constexpr bool REALLOC = (NQT == 2 && CSPLIT == 1);
   static constexpr int THREADS = REALLOC ? 32 * (SOFTMAX_WARPS + 4) : 32 * (SOFTMAX_WARPS + 2);
-  static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = (ELEM == kE4M3) ? 72 : 104;
-  static constexpr int SOFTMAX_REGS = (ELEM == kE4M3) ? 216 : 200;
+  // Split softmax: 18 warps (16 softmax, MMA, load), up to 5 per
+  // sub-partition, so at most 96 registers each, without reallocation.
+  static constexpr int LAUNCH_REGS = (CSPLIT == 2) ? 96 : 168;
+  static constexpr int CTRL_REGS = (CSPLIT == 2) ? 96 : (ELEM == kE4M3) ? 72 : 104;
+  static constexpr int SOFTMAX_REGS = (CSPLIT == 2) ? 96 : (ELEM == kE4M3) ? 216 : 200;
   static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max
-  static constexpr float TAU = (ELEM == kE4M3) ? 2.0f : 8.0f;
+  static constexpr float TAU = (VAR & kVarEagerRescale) ? 0.0f : (ELEM == kE4M3) ? 2.0f : 8.0f;
   // FP8: P is stored as p * 2^6 * (s_Vj / max_j s_Vj) <= 2^6 * 2^TAU = 256,
   // inside the E4M3 range (448)
   static constexpr float P8_SCALE = 64.0f;
@@ -112,7 +137,8 @@ struct AttnCfg {
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = Q_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + NS * SLOT_BYTES;
+  static constexpr int OFF_XCH = OFF_RING + NS * SLOT_BYTES;
+  static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 1024 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
 };
@@ -195,11 +221,11 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int nkv, int off) {
 // q_period) and, when prm.splits > 1, units cover runs of key tiles and
 // write fp32 partial results.  Without it every row is its own position and
 // a unit covers the whole key range.
-template <int ELEM, int D, bool CAUSAL, bool SPLIT>
-__global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
+template <int ELEM, int D, bool CAUSAL, bool SPLIT, int VAR = 0>
+__global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams prm) {
-  using C = AttnCfg<ELEM, D, CAUSAL>;
+  using C = AttnCfg<ELEM, D, CAUSAL, VAR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars<C::NS>* bars = reinterpret_cast<Bars<C::NS>*>(smem + C::OFF_BAR);
@@ -433,7 +459,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         if (!ok) break;
         // every load of this unit is issued: claim the next unit
         int nu = -1;
-        if (more) {
+        if (more && !(VAR & kVarNoSteal)) {
           mbar_arrive_expect_tx(&bars->clc_bar, 16);
           clc_try_cancel(bars->clc_resp, &bars->clc_bar);
           if (!mbar_wait(&bars->clc_bar, (uint32_t)(n_req & 1), abort_flag, prm.err)) { ok = false; break; }
@@ -539,7 +565,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           for (int ks = h * (C::KSTEPS_PV / 2); ks < (h + 1) * (C::KSTEPS_PV / 2); ++ks) {
             // keys ks*KSTEP .. +KSTEP-1 are KSTEP/8 groups of 8 rows (1024 B each)
             const uint64_t b = v0 + (uint64_t)((ks * (C::KSTEP / 8) * 1024) >> 4);
-            mma_ts_elect<C::MMA_KIND>(d_tmem, p_tmem + ks * 8, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+            const uint32_t p_col = (uint32_t)(h * C::P_HALF_OFF + (ks - h * (C::KSTEPS_PV / 2)) * 8);
+            mma_ts_elect<C::MMA_KIND>(d_tmem, p_tmem + p_col, b, C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
           }
         }
       };
@@ -664,22 +691,39 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
   } else {
     // --------------------------------------------------------- softmax --
     if constexpr (C::REALLOC) regs_inc<C::SOFTMAX_REGS>();
-    const int t = warp / 4;                 // Q tile of this warpgroup
-    const int wq = warp % 4;                // TMEM lane quarter
-    const int r_in = wq * 32 + lane;        // row within the tile
+    constexpr int NCOL = C::SCOLS;                  // key columns of a tile per thread
+    const int t = warp / (4 * C::CSPLIT);           // Q tile of this warp
+    const int part = (warp / 4) % C::CSPLIT;        // which NCOL key columns (split softmax)
+    const int cbase = part * NCOL;                  // first of them within a key tile
+    const int wq = warp % 4;                        // TMEM lane quarter
+    const int r_in = wq * 32 + lane;                // row within the tile
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    // Split softmax: the two warps holding the two column parts of the same
+    // 32 rows meet at their own named barrier (1..8), always through the
+    // predicate-AND form, so that a warp that gave up never leaves its
+    // partner waiting; row maxima and row sums cross through shared memory
+    // (slot parity alternates with the tile count, so a slot is rewritten
+    // only after the partner has passed the next barrier).
+    const uint32_t pair_bar = 1u + (uint32_t)(t * 4 + wq);
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+    auto xslot = [&](int parity, int prt) -> float* { return xch + ((parity * 2 + t) * 2 + prt) * 128 + r_in; };
     const bool neg = prm.scale_log2 < 0.0f;
     const float mask_val = neg ? INFINITY : -INFINITY;
     int sc = 0;               // two Q tiles: S handshakes consumed (this tile)
     int g = 0;                // one Q tile: running iteration count
     int oc = 0;               // units finished by this tile (o_full phases)
     int pv_seen = 0;          // one Q tile: PV completions consumed (global iteration order)
+    int xc = 0;               // split softmax: exchanges made (slot parity)
     bool ok = true;
 
     for (int rr = 0; ok; ++rr) {
       bool okr = true;
       const Unit w = fetch_unit(rr, lane == 0, okr);
-      if (!__all_sync(0xffffffffu, okr)) { ok = false; break; }
+      okr = __all_sync(0xffffffffu, okr);
+      // the two column parts of a row agree on going on, so that neither
+      // waits at their barrier for a partner that has left
+      if constexpr (C::CSPLIT == 2) okr = bar_and(pair_bar, 64, okr);
+      if (!okr) { ok = false; break; }
       if (w.bh < 0) break;
       do {  // one unit (skipped when this tile lies beyond N)
       if (!(t == 0 ? w.active[0] : w.active[1])) break;
@@ -687,21 +731,25 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       const int q0 = w.q_base + t * kBM;
       const int row = q0 + r_in;
       const int Jn = (t == 0) ? w.Jt[0] : w.Jt[1];
+      // output columns of this thread: all D, or its part's half
+      constexpr int OCOLS = D / C::CSPLIT;
+      const int ocol0 = part * OCOLS;
       if (Jn == 0) {
         // no row of this tile sees a key of this unit (causal, Nq > Nk, or a
         // key split beyond the tile's last key): O = 0, LSE = -inf
         if (row < N) {
           if (SPLIT && S > 1) {
             const size_t pr = ((size_t)w.split * prm.BH + bh) * N + row;
-            float4* dst = reinterpret_cast<float4*>(prm.o_part + pr * D);
+            float4* dst = reinterpret_cast<float4*>(prm.o_part + pr * D + ocol0);
 #pragma unroll 1
-            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            prm.lse_part[pr] = -INFINITY;
+            for (int i = 0; i < OCOLS / 4; ++i) dst[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (part == 0) prm.lse_part[pr] = -INFINITY;
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + row) * D * 2);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(prm.o) +
+                                                  (((size_t)bh * N + row) * D + ocol0) * 2);
 #pragma unroll 1
-            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-            prm.lse[(size_t)bh * N + row] = -INFINITY;
+            for (int i = 0; i < OCOLS / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (part == 0) prm.lse[(size_t)bh * N + row] = -INFINITY;
           }
         }
         break;
@@ -719,7 +767,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         last_col = min(Nk - 1, row + koff);
       }
       float m_run = -INFINITY;  // reference maximum, log2 units
-      float l_run = 0.0f;
+      float l_run = 0.0f;       // row sum over this thread's key columns
       float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
       const int bh_blk = bh * prm.nblk;          // Q descale blocks of this head
       const int kv_blk = w.kvh * prm.nblk_k;     // K/V descale blocks
@@ -766,58 +814,199 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         return true;
       };
 
+
       for (int j = 0; j < Jn && ok; ++j) {
         const int gj = g + j;
         const int buf = (C::NQT == 2) ? t : (gj & 1);
         const uint32_t ph = (C::NQT == 2) ? (uint32_t)(sc & 1) : (uint32_t)((gj >> 1) & 1);
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], ph, abort_flag, prm.err));
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], ph, abort_flag, prm.err));
         ++sc;
-        if (!ok) break;
-        tc_fence_after();
+        if constexpr (C::CSPLIT == 2) {
+          // ---- split softmax: this thread's 64 key columns of the tile, read
+          // from TMEM twice (once for the row maximum, once for P), 32 at a
+          // time, so that few registers are live
+          const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
+          float cj = prm.scale_log2;   // scale of this tile (log2 units)
+          const int col0 = (w.tb + j) * kBN;
+          const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > first_last);
+          const int lim = last_col - col0 - cbase;   // this part's columns c > lim are masked
+          float mx = mask_val;
+          if (okw) {
+            tc_fence_after();
+            uint32_t ua[32], ub[32];
+            tmem_ld32(s_addr + cbase, ua);
+            tmem_ld32(s_addr + cbase + 32, ub);
+            tmem_wait_ld();
+            if constexpr (ELEM == kE4M3) {
+              cj *= f_k;
+              if (j + 1 < Jn) {
+                kd_next = prm.k_ds[kv_blk + w.tb + j + 1];
+                vd_next = prm.v_ds[kv_blk + w.tb + j + 1];
+              }
+            }
+            auto sv = [&](int c) -> float {
+              const float x = __uint_as_float(c < 32 ? ua[c] : ub[c - 32]);
+              return (need_mask && c > lim) ? mask_val : x;
+            };
+            // row max (min for a negative scale): eight chains of 3-input max
+            float r8[8];
+            if (!neg) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) r8[i] = fmaxf(sv(i), sv(8 + i));
+#pragma unroll
+              for (int c = 16; c < 64; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r8[i] = max3f(r8[i], sv(c + i), sv(c + 8 + i));
+              mx = max3f(max3f(r8[0], r8[1], r8[2]), max3f(r8[3], r8[4], r8[5]), fmaxf(r8[6], r8[7]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) r8[i] = fminf(sv(i), sv(8 + i));
+#pragma unroll
+              for (int c = 16; c < 64; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r8[i] = min3f(r8[i], sv(c + i), sv(c + 8 + i));
+              mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
+            }
+          }
+          // the whole row's maximum: exchange with the other column part
+          if (okw) *xslot(xc & 1, part) = mx;
+          if (!bar_and(pair_bar, 64, okw)) { ok = false; break; }
+          {
+            const float other = *xslot(xc & 1, part ^ 1);
+            mx = neg ? fminf(mx, other) : fmaxf(mx, other);
+          }
+          ++xc;
+          // a row whose keys in this tile are all masked keeps -inf (for a
+          // zero scale mx * cj would be inf * 0 = NaN)
+          const float mx2 = (mx == mask_val) ? -INFINITY : mx * cj;
+          float alpha = 1.0f;
+          const bool move = (mx2 > m_run + C::TAU) || (m_run == -INFINITY && mx2 != -INFINITY);
+          if (move) {
+            alpha = ex2(m_run - mx2);  // 0 on the first tile
+            m_run = mx2;
+          }
+          l_run *= alpha;
+          // rescale this part's half of O when any row of the warp moved
+          if (j > 0 && __any_sync(0xffffffffu, move)) {
+            const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D + ocol0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < OCOLS; c0 += 32) {
+              uint32_t u[32];
+              tmem_ld32(o_addr + c0, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+              tmem_st32(o_addr + c0, u);
+            }
+            tmem_wait_st();
+          }
+          // P = 2^(s*cj - m), 32 keys at a time, into this part's P columns
+          // (which start at the first S column it reads, so a chunk of P only
+          // overwrites S this thread has already read)
+          const float2 cj2 = make_float2(cj, cj);
+          const float lpv = f_lpv, inv_pv = f_inv;
+          const float2 nm2 = make_float2(lpv - m_run, lpv - m_run);
+          float2 acc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+          const uint32_t p_addr = s_addr + (uint32_t)(part * C::P_HALF_OFF);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t u[32];
+            tmem_ld32(s_addr + cbase + 32 * q, u);
+            tmem_wait_ld();
+            auto p_pair = [&](int c) -> float2 {   // c: column within this chunk
+              const float2 x = fma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), cj2, nm2);
+              float2 p = make_float2(ex2(x.x), ex2(x.y));
+              if (need_mask) {
+                p.x = (32 * q + c > lim) ? 0.0f : p.x;
+                p.y = (32 * q + c + 1 > lim) ? 0.0f : p.y;
+              }
+              return p;
+            };
+            if constexpr (ELEM == kE4M3) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float2 a = p_pair(4 * i), b = p_pair(4 * i + 2);
+                acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
+                acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
+                pk[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+              }
+              tmem_st8(p_addr + q * 8, pk);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float2 a = p_pair(h * 16 + 2 * i);
+                  acc[i & 3] = add2(acc[i & 3], a);
+                  pk[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
+                }
+                tmem_st8(p_addr + q * 16 + h * 8, pk);
+              }
+            }
+          }
+          {
+            const float2 tt = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+            l_run += (ELEM == kE4M3) ? (tt.x + tt.y) * inv_pv : (tt.x + tt.y);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          // this part's keys are half `part` of the tile
+          mbar_arrive(&bars->p_full[buf][part]);
+          if constexpr (ELEM == kE4M3) {
+            if (j + 1 < Jn) fp8_factors(kd_next, vd_next);
+          }
+        } else {
+        if (!okw) { ok = false; break; }
         if constexpr (C::NQT == 1) {
+          tc_fence_after();
           // PV(gj-2) was issued before S(gj), so it has completed: consume
           // its o_ready phase to keep at most one pending per buffer
           if (gj >= 2 && !consume_o(gj - 2)) { ok = false; break; }
         }
         const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
-        float s[kBN];
-        {
-          uint32_t u[32];
-#pragma unroll
-          for (int c4 = 0; c4 < kBN / 32; ++c4) {
-            tmem_ld32(s_addr + c4 * 32, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
-          }
-          tmem_wait_ld();
-        }
-        // scale of this tile (log2 units)
-        float cj = prm.scale_log2;
-        if constexpr (ELEM == kE4M3) {
-          cj *= f_k;
-          if (j + 1 < Jn) {
-            kd_next = prm.k_ds[kv_blk + w.tb + j + 1];
-            vd_next = prm.v_ds[kv_blk + w.tb + j + 1];
-          }
-        }
+        float s[NCOL];
+        float cj = prm.scale_log2;   // scale of this tile (log2 units)
         const int col0 = (w.tb + j) * kBN;
         const bool need_mask = (col0 + kBN > Nk) || (CAUSAL && col0 + kBN - 1 > first_last);
-        if (need_mask) {
-          const int lim = last_col - col0;
+        float mx = mask_val;
+        if (okw) {
+          if constexpr (C::NQT == 2) tc_fence_after();
+          {
+            uint32_t u[32];
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            s[c] = (c > lim) ? mask_val : s[c];
+            for (int c4 = 0; c4 < NCOL / 32; ++c4) {
+              tmem_ld32(s_addr + cbase + c4 * 32, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
+            }
+            tmem_wait_ld();
           }
-        }
-        // row max (min for a negative scale): eight chains of 3-input max
-        float mx;
-        {
+          if constexpr (ELEM == kE4M3) {
+            cj *= f_k;
+            if (j + 1 < Jn) {
+              kd_next = prm.k_ds[kv_blk + w.tb + j + 1];
+              vd_next = prm.v_ds[kv_blk + w.tb + j + 1];
+            }
+          }
+          if (need_mask) {
+            const int lim = last_col - col0 - cbase;
+#pragma unroll
+            for (int c = 0; c < NCOL; ++c) {
+              s[c] = (c > lim) ? mask_val : s[c];
+            }
+          }
+          // row max (min for a negative scale) of this thread's columns:
+          // eight chains of 3-input max
           float r8[8];
           if (!neg) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) r8[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-            for (int c = 16; c < kBN; c += 16)
+            for (int c = 16; c < NCOL; c += 16)
 #pragma unroll
               for (int i = 0; i < 8; ++i) r8[i] = max3f(r8[i], s[c + i], s[c + 8 + i]);
             mx = max3f(max3f(r8[0], r8[1], r8[2]), max3f(r8[3], r8[4], r8[5]), fmaxf(r8[6], r8[7]));
@@ -825,7 +1014,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) r8[i] = fminf(s[i], s[8 + i]);
 #pragma unroll
-            for (int c = 16; c < kBN; c += 16)
+            for (int c = 16; c < NCOL; c += 16)
 #pragma unroll
               for (int i = 0; i < 8; ++i) r8[i] = min3f(r8[i], s[c + i], s[c + 8 + i]);
             mx = min3f(min3f(r8[0], r8[1], r8[2]), min3f(r8[3], r8[4], r8[5]), fminf(r8[6], r8[7]));
@@ -842,16 +1031,17 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           m_run = mx2;
         }
         l_run *= alpha;
-        // rescale O when any row of the warp moved (never on the first tile)
+        // rescale O (this thread's output columns) when any row of the warp
+        // moved (never on the first tile)
         if (j > 0 && __any_sync(0xffffffffu, move)) {
           if constexpr (C::NQT == 1) {
             // O holds PV(gj-1): wait for it
             if (!consume_o(gj - 1)) { ok = false; break; }
             tc_fence_after();
           }
-          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D + ocol0;
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < OCOLS; c0 += 32) {
             uint32_t u[32];
             tmem_ld32(o_addr + c0, u);
             tmem_wait_ld();
@@ -862,10 +1052,10 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           tmem_wait_st();
         }
         // P = 2^(s*cj - m) and the row sum (four packed pairs of chains),
-        // packed and written back over S a quarter at a time, so the stores
-        // overlap the rest and few registers are live at once.  Masked tiles
-        // (causal diagonal, ragged tail) zero the masked p explicitly; every
-        // other tile takes the select-free loop.
+        // packed and written back over S a quarter (32 keys) at a time, so
+        // the stores overlap the rest and few registers are live at once.
+        // Masked tiles (causal diagonal, ragged tail) zero the masked p
+        // explicitly; every other tile takes the select-free loop.
         const float2 cj2 = make_float2(cj, cj);
         // FP8: the V-block factor of p~ is folded into the exponent
         // (2^(x - m + f_lpv)); the row sum is rescaled once per tile (f_inv)
@@ -883,10 +1073,14 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
           }
           return p;
         };
+        // quarters (32 keys) of the tile held by this thread; P of quarter
+        // Q sits in TMEM columns Q * 32 * ES / 4 .. of the S/P buffer
+        constexpr int NQ = NCOL / 32;
         auto emit = [&](bool masked_tile) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (q == 2) {
+          for (int q = 0; q < NQ; ++q) {
+            const int qq = part * NQ + q;   // quarter within the tile
+            if (C::CSPLIT == 1 && !(VAR & kVarWholeP) && q == 2) {
               // keys 0..63 of P are in TMEM: let their MMAs start
               tmem_wait_st();
               tc_fence_before();
@@ -902,7 +1096,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
                 acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
                 u[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
               }
-              tmem_st8(s_addr + q * 8, u);
+              tmem_st8(s_addr + qq * 8, u);
             } else {
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -914,7 +1108,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
                   acc[i & 3] = add2(acc[i & 3], a);
                   u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
                 }
-                tmem_st8(s_addr + q * 16 + h * 8, u);
+                tmem_st8(s_addr + qq * 16 + h * 8, u);
               }
             }
           }
@@ -922,34 +1116,44 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
         if (need_mask) emit(true);
         else emit(false);
         {
-          const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-          l_run += (ELEM == kE4M3) ? (t.x + t.y) * inv_pv : (t.x + t.y);
+          const float2 tt = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+          l_run += (ELEM == kE4M3) ? (tt.x + tt.y) * inv_pv : (tt.x + tt.y);
         }
         tmem_wait_st();
         tc_fence_before();
+        if (VAR & kVarWholeP) mbar_arrive(&bars->p_full[buf][0]);
         mbar_arrive(&bars->p_full[buf][1]);
         if constexpr (ELEM == kE4M3) {
           if (j + 1 < Jn) fp8_factors(kd_next, vd_next);
+        }
         }
       }
 
       // ---------------------------------------------------------- epilogue --
       if (ok) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], (uint32_t)(oc & 1), abort_flag, prm.err));
+        bool oke = __all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], (uint32_t)(oc & 1), abort_flag, prm.err));
         ++oc;
+        if constexpr (C::CSPLIT == 2) {
+          // the whole row's sum: exchange with the other column part
+          if (oke) *xslot(xc & 1, part) = l_run;
+          oke = bar_and(pair_bar, 64, oke);
+          if (oke) l_run += *xslot(xc & 1, part ^ 1);
+          ++xc;
+        }
+        ok = oke;
         if (ok) {
           tc_fence_after();
           const float inv_l = (l_run > 0.0f) ? (1.0f / l_run) : 0.0f;
           const float f = inv_l * v_mult;
-          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D;
+          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D + ocol0;
           const bool store = row < N;
           if (SPLIT && S > 1) {
             // split-KV partial: O normalised over this split's keys, fp32,
             // and the split's LSE (a row without visible keys: 0, -inf)
             const size_t pr = ((size_t)w.split * prm.BH + bh) * N + (size_t)(store ? row : 0);
-            float* prow = prm.o_part + pr * D;
+            float* prow = prm.o_part + pr * D + ocol0;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < OCOLS; c0 += 32) {
               uint32_t u[32];
               tmem_ld32(o_addr + c0, u);
               tmem_wait_ld();
@@ -960,11 +1164,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
                 for (int i = 0; i < 4; ++i) st_global_v8(prow + c0 + 8 * i, u + 8 * i);
               }
             }
-            if (store) prm.lse_part[pr] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
+            if (store && part == 0) prm.lse_part[pr] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
           } else {
-          uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + ((size_t)bh * N + (size_t)(store ? row : 0)) * D * 2;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(prm.o) + (((size_t)bh * N + (size_t)(store ? row : 0)) * D + ocol0) * 2;
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < OCOLS; c0 += 32) {
             uint32_t u[32];
             tmem_ld32(o_addr + c0, u);
             tmem_wait_ld();
@@ -987,7 +1191,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
               }
             }
           }
-          if (store) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
+          if (store && part == 0) prm.lse[(size_t)bh * N + row] = (m_run + lg2(l_run)) * 0.69314718055994530942f;
           }
         }
       }
@@ -995,7 +1199,6 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL>::THREADS, 1)
       } while (0);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == C::MMA_WARP) {
@@ -1017,10 +1220,21 @@ struct AttnLaunch {
   cudaStream_t stream;
 };
 
-template <int ELEM, int D, bool CAUSAL, bool SPLIT>
+// Element-type code for FP8 inputs in internal_prepare_fwd (the C ABI's
+// dtype codes cover bf16 and fp16).
+constexpr int kDtypeE4M3 = 100;
+
+// Checks the arguments of a forward call, encodes the tensor maps and fills
+// the launch (defined in api.cu).  *empty: nothing to do (FA_OK).
+fa_status internal_prepare_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                               int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                               int dtype, const float* q_descale, const float* k_descale, const float* v_descale,
+                               cudaStream_t stream, AttnLaunch* out, bool* empty);
+
+template <int ELEM, int D, bool CAUSAL, bool SPLIT, int VAR = 0>
 cudaError_t launch_attn(const AttnLaunch& L) {
-  using C = AttnCfg<ELEM, D, CAUSAL>;
-  auto kern = attn_fwd_kernel<ELEM, D, CAUSAL, SPLIT>;
+  using C = AttnCfg<ELEM, D, CAUSAL, VAR>;
+  auto kern = attn_fwd_kernel<ELEM, D, CAUSAL, SPLIT, VAR>;
   static bool attr_done[64] = {};  // the attribute is per function and device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -1,0 +1,47 @@
+/*
+ * fa_ablate.h -- ablation entry point of libfa_ablate.so (a separate
+ * library built beside libfa.so, which it links against; not part of the
+ * product API).
+ *
+ * The attention forward of fa_fwd / fa_fwd_fp8 (B, H, N, d = 128, Hq = Hkv,
+ * Nq = Nk) with one design choice of the kernel switched, so that what each
+ * choice is worth can be timed from the committed tree.  The pages motivate
+ * the comparison: "FlashAttention-3: async pipelines on Hopper", section
+ * "second overlap" (two consumer groups alternating softmax and GEMMs, the
+ * ping-pong measured at 570 -> 620-640 TFLOPS on H100) and section "third
+ * overlap" (the next Q K^T during the softmax).  Variant codes (bits):
+ *   0   the shipped kernel (fa_fwd / fa_fwd_fp8 of libfa.so)
+ *   1   split softmax: two softmax warpgroups per Q tile, 64 key columns each
+ *   2   eager rescale: O rescaled whenever a row maximum rises (no lazy threshold)
+ *   4   whole P: P handed to the MMA warp in one piece, not in two halves
+ *   8   one Q tile per CTA with S double-buffered (no two-tile alternation)
+ *   16  no work stealing: each CTA runs only the unit it was launched with
+ * Built instances: bf16 non-causal and FP8 non-causal with every code above;
+ * bf16 causal with 0, 1, 8 and 16.
+ *   variant      one of the codes above
+ *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
+ *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8
+ *   other arguments as fa_fwd / fa_fwd_fp8 (device pointers, [B, H, N, d]
+ *   contiguous, o bf16, lse fp32 [B, H, N]); d must be 128.
+ * Errors: FA_ERR_UNSUPPORTED for a variant / type / causal combination that
+ * was not built or d != 128; otherwise as fa_fwd.
+ */
+#ifndef FA_ABLATE_H
+#define FA_ABLATE_H
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+fa_status fa_ablate_fwd(int variant, int fp8, const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                        const float* q_descale, const float* k_descale, const float* v_descale,
+                        cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_ABLATE_H */

@@ -165,3 +165,14 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         fa.lib()
+
+
+def test_ablation_library_exports_its_header():
+    from exact_attention_forward_09_gb300 import build
+    build.build()
+    lib = ctypes.CDLL(build.LIB_ABLATE)
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "fa_ablate.h")).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+    assert names == ["fa_ablate_fwd"]
+    for name in names:
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)

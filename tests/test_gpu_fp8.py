@@ -215,3 +215,51 @@ def test_fwd_fp8_with_rope(fa, layout):
                                      causal=causal, scale=scale)
         rmse = float(np.sqrt(((o.float().cpu().numpy() - o_ex) ** 2).mean()))
         assert np.isfinite(rmse) and rmse <= FP8_O_RMSE, (causal, rmse)
+
+
+@pytest.mark.parametrize("sigma", [10.0, 100.0])
+def test_fp8_error_study(fa, sigma):
+    """The FP8 error study at the FP8 workloads (B = 16384 / N, H = 16,
+    d = 128, N in {1k, 4k, 16k}, non-causal): inputs N(0,1) plus rare
+    outliers N(0, sigma^2) (sigma = 10 is the workload's reading; 100 the
+    other reading of its notation), quantised on the GPU three ways --
+    per-tensor scale, block scales, block scales + Hadamard on Q and K --
+    then FP8 attention; O RMSE against the fp64 oracle on the unquantised
+    inputs over 64 sampled query rows of every head.  Block + Hadamard must
+    beat the per-tensor baseline (the pages report 2.6x on H100 as context,
+    not as a bar).  With FA_REPORT_DIR set, the figures are written there as
+    JSON."""
+    import json
+    import os
+    d, H = 128, 16
+    signs = gen.hadamard_signs(d, 4)
+    report = {}
+    for N in gen.FP8_N:
+        B = gen.TOTAL_TOKENS // N
+        rows = gen.sample_rows(N, 64, 8)
+        q, k, v = gen.qkv_outliers((B, H, N, d), 3, sigma=sigma)
+        o_ref, _ = oracle.attn_fwd(q, k, v, causal=False, scale=1.0 / math.sqrt(d), rows=rows)
+        qd, kd, vd = (torch.from_numpy(a).cuda() for a in (q, k, v))
+        res = {}
+        for name, rot, pt in (("per_tensor", False, True), ("block", False, False),
+                              ("block_hadamard", True, False)):
+            sg = signs if rot else None
+            q8, qs = fa.quant_fp8(qd, signs=sg, per_tensor=pt)
+            k8, ks = fa.quant_fp8(kd, signs=sg, per_tensor=pt)
+            v8, vs = fa.quant_fp8(vd, per_tensor=pt)
+            o, _ = fa.fwd_fp8(q8, k8, v8, qs, ks, vs, causal=False, scale=1.0 / math.sqrt(d))
+            fa.check_device_error()
+            og = o.float().cpu().numpy().astype(np.float64)[:, :, rows]
+            res[name] = float(math.sqrt(((og - o_ref) ** 2).mean()))
+        res["ratio_per_tensor_over_block_hadamard"] = res["per_tensor"] / res["block_hadamard"]
+        report[f"N{N}"] = res
+        assert res["block_hadamard"] < res["per_tensor"], (N, res)
+        if sigma == 10.0:
+            assert res["block_hadamard"] <= FP8_O_RMSE and res["block"] <= FP8_O_RMSE, (N, res)
+        del qd, kd, vd
+    print(f"\nFP8 error study, sigma = {sigma}: {json.dumps(report)}")
+    out = os.environ.get("FA_REPORT_DIR")
+    if out:
+        os.makedirs(out, exist_ok=True)
+        with open(os.path.join(out, f"fp8_error_study_sigma{int(sigma)}.json"), "w") as f:
+            json.dump({"sigma": sigma, "rows_per_head": 64, "rmse_vs_fp64_oracle": report}, f, indent=1)
