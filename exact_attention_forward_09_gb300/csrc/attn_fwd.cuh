@@ -167,6 +167,10 @@ struct AttnParams {
   // or Nq when the query heads of a key/value group are packed into one
   // head of g * Nq rows); causal masks use that position.
   int q_period;
+  // Causal unit order: heads are taken head_chunk at a time (chunks in
+  // head order), and within a chunk the units with the most key tiles come
+  // first (longest processing time first).  head_chunk = BH: one chunk.
+  int head_chunk;
   // Split-KV: splits > 1 divides each row's key tiles into runs of
   // split_tiles; a unit then covers one run and writes O normalised over its
   // keys (fp32) to o_part[split][bh][row][d] and its LSE to
@@ -273,8 +277,14 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       single = x % 2;
     }
     if constexpr (CAUSAL) {
-      group = n_groups - 1 - v / prm.BH;
-      w.bh = v % prm.BH;
+      // heaviest groups first within chunks of head_chunk heads (chunks in
+      // head order), so that the K/V of the heads in flight stay in L2
+      const int per_chunk = prm.head_chunk * n_groups;
+      const int c = v / per_chunk;
+      const int idx = v - c * per_chunk;
+      const int heads_here = min(prm.head_chunk, prm.BH - c * prm.head_chunk);
+      group = n_groups - 1 - idx / heads_here;
+      w.bh = c * prm.head_chunk + idx % heads_here;
     } else {
       w.bh = v / n_groups;
       group = v % n_groups;
@@ -1263,6 +1273,18 @@ cudaError_t launch_attn(const AttnLaunch& L) {
     if (rem > 0 && 2 * rem <= sms) prm.pair_units = (int)(n_groups_all - rem);
   }
   const long long units = n_groups_all + (C::NQT - 1) * (n_groups_all - prm.pair_units);
+  // Causal: chunks of heads whose K/V (read once from HBM, then re-read by
+  // every Q tile of the head from L2) take up to about half of L2 at a time;
+  // with all heads at once, long sequences re-read K/V from HBM many times.
+  prm.head_chunk = prm.BH;
+  if constexpr (CAUSAL && !SPLIT) {
+    const long long kv_head_bytes = 2LL * L.prm.Nk * C::ROW_BYTES;
+    const long long budget = 64LL << 20;
+    const int qgroup = L.prm.Hq / L.prm.Hkv;
+    long long chunk = (budget / (kv_head_bytes > 0 ? kv_head_bytes : 1)) * qgroup;
+    if (chunk < qgroup) chunk = qgroup;
+    if (chunk < prm.BH) prm.head_chunk = (int)chunk;
+  }
   if constexpr (C::REALLOC) {
     // the register split must fit what the kernel is launched with, or the
     // growing warpgroups would wait for registers that never come
