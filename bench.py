@@ -48,6 +48,7 @@ KERNEL_SOURCES = ["exact_attention_forward_09_gb300/csrc/attn_fwd.cuh",
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SHAPES = {"long": (1, 16, 65536, 128, True), "mid": (4, 16, 2048, 128, False),
           "sweep4k": (4, 16, 4096, 128, False), "sweep16k": (1, 16, 16384, 128, False),
+          "sweep8k_d64": (2, 32, 8192, 64, False), "sweep512": (32, 16, 512, 128, False),
           "fp8_1k": (16, 16, 1024, 128, False), "fp8_4k": (4, 16, 4096, 128, False),
           "fp8_16k": (1, 16, 16384, 128, False)}
 FLUSH_BYTES = 512 * 1024 * 1024
@@ -330,7 +331,7 @@ def run_fp8_point(device, flush):
     return {"workload": f"fp8_16k: B={B} H={H} N={N} d={d} non-causal, Q/K block scales + Hadamard, V block scales",
             "value": tf, "unit": "TFLOPS", "ms": ms, "peak": fp8_peak, "frac": tf / fp8_peak,
             "peak_source": f"{src} bf16 burst (cuBLAS GEMM) x 2, the nominal dense fp8:bf16 ratio",
-            "kernel": f"attn_fwd_kernel<e4m3,{d},non-causal>",
+            "kernel": f"attn_fwd_kernel<e4m3,{d},non-causal>", "traffic": load_traffic("fp8_16k"),
             "step_ms": ms_step, "step_tflops": fl / (ms_step * 1e-3) / 1e12}
 
 
@@ -476,8 +477,9 @@ def run_extra(device, flush):
 ABLATE_VARIANTS = {0: "shipped kernel", 1: "split softmax (two warpgroups per Q tile, 64 keys each)",
                    2: "eager rescale (no lazy threshold)", 4: "P handed over whole (not in two halves)",
                    8: "one Q tile per CTA, S double-buffered (no two-tile alternation)",
-                   16: "no work stealing"}
-ABLATE_BUILT = {(False, False): (0, 1, 2, 4, 8, 16), (False, True): (0, 1, 8, 16), (True, False): (0, 1, 2, 4, 8, 16)}
+                   16: "no work stealing", 32: "separate P (Q K^T of the next tile starts once S is read)"}
+ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16), (False, True, 128): (0, 1, 8, 16),
+                (True, False, 128): (0, 1, 2, 4, 8, 16), (False, False, 64): (0, 32), (False, True, 64): (0, 32)}
 
 
 def run_ablate(args, device):
@@ -499,13 +501,15 @@ def run_ablate(args, device):
     g = torch.Generator(device=device)
     g.manual_seed(13)
     out = {}
-    for name, (B, H, N, causal, fp8) in (("N16384_bf16", (1, 16, 16384, False, False)),
-                                         ("mid_bf16", (4, 16, 2048, False, False)),
-                                         ("N16384_bf16_causal", (1, 16, 16384, True, False)),
-                                         ("mid_bf16_causal", (4, 16, 2048, True, False)),
-                                         ("N16384_fp8", (1, 16, 16384, False, True)),
-                                         ("N4096_fp8", (4, 16, 4096, False, True))):
-        d = 128
+    for name, (B, H, N, d, causal, fp8) in (("N16384_bf16", (1, 16, 16384, 128, False, False)),
+                                            ("mid_bf16", (4, 16, 2048, 128, False, False)),
+                                            ("N16384_bf16_causal", (1, 16, 16384, 128, True, False)),
+                                            ("mid_bf16_causal", (4, 16, 2048, 128, True, False)),
+                                            ("N16384_fp8", (1, 16, 16384, 128, False, True)),
+                                            ("N4096_fp8", (4, 16, 4096, 128, False, True)),
+                                            ("N8192_d64_bf16", (2, 32, 8192, 64, False, False)),
+                                            ("N2048_d64_bf16", (8, 32, 2048, 64, False, False)),
+                                            ("N8192_d64_bf16_causal", (2, 32, 8192, 64, True, False))):
         if fp8:
             x = [torch.randn((B, H, N, d), device=device, generator=g) for _ in range(3)]
             signs = gen.hadamard_signs(d, 4)
@@ -519,7 +523,7 @@ def run_ablate(args, device):
         o = torch.empty((B, H, N, d), device=device, dtype=torch.bfloat16)
         lse = torch.empty((B, H, N), device=device, dtype=torch.float32)
         res = {}
-        for var in ABLATE_BUILT[(fp8, causal)]:
+        for var in ABLATE_BUILT[(fp8, causal, d)]:
             def fn(var=var):
                 st = lib.fa_ablate_fwd(var, int(fp8), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                        lse.data_ptr(), B, H, N, d, int(causal), 1.0 / math.sqrt(d), *ds,

@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "libfa.so")
 LIB_ABLATE = os.path.join(HERE, "libfa_ablate.so")
 UNITS = ["api.cu", "attn_bf16.cu", "attn_fp16.cu", "attn_fp8.cu", "quant_fp8.cu", "quant_fp8_noalloc.cu",
          "splitkv.cu", "attn_split_bf16.cu", "attn_split_fp16.cu", "attn_bwd.cu"]
-ABLATE_UNITS = ["ablate_api.cu", "ablate_bf16.cu", "ablate_bf16_causal.cu", "ablate_fp8.cu"]
+ABLATE_UNITS = ["ablate_api.cu", "ablate_bf16.cu", "ablate_bf16_causal.cu", "ablate_fp8.cu", "ablate_d64.cu"]
 HEADERS = ["ptx.cuh", "attn_fwd.cuh", "quant_fp8.h", "attn_bwd.h", "splitkv.h", "ablate_inst.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

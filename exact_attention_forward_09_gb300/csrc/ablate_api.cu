@@ -7,10 +7,11 @@
 #include "fa_ablate.h"
 
 namespace fa {
-#define FA_EXTERN(E, C, V) extern template cudaError_t launch_attn<E, 128, C, false, V>(const AttnLaunch&);
+#define FA_EXTERN(E, D, C, V) extern template cudaError_t launch_attn<E, D, C, false, V>(const AttnLaunch&);
 FA_ABLATE_BF16_NONCAUSAL(FA_EXTERN)
 FA_ABLATE_BF16_CAUSAL(FA_EXTERN)
 FA_ABLATE_FP8(FA_EXTERN)
+FA_ABLATE_BF16_D64(FA_EXTERN)
 #undef FA_EXTERN
 }  // namespace fa
 
@@ -18,7 +19,7 @@ extern "C" fa_status fa_ablate_fwd(int variant, int fp8, const void* q, const vo
                                    float* lse, int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                                    const float* q_descale, const float* k_descale, const float* v_descale,
                                    cudaStream_t stream) {
-  if (d != 128 || (fp8 != 0 && fp8 != 1)) return FA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || (fp8 != 0 && fp8 != 1)) return FA_ERR_UNSUPPORTED;
   if (variant == 0) {
     // the shipped kernel, through the product's entry points
     if (fp8) return fa_fwd_fp8(q, k, v, o, lse, B, H, N, d, causal, scale, q_descale, k_descale, v_descale, stream);
@@ -32,16 +33,17 @@ extern "C" fa_status fa_ablate_fwd(int variant, int fp8, const void* q, const vo
   if (st != FA_OK || empty) return st;
   cudaError_t e = cudaErrorInvalidValue;
   bool built = false;
-#define FA_CASE(E, C, V)                                              \
-  if (!built && (E == fa::kE4M3) == (fp8 != 0) && C == (causal != 0) && V == variant) { \
-    e = fa::launch_attn<fa::E, 128, C, false, V>(L);                   \
-    built = true;                                                      \
+#define FA_CASE(E, D, C, V)                                                                      \
+  if (!built && (E == fa::kE4M3) == (fp8 != 0) && D == d && C == (causal != 0) && V == variant) { \
+    e = fa::launch_attn<fa::E, D, C, false, V>(L);                                                 \
+    built = true;                                                                                  \
   }
   using fa::kBF16;
   using fa::kE4M3;
   FA_ABLATE_BF16_NONCAUSAL(FA_CASE)
   FA_ABLATE_BF16_CAUSAL(FA_CASE)
   FA_ABLATE_FP8(FA_CASE)
+  FA_ABLATE_BF16_D64(FA_CASE)
 #undef FA_CASE
   if (!built) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

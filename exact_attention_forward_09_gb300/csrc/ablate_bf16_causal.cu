@@ -3,7 +3,7 @@
 #include "ablate_inst.h"
 
 namespace fa {
-#define FA_INST(E, C, V) template cudaError_t launch_attn<E, 128, C, false, V>(const AttnLaunch&);
+#define FA_INST(E, D, C, V) template cudaError_t launch_attn<E, D, C, false, V>(const AttnLaunch&);
 FA_ABLATE_BF16_CAUSAL(FA_INST)
 #undef FA_INST
 }  // namespace fa

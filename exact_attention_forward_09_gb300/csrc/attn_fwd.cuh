@@ -64,6 +64,8 @@ enum : int {
   kVarWholeP = 4,          // hand P to the MMA warp in one piece instead of two halves
   kVarOneTile = 8,         // one Q tile per CTA (S double-buffered) also for d <= 128
   kVarNoSteal = 16,        // no work stealing: every CTA runs only the unit it was launched with
+  kVarSepP = 32,           // P in its own tensor-memory columns (d = 64, two Q tiles): Q K^T(j+1) may
+                           // start once the softmax has read S(j)
 };
 
 template <int ELEM, int D, bool CAUSAL, int VAR = 0>
@@ -102,8 +104,14 @@ struct AttnCfg {
   // lands on S columns the other part has still to read.
   static constexpr int P_HALF_OFF = (CSPLIT == 2) ? 64 : P_COLS / 2;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL0 = 0;                        // S/P buffers at 0 and 128
-  static constexpr uint32_t O_COL0 = 256;                      // O accumulators from 256
+  // Separate P (two Q tiles, when S, P and O of both fit): S_t at 128 t,
+  // P_t after both S buffers, O_t after both P buffers.  Otherwise P is
+  // written over S (same columns).
+  static constexpr bool SEPP = (VAR & kVarSepP) && NQT == 2 && CSPLIT == 1 &&
+                               2 * (kBN + P_COLS + D) <= (int)TMEM_COLS;
+  static constexpr uint32_t S_COL0 = 0;                        // S buffers at 0 and 128
+  static constexpr uint32_t P_COL0 = SEPP ? 2 * kBN : 0;       // P buffers (SEPP) or P over S
+  static constexpr uint32_t O_COL0 = SEPP ? 2 * kBN + 2 * P_COLS : 256;  // O accumulators
   static_assert(O_COL0 + NQT * D <= TMEM_COLS, "TMEM budget");
   static constexpr int SOFTMAX_WARPS = 4 * NQT * CSPLIT;
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
@@ -189,6 +197,8 @@ struct Bars {
   uint64_t full[NS];
   uint64_t empty[NS];
   uint64_t s_full[2];
+  uint64_t s_free[2];     // separate P: the softmax has read S (the next Q K^T may overwrite it)
+  uint64_t p_free[2];     // separate P: P V done (P buffer free, O stable)
   uint64_t p_full[2][2];  // [S/P buffer][half of the key tile]
   uint64_t o_ready[2];
   uint64_t o_full[2];
@@ -331,6 +341,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], 128);
+      mbar_init(&bars->p_free[t], 1);
       mbar_init(&bars->p_full[t][0], 128);
       mbar_init(&bars->p_full[t][1], 128);
       mbar_init(&bars->o_ready[t], 1);
@@ -515,6 +527,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       int pos = 0;          // ring position of the next item to consume
       int k = 0;            // units processed
       int pc[2] = {0, 0};   // two Q tiles: P handshakes consumed per tile
+      int nqk[2] = {0, 0};  // separate P: Q K^T issued per tile (s_free phase of the previous one)
       int g = 0;            // one Q tile: S/P iterations so far (buffer = g & 1)
       bool ok = true;
       // every lane waits; the outcome is made uniform across the warp
@@ -566,7 +579,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       };
       // O_t (+)= P_buf V for half h of the keys of the V tile at ring position p
       auto issue_pv = [&](int t, int buf, int p, bool acc, int h) {
-        const uint32_t p_tmem = tmem + C::S_COL0 + buf * kBN;
+        const uint32_t p_tmem = tmem + C::P_COL0 + buf * (C::SEPP ? C::P_COLS : kBN);
 #pragma unroll
         for (int sp = 0; sp < C::SPT; ++sp) {
           const uint32_t d_tmem = tmem + C::O_COL0 + t * D + sp * C::SLOT_D;
@@ -594,7 +607,68 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
         auto qk_issued = [&]() {
           if (--qk_left == 0) mma_commit_elect(&bars->q_empty);
         };
-        if constexpr (C::NQT == 2) {
+        if constexpr (C::NQT == 2 && C::SEPP) {
+          // Separate P: S_t(j+1) is computed as soon as the softmax has read
+          // S_t(j) (s_free), while it still works on P_t(j); P V_t(j) then
+          // follows from the P buffer.  p_free tells the softmax that P V_t(j)
+          // is done (O stable, P buffer free); the unit's last P V commits
+          // o_full instead.
+          auto qk_next = [&](int t, int p) -> bool {
+            if (nqk[t] > 0) {
+              if (!warp_wait(&bars->s_free[t], (uint32_t)((nqk[t] - 1) & 1), abort_flag, prm.err)) return false;
+              tc_fence_after();
+            }
+            issue_qk(t, t, p);
+            mma_commit_elect(&bars->s_full[t]);
+            qk_issued();
+            ++nqk[t];
+            return true;
+          };
+          ok = wait_tile(pos);
+          if (!ok) break;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (ok && w.Jt[t] > 0) ok = qk_next(t, pos);
+          if (!ok) break;
+          release_tile(pos);
+          pos += C::SPT;
+          for (int j = 0; j < w.J && ok; ++j) {
+            const int pv_pos = pos;            // V_j
+            const int k_pos = pos + C::SPT;    // K_{j+1}
+            if (j + 1 < w.J) {
+              ok = wait_tile(k_pos);
+              if (!ok) break;
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                if (ok && j + 1 < w.Jt[t]) ok = qk_next(t, k_pos);
+              if (!ok) break;
+            }
+            ok = wait_tile(pv_pos);
+            if (!ok) break;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok) break;
+              if (j >= w.Jt[t]) continue;
+#pragma unroll
+              for (int h = 0; h < 2 && ok; ++h) {
+                ok = warp_wait(&bars->p_full[t][h], (uint32_t)(pc[t] & 1), abort_flag, prm.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, t, pv_pos, j > 0, h);
+              }
+              ++pc[t];
+              if (!ok) break;
+              mma_commit_elect(j + 1 < w.Jt[t] ? &bars->p_free[t] : &bars->o_full[t]);
+            }
+            if (!ok) break;
+            release_tile(pv_pos);
+            pos += C::SPT;
+            if (j + 1 < w.J) {
+              release_tile(k_pos);
+              pos += C::SPT;
+            }
+          }
+        } else if constexpr (C::NQT == 2) {
           // prologue: S_t(0) for both tiles
           ok = wait_tile(pos);
           if (!ok) break;
@@ -724,6 +798,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
     int oc = 0;               // units finished by this tile (o_full phases)
     int pv_seen = 0;          // one Q tile: PV completions consumed (global iteration order)
     int xc = 0;               // split softmax: exchanges made (slot parity)
+    int pfw = 0;              // separate P: p_free phases consumed (this tile)
     bool ok = true;
 
     for (int rr = 0; ok; ++rr) {
@@ -978,6 +1053,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
           if (gj >= 2 && !consume_o(gj - 2)) { ok = false; break; }
         }
         const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + buf * kBN;
+        // where P goes: over S, or (separate P) this tile's P buffer
+        const uint32_t p_base = C::SEPP ? tmem + lane_addr + C::P_COL0 + t * C::P_COLS : s_addr;
         float s[NCOL];
         float cj = prm.scale_log2;   // scale of this tile (log2 units)
         const int col0 = (w.tb + j) * kBN;
@@ -994,6 +1071,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
               for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(u[i]);
             }
             tmem_wait_ld();
+          }
+          if constexpr (C::SEPP) {
+            // S is in registers: the next Q K^T may overwrite it
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[t]);
           }
           if constexpr (ELEM == kE4M3) {
             cj *= f_k;
@@ -1041,6 +1123,18 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
           m_run = mx2;
         }
         l_run *= alpha;
+        if constexpr (C::SEPP) {
+          // P V of the previous tile must be done before O is rescaled and
+          // the P buffer rewritten
+          if (j > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_free[t], (uint32_t)(pfw & 1), abort_flag, prm.err))) {
+              ok = false;
+              break;
+            }
+            ++pfw;
+            tc_fence_after();
+          }
+        }
         // rescale O (this thread's output columns) when any row of the warp
         // moved (never on the first tile)
         if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -1106,7 +1200,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
                 acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
                 u[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
               }
-              tmem_st8(s_addr + qq * 8, u);
+              tmem_st8(p_base + qq * 8, u);
             } else {
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -1118,7 +1212,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
                   acc[i & 3] = add2(acc[i & 3], a);
                   u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
                 }
-                tmem_st8(s_addr + qq * 16 + h * 8, u);
+                tmem_st8(p_base + qq * 16 + h * 8, u);
               }
             }
           }

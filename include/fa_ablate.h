@@ -16,15 +16,19 @@
  *   4   whole P: P handed to the MMA warp in one piece, not in two halves
  *   8   one Q tile per CTA with S double-buffered (no two-tile alternation)
  *   16  no work stealing: each CTA runs only the unit it was launched with
- * Built instances: bf16 non-causal and FP8 non-causal with every code above;
- * bf16 causal with 0, 1, 8 and 16.
+ *   32  separate P: P gets its own tensor-memory columns, so the next Q K^T
+ *       starts once the softmax has read S (d = 64 only: there S, P and O of
+ *       two Q tiles fit the 512 columns)
+ * Built instances: d = 128 bf16 non-causal and FP8 non-causal with codes
+ * 0, 1, 2, 4, 8, 16; d = 128 bf16 causal with 0, 1, 8, 16; d = 64 bf16
+ * (causal and not) with 0 and 32.
  *   variant      one of the codes above
  *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
  *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8
  *   other arguments as fa_fwd / fa_fwd_fp8 (device pointers, [B, H, N, d]
- *   contiguous, o bf16, lse fp32 [B, H, N]); d must be 128.
- * Errors: FA_ERR_UNSUPPORTED for a variant / type / causal combination that
- * was not built or d != 128; otherwise as fa_fwd.
+ *   contiguous, o bf16, lse fp32 [B, H, N]); d is 64 or 128.
+ * Errors: FA_ERR_UNSUPPORTED for a variant / type / head dimension / causal
+ * combination that was not built; otherwise as fa_fwd.
  */
 #ifndef FA_ABLATE_H
 #define FA_ABLATE_H

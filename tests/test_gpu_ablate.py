@@ -15,7 +15,8 @@ from gpu_util import FP8_O_RMSE, assert_bf16_parity, errors, make_qkv, oracle_ro
 
 pytestmark = pytest.mark.gpu
 
-BUILT = {(False, False): (0, 1, 2, 4, 8, 16), (False, True): (0, 1, 8, 16), (True, False): (0, 1, 2, 4, 8, 16)}
+BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16), (False, True, 128): (0, 1, 8, 16),
+         (True, False, 128): (0, 1, 2, 4, 8, 16), (False, False, 64): (0, 32), (False, True, 64): (0, 32)}
 
 
 @pytest.fixture(scope="module")
@@ -31,22 +32,23 @@ def ab():
     return fa, lib
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [640, 1100])
-def test_bf16_variants(ab, causal, N):
+def test_bf16_variants(ab, d, causal, N):
     fa, lib = ab
-    host, (q, k, v) = make_qkv(2, 3, N, 128, 1700 + N)
-    scale = 1.0 / math.sqrt(128)
+    host, (q, k, v) = make_qkv(2, 3, N, d, 1700 + N + d)
+    scale = 1.0 / math.sqrt(d)
     o_ref, l_ref = oracle_rows(host, causal, scale)
-    for var in BUILT[(False, causal)]:
+    for var in BUILT[(False, causal, d)]:
         o = torch.empty_like(q)
         lse = torch.empty((2, 3, N), device="cuda", dtype=torch.float32)
         st = lib.fa_ablate_fwd(var, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               2, 3, N, 128, int(causal), scale, None, None, None,
+                               2, 3, N, d, int(causal), scale, None, None, None,
                                torch.cuda.current_stream().cuda_stream)
         assert st == fa.FA_OK
         fa.check_device_error()
-        assert_bf16_parity(errors(o, lse, o_ref, l_ref), f"variant {var} causal={causal} N={N}")
+        assert_bf16_parity(errors(o, lse, o_ref, l_ref), f"variant {var} d={d} causal={causal} N={N}")
 
 
 def test_fp8_variants(ab):
@@ -60,7 +62,7 @@ def test_fp8_variants(ab):
     dev = lambda a: torch.from_numpy(a).cuda()
     qd, kd, vd, qsd, ksd, vsd = (dev(a) for a in (qc, kc, vc, qs, ks, vs))
     o_ex, _ = oracle.attn_fwd(q, k, v, causal=False, scale=1 / math.sqrt(d))
-    for var in BUILT[(True, False)]:
+    for var in BUILT[(True, False, 128)]:
         o = torch.empty((B, H, N, d), device="cuda", dtype=torch.bfloat16)
         lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
         st = lib.fa_ablate_fwd(var, 1, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -75,7 +77,9 @@ def test_fp8_variants(ab):
 def test_unbuilt_variant_is_refused(ab):
     fa, lib = ab
     p = torch.empty(16, device="cuda").data_ptr()
-    # causal FP8 variants are not built; d other than 128 is not either
+    # causal FP8 variants are not built, nor separate P at d = 128, nor d = 256
     assert lib.fa_ablate_fwd(2, 1, p, p, p, p, p, 1, 1, 128, 128, 1, 0.1, p, p, p, None) == fa.FA_ERR_UNSUPPORTED
-    assert lib.fa_ablate_fwd(0, 0, p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, None, None, None, None) == \
+    assert lib.fa_ablate_fwd(32, 0, p, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None, None, None, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_ablate_fwd(0, 0, p, p, p, p, p, 1, 1, 128, 256, 0, 0.1, None, None, None, None) == \
         fa.FA_ERR_UNSUPPORTED
