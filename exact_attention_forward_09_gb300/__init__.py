@@ -84,6 +84,8 @@ def _lib():
         lib.fa_check_device_error.restype = i32
         lib.fa_debug_inject.argtypes = [i32]
         lib.fa_debug_inject.restype = i32
+        lib.fa_debug_exp2.argtypes = [vp, vp, i64, i32, vp]
+        lib.fa_debug_exp2.restype = i32
         lib.fa_version.argtypes = []
         lib.fa_version.restype = i32
         _LIB = lib

@@ -262,6 +262,20 @@ fa_status internal_prepare_fwd(const void* q, const void* k, const void* v, void
   L.stream = stream;
   return FA_OK;
 }
+
+// the two ways the forward kernels compute an exponential of P, one pair
+// per thread (fa_debug_exp2)
+template <int METHOD>
+__global__ void exp2_eval_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float2 a = make_float2(x[i], (i + 1 < n) ? x[i + 1] : 0.0f);
+  float2 r;
+  if constexpr (METHOD == 0) r = make_float2(ex2(a.x), ex2(a.y));
+  else r = ex2_poly2<METHOD>(a);
+  y[i] = r.x;
+  if (i + 1 < n) y[i + 1] = r.y;
+}
 }  // namespace fa
 
 extern "C" {
@@ -719,6 +733,23 @@ fa_status fa_debug_inject(int flags) {
   g_inject.store(flags & 1);
   g_inject_quant.store((flags >> 1) & 1);
   return FA_OK;
+}
+
+fa_status fa_debug_exp2(const float* x, float* y, int64_t n, int method, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (x == nullptr || y == nullptr)) || !(method == 0 || method == 3 || method == 4))
+    return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  const int64_t pairs = (n + 1) / 2;
+  if (pairs > (int64_t)256 * 0x7fffffff) return FA_ERR_INVALID_ARG;
+  const unsigned grid = (unsigned)((pairs + 255) / 256);
+  if (method == 0) fa::exp2_eval_kernel<0><<<grid, 256, 0, stream>>>(x, y, n);
+  else if (method == 3) fa::exp2_eval_kernel<3><<<grid, 256, 0, stream>>>(x, y, n);
+  else fa::exp2_eval_kernel<4><<<grid, 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_version(void) { return 100; }

@@ -66,6 +66,7 @@ enum : int {
   kVarNoSteal = 16,        // no work stealing: every CTA runs only the unit it was launched with
   kVarSepP = 32,           // P in its own tensor-memory columns (d = 64, two Q tiles): Q K^T(j+1) may
                            // start once the softmax has read S(j)
+  kVarPoly = 64,           // a share of P's exponentials by a polynomial on the FMA pipe (measured slower)
 };
 
 template <int ELEM, int D, bool CAUSAL, int VAR = 0>
@@ -135,6 +136,16 @@ struct AttnCfg {
                 "register split exceeds the launch budget");
   // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max
   static constexpr float TAU = (VAR & kVarEagerRescale) ? 0.0f : (ELEM == kE4M3) ? 2.0f : 8.0f;
+  // Exponentials of P: POLY of every 8 pairs by the FMA-pipe polynomial
+  // (ex2_poly2, degree POLY_DEG), the rest by MUFU ex2.  Off in the shipped
+  // kernels: the softmax of a tile is a chain of dependent steps, not a
+  // saturated special-function unit, and every 1/8 of the exponentials moved
+  // onto the FMA pipe lengthened it (5-10% slower per 1/8, measured on
+  // bf16 d = 64 / 128 and FP8).  fp16 P (11-bit significand) would take the
+  // degree-4 polynomial.
+  static constexpr int POLY = !(VAR & kVarPoly) ? 0 : (ELEM == kE4M3) ? 3 : (D <= 64) ? 3 : 1;
+  static constexpr int POLY_DEG = (ELEM == kFP16) ? 4 : 3;
+  static constexpr bool poly_pair(int k) { return ((k % 8 + 1) * POLY) / 8 > ((k % 8) * POLY) / 8; }
   // FP8: P is stored as p * 2^6 * (s_Vj / max_j s_Vj) <= 2^6 * 2^TAU = 256,
   // inside the E4M3 range (448)
   static constexpr float P8_SCALE = 64.0f;
@@ -1168,9 +1179,9 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
         float2 acc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-        auto p_pair = [&](int c, bool masked_tile) -> float2 {
+        auto p_pair = [&](int c, bool masked_tile, bool poly) -> float2 {
           const float2 x = fma2(make_float2(s[c], s[c + 1]), cj2, nm2);
-          float2 p = make_float2(ex2(x.x), ex2(x.y));
+          float2 p = poly ? ex2_poly2<C::POLY_DEG>(x) : make_float2(ex2(x.x), ex2(x.y));
           if (masked_tile) {
             p.x = (s[c] == mask_val) ? 0.0f : p.x;
             p.y = (s[c + 1] == mask_val) ? 0.0f : p.y;
@@ -1195,7 +1206,8 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const int c = q * 32 + 4 * i;
-                const float2 a = p_pair(c, masked_tile), b = p_pair(c + 2, masked_tile);
+                const float2 a = p_pair(c, masked_tile, C::poly_pair(2 * i));
+                const float2 b = p_pair(c + 2, masked_tile, C::poly_pair(2 * i + 1));
                 acc[(2 * i) & 3] = add2(acc[(2 * i) & 3], a);
                 acc[(2 * i + 1) & 3] = add2(acc[(2 * i + 1) & 3], b);
                 u[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
@@ -1208,7 +1220,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const int c = q * 32 + h * 16 + 2 * i;
-                  const float2 a = p_pair(c, masked_tile);
+                  const float2 a = p_pair(c, masked_tile, C::poly_pair(i));
                   acc[i & 3] = add2(acc[i & 3], a);
                   u[i] = (ELEM == kBF16) ? pack_bf16x2(a.x, a.y) : pack_f16x2(a.x, a.y);
                 }

@@ -447,6 +447,16 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t A, B, D;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(D) : "l"(A), "l"(B));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(D));
+  return r;
+}
+
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   uint64_t A, B, D;
   asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
@@ -467,6 +477,55 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;
   asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// max that propagates NaN (plain max returns the other operand)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// 2^x for a pair, on the FMA pipe instead of the special-function unit, so
+// that a share of a tile's exponentials can run beside the MUFU ones
+// (sharing the exponentials between the two pipes follows FlashAttention-4;
+// the evaluation is textbook range reduction plus a fitted polynomial):
+//   * x is raised to at least -126 (so 2^n below stays a normal power; a
+//     result that would be smaller comes out near 2^-126 instead), NaN kept;
+//   * n = round(x): adding 1.5 * 2^23 leaves round-to-nearest(x) in the low
+//     mantissa bits of the sum, and subtracting it again gives n as a float
+//     (Cody and Waite's additive range reduction), f = x - n in [-1/2, 1/2];
+//   * 2^f by Horner's rule on a minimax polynomial of degree DEG, its
+//     coefficients fitted for the relative error on [-1/2, 1/2] by the Remez
+//     exchange algorithm: at most 7.5e-5 (degree 3) or 2.6e-6 (degree 4)
+//     with fp32 coefficients and fp32 evaluation;
+//   * the result is p(f) * 2^n, 2^n built from its exponent field
+//     ((n + 127) << 23, n taken from the low bits of the rounding sum); the
+//     product by a power of two is exact and keeps a NaN a NaN.
+// Valid for x <= 127 (the result then stays finite); the kernels keep x below 16.
+template <int DEG>
+__device__ __forceinline__ float2 ex2_poly2(float2 x) {
+  static_assert(DEG == 3 || DEG == 4, "degree 3 or 4");
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmax_nan(x.x, -126.0f);
+  x.y = fmax_nan(x.y, -126.0f);
+  const float2 y = add2(x, make_float2(kShift, kShift));
+  const float2 n = sub2(y, make_float2(kShift, kShift));
+  const float2 f = sub2(x, n);
+  float2 p;
+  if constexpr (DEG == 3) {
+    p = fma2(f, make_float2(0.0551716685f, 0.0551716685f), make_float2(0.242611125f, 0.242611125f));
+    p = fma2(p, f, make_float2(0.693260968f, 0.693260968f));
+    p = fma2(p, f, make_float2(0.999928057f, 0.999928057f));
+  } else {
+    p = fma2(f, make_float2(0.00957010221f, 0.00957010221f), make_float2(0.0559178591f, 0.0559178591f));
+    p = fma2(p, f, make_float2(0.240247443f, 0.240247443f));
+    p = fma2(p, f, make_float2(0.693121791f, 0.693121791f));
+    p = fma2(p, f, make_float2(0.999999285f, 0.999999285f));
+  }
+  const float2 two_n = make_float2(__uint_as_float((__float_as_uint(y.x) << 23) + 0x3f800000u),
+                                   __uint_as_float((__float_as_uint(y.y) << 23) + 0x3f800000u));
+  return mul2(p, two_n);
 }
 
 __device__ __forceinline__ float lg2(float x) {

@@ -115,11 +115,6 @@ __device__ __forceinline__ int elem_of(int e, int p) {
   return (e & (G - 1)) + G * p + 128 * (e >> 5);
 }
 
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  // RN(a - b) per half: a fused multiply-add whose product b * -1 is exact
-  return fma2(b, make_float2(-1.0f, -1.0f), a);
-}
-
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float2 lo, float2 hi) {
   uint16_t a, b;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(a) : "f"(lo.y), "f"(lo.x));

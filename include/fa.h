@@ -390,6 +390,21 @@ fa_status fa_check_device_error(cudaStream_t stream);
  */
 fa_status fa_debug_inject(int flags);
 
+/*
+ * fa_debug_exp2 -- TEST HOOK: evaluates, element by element, y[i] = 2^x[i]
+ * the ways the forward kernels can compute the exponentials of P: method 0
+ * with the special-function unit's ex2 as the shipped kernels do
+ * (approximate, subnormal results flushed to zero), method 3 or 4 with the
+ * FMA-pipe polynomial of that degree that the ablation variant 64 of
+ * fa_ablate.h uses for a share of P (range
+ * reduction x = n + f, |f| <= 1/2, minimax polynomial for 2^f; relative
+ * error at most 7.5e-5 (degree 3) or 2.6e-6 (degree 4) for -125 <= x <= 127;
+ * x below -126 gives a result of at most 2^-125.5; NaN gives NaN).  x, y:
+ * device arrays of n fp32 values (y may equal x).  Asynchronous on `stream`.
+ * FA_ERR_INVALID_ARG for n < 0, a null pointer with n > 0 or another method.
+ */
+fa_status fa_debug_exp2(const float* x, float* y, int64_t n, int method, cudaStream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fa_version(void);
 

@@ -19,9 +19,13 @@
  *   32  separate P: P gets its own tensor-memory columns, so the next Q K^T
  *       starts once the softmax has read S (d = 64 only: there S, P and O of
  *       two Q tiles fit the 512 columns)
+ *   64  polynomial exponentials: 1 of every 8 pairs of P (d = 128 bf16) or
+ *       3 of 8 (FP8, d = 64) computed on the FMA pipe by range reduction and
+ *       a degree-3 minimax polynomial instead of the special-function unit
+ *       (fa_debug_exp2 method 3 evaluates the same function)
  * Built instances: d = 128 bf16 non-causal and FP8 non-causal with codes
- * 0, 1, 2, 4, 8, 16; d = 128 bf16 causal with 0, 1, 8, 16; d = 64 bf16
- * (causal and not) with 0 and 32.
+ * 0, 1, 2, 4, 8, 16, 64; d = 128 bf16 causal with 0, 1, 8, 16; d = 64 bf16
+ * non-causal with 0, 32, 64 and causal with 0, 32.
  *   variant      one of the codes above
  *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
  *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8
