@@ -478,9 +478,10 @@ ABLATE_VARIANTS = {0: "shipped kernel", 1: "split softmax (two warpgroups per Q 
                    2: "eager rescale (no lazy threshold)", 4: "P handed over whole (not in two halves)",
                    8: "one Q tile per CTA, S double-buffered (no two-tile alternation)",
                    16: "no work stealing", 32: "separate P (Q K^T of the next tile starts once S is read)",
-                   64: "polynomial exponentials on the FMA pipe for 1/8 (d=128 bf16) or 3/8 (FP8, d=64) of P"}
-ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64), (False, True, 128): (0, 1, 8, 16),
-                (True, False, 128): (0, 1, 2, 4, 8, 16, 64), (False, False, 64): (0, 32, 64),
+                   64: "polynomial exponentials on the FMA pipe for 1/8 (d=128 bf16) or 3/8 (FP8, d=64) of P",
+                   128: "early partial Q K^T (keys beyond P's columns issued at P's first half)"}
+ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64, 128), (False, True, 128): (0, 1, 8, 16),
+                (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128), (False, False, 64): (0, 32, 64, 128),
                 (False, True, 64): (0, 32)}
 
 

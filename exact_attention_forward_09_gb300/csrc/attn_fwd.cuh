@@ -67,6 +67,9 @@ enum : int {
   kVarSepP = 32,           // P in its own tensor-memory columns (d = 64, two Q tiles): Q K^T(j+1) may
                            // start once the softmax has read S(j)
   kVarPoly = 64,           // a share of P's exponentials by a polynomial on the FMA pipe (measured slower)
+  kVarEarlyQK = 128,       // two Q tiles, P over S: the part of the next Q K^T whose S columns P does not
+                           // use is issued when the first half of P arrives, the rest after the second half
+                           // (measured slower: an MMA with N = 64 runs at 2/3 of the N = 128 rate)
 };
 
 template <int ELEM, int D, bool CAUSAL, int VAR = 0>
@@ -152,6 +155,13 @@ struct AttnCfg {
   static_assert(ELEM != kE4M3 || P8_SCALE * (1 << (int)TAU) <= 256.0f, "FP8 P would leave the E4M3 range");
   static constexpr uint32_t A_FMT = (ELEM == kBF16) ? 1u : 0u;  // bf16=1, f16=0, e4m3=0
   static constexpr uint32_t IDESC_QK = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN);
+  // Early Q K^T: keys QK_SPLIT.. of the next tile land on S columns that P
+  // (written over S from column 0) never uses.
+  static constexpr bool EARLY_QK = (VAR & kVarEarlyQK) && NQT == 2 && CSPLIT == 1 && !SEPP && !(VAR & kVarWholeP);
+  static constexpr int QK_SPLIT = P_COLS;
+  static_assert(!EARLY_QK || (QK_SPLIT % 16 == 0 && QK_SPLIT < kBN), "MMA N must be a multiple of 16");
+  static constexpr uint32_t IDESC_QK_LO = instr_desc(A_FMT, A_FMT, 0, 0, 128, QK_SPLIT);
+  static constexpr uint32_t IDESC_QK_HI = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN - QK_SPLIT);
   static constexpr uint32_t IDESC_PV = instr_desc(A_FMT, A_FMT, 0, 1, 128, SLOT_D);
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
@@ -568,14 +578,17 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       const uint64_t ring_k_desc0 = smem_desc(ring_s, 16, 1024, 2);         // K slots, K-major
       const uint64_t ring_v_desc0 = smem_desc(ring_s, C::CHUNK_BYTES, 1024, 2);  // V slots, MN-major
       auto slot_of = [&](int p) -> uint32_t { return (uint32_t)(p % C::NS); };
-      // S_buf = Q_t K^T for the K tile at ring position p
-      auto issue_qk = [&](int t, int buf, int p) {
-        const uint32_t d_tmem = tmem + C::S_COL0 + buf * kBN;
+      // S_buf = Q_t K^T for the K tile at ring position p; part 0: all keys,
+      // part 1: keys 0 .. QK_SPLIT-1, part 2: keys QK_SPLIT .. kBN-1
+      auto issue_qk = [&](int t, int buf, int p, int part = 0) {
+        const int key0 = (part == 2) ? C::QK_SPLIT : 0;
+        const uint32_t idesc = (part == 0) ? C::IDESC_QK : (part == 1) ? C::IDESC_QK_LO : C::IDESC_QK_HI;
+        const uint32_t d_tmem = tmem + C::S_COL0 + buf * kBN + key0;
         const uint64_t a0 = q_desc0 + (uint64_t)((t * C::NCH * C::CHUNK_BYTES) >> 4);
         uint64_t b0[C::SPT];
 #pragma unroll
         for (int sp = 0; sp < C::SPT; ++sp)
-          b0[sp] = ring_k_desc0 + (uint64_t)((slot_of(p + sp) * C::SLOT_BYTES) >> 4);
+          b0[sp] = ring_k_desc0 + (uint64_t)((slot_of(p + sp) * C::SLOT_BYTES + key0 * 128) >> 4);
 #pragma unroll
         for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
           const int byte_k = ks * 32;                         // byte offset along the row
@@ -585,7 +598,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
           const int ch_in_slot = ch % C::SLOT_CH;
           const uint64_t a = a0 + (uint64_t)((ch * C::CHUNK_BYTES + in_ch) >> 4);
           const uint64_t b = b0[sp] + (uint64_t)((ch_in_slot * C::CHUNK_BYTES + in_ch) >> 4);
-          mma_ss_elect<C::MMA_KIND>(d_tmem, a, b, C::IDESC_QK, ks > 0 ? 1u : 0u);
+          mma_ss_elect<C::MMA_KIND>(d_tmem, a, b, idesc, ks > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_buf V for half h of the keys of the V tile at ring position p
@@ -709,12 +722,18 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(t, t, pv_pos, j > 0, h);
+                if (C::EARLY_QK && h == 0 && j + 1 < w.Jt[t]) {
+                  // the softmax has read all of S(j): the S columns that P
+                  // does not use can take their part of S(j+1) now
+                  if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
+                  issue_qk(t, t, k_pos, 2);
+                }
               }
               ++pc[t];
               if (!ok) break;
               if (j + 1 < w.Jt[t]) {
                 if (!k_ready) { ok = wait_tile(k_pos); k_ready = true; if (!ok) break; }
-                issue_qk(t, t, k_pos);
+                issue_qk(t, t, k_pos, C::EARLY_QK ? 1 : 0);
                 mma_commit_elect(&bars->s_full[t]);
                 qk_issued();
               } else {

@@ -23,9 +23,13 @@
  *       3 of 8 (FP8, d = 64) computed on the FMA pipe by range reduction and
  *       a degree-3 minimax polynomial instead of the special-function unit
  *       (fa_debug_exp2 method 3 evaluates the same function)
+ *   128 early partial Q K^T: the keys of the next tile whose S columns P
+ *       (written over S from column 0) does not use are multiplied as soon as
+ *       the first half of P arrives, the remaining keys after the second half
+ *       (two narrower MMAs instead of one of N = 128)
  * Built instances: d = 128 bf16 non-causal and FP8 non-causal with codes
- * 0, 1, 2, 4, 8, 16, 64; d = 128 bf16 causal with 0, 1, 8, 16; d = 64 bf16
- * non-causal with 0, 32, 64 and causal with 0, 32.
+ * 0, 1, 2, 4, 8, 16, 64, 128; d = 128 bf16 causal with 0, 1, 8, 16; d = 64
+ * bf16 non-causal with 0, 32, 64, 128 and causal with 0, 32.
  *   variant      one of the codes above
  *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
  *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8
