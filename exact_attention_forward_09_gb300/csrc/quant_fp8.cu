@@ -31,8 +31,8 @@
 // Kernel organisation (persistent, one CTA per SM).  A load warp streams the
 // input through a ring of shared-memory slots with TMA (each slot is half a
 // 128-row block: 32-float x 64-row boxes, 128-byte swizzle, rows past N read
-// as zero), with full / empty mbarriers; sixteen consumer warps take 8 rows
-// each, so a block is one pass.  A row is spread over 4 lanes (lane / 8 picks
+// as zero), with full / empty mbarriers; a group of warps takes a block in
+// one pass, 8 or 16 rows per warp (two groups on alternate blocks).  A row is spread over 4 lanes (lane / 8 picks
 // the quarter, lane % 8 the row), chosen so that the 8 lanes of each
 // shared-memory phase read 8 different rows and the swizzle puts them in
 // different banks.  The rotated rows stay in registers: each warp frees its
@@ -54,31 +54,39 @@ namespace {
 
 template <int D>
 struct QCfg {
-  static constexpr int NW = 16;                  // warps per CTA
+  // Warps per CTA.  The rotation and the exact rounding are latency-bound
+  // chains per row, so the warps in flight matter: d = 64 runs 32 warps of
+  // 64 registers (measured 13% faster with the rotation than 16 warps); at
+  // d = 128 that many warps spill and leave 2 ring slots per group instead
+  // of 3 (measured slower), so it keeps 16 warps with two row sets each;
+  // d = 256 runs 16 warps (its rows need 128 registers).
+  static constexpr int NW = (D == 64) ? 32 : 16;
   static constexpr int THREADS = 32 * NW;
-  // Two groups of 8 warps work on alternate blocks, each with its own ring
-  // and barrier, so that one group's wait for its block maximum overlaps
-  // the other group's work (d = 256: one group; its rows do not fit twice).
+  // Two groups work on alternate blocks, each with its own ring and
+  // barrier, so that one group's wait for its block maximum overlaps the
+  // other group's work (d = 256: one group; its rows do not fit twice).
   static constexpr int NG = (D == 256) ? 1 : 2;
   static constexpr int WG = NW / NG;             // warps per group
-  static constexpr int RS = NG;                  // 8-row sets per warp and block
+  static constexpr int RS = 128 / (8 * WG);      // 8-row sets per warp and block
+  static_assert(RS == 1 || RS == 2, "a group covers a 128-row block");
   static constexpr int E = D / 4;                // elements of a row per lane
   static constexpr int G = E < 32 ? E : 32;      // contiguous run of a lane's elements
   static constexpr int BOXES = D / 32;           // 32-float boxes per row
   static constexpr int SLOT_ROWS = 64;           // half a block per slot
   static constexpr int BOX_BYTES = SLOT_ROWS * 128;
   static constexpr int SLOT_BYTES = BOXES * BOX_BYTES;
-  // Slots per group.  With one group each slot must serve one half of the
-  // block only, so the count is even: position q goes to slot q % NSG and to
-  // half q % 2.  (An odd count would let a slot alternate between the
-  // halves, and a half running a block ahead could wait on a slot two phases
-  // ahead of its last fill, which an mbarrier's phase parity cannot tell
-  // from the previous phase.)  With two groups every warp of a group reads
-  // both halves, in order, so any count works.
+  // Slots per group.  With one row set per warp, a warp reads one half of
+  // each block, so each slot must serve one half only and the count is even:
+  // position q goes to slot q % NSG and to half q % 2.  (An odd count would
+  // let a slot alternate between the halves, and a half running a block
+  // ahead could wait on a slot two phases ahead of its last fill, which an
+  // mbarrier's phase parity cannot tell from the previous phase.)  With two
+  // row sets every warp of a group reads both halves, in order, so any
+  // count works.
   static constexpr int NSG_RAW = 196608 / SLOT_BYTES / NG;
   static constexpr int NSG_CAP = NSG_RAW > 8 ? 8 : NSG_RAW;
-  static constexpr int NSG = (NG == 1) ? (NSG_CAP & ~1) : NSG_CAP;
-  static_assert(NSG >= 2 && (NG == 2 || NSG % 2 == 0), "ring too shallow or odd");
+  static constexpr int NSG = (RS == 1) ? (NSG_CAP & ~1) : NSG_CAP;
+  static_assert(NSG >= 2 && (RS == 2 || NSG % 2 == 0), "ring too shallow or odd");
   static constexpr int NSLOT = NG * NSG;
   static constexpr int SMEM_BYTES = NSLOT * SLOT_BYTES + 1024 + 1024;  // ring + barriers + alignment
 };
@@ -87,7 +95,7 @@ template <int NS>
 struct QShared {
   uint64_t full[NS];
   uint64_t empty[NS];
-  float red[2][2][8];  // [group][block parity][warp of group] (one group: [0][parity][16])
+  float red[64];       // [group][block parity][warp of group]; MODE 1: [warp]
   int last_pos[NS];
   int abort_flag;
   int first_bad;       // first block iteration (of the CTA) some warp could not finish
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
   // it = g, g + NG, g + 2 NG, ...  Its j-th block fills group positions 2j
   // (rows 0..63) and 2j + 1 (rows 64..127) of the group's ring of NSG slots.
   // Row set k of this warp: half hk, row r_slot within the half.
-  auto half_of = [&](int k) -> int { return (C::NG == 2) ? k : wg / 8; };
+  auto half_of = [&](int k) -> int { return (RS == 2) ? k : wg / 8; };
   const int r_slot = (wg % 8) * 8 + rl;
   uint8_t* gring = ring + grp * NSG * C::SLOT_BYTES;
   uint64_t* gfull = &sh->full[grp * NSG];
@@ -434,8 +442,7 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
       // for every warp of the group as soon as one of them could not read
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
-      float* red = &sh->red[0][0][0] + (grp * 2 + (j & 1)) * 8;   // one group: 16 entries over [0][parity]
-      if (C::NG == 1) red = &sh->red[0][0][0] + (j & 1) * 16;
+      float* red = &sh->red[0] + (grp * 2 + (j & 1)) * C::WG;
       if (lane == 0) red[wg] = am;
       if (!bar_and(1 + grp, 32 * C::WG, ok)) {
         if (lane == 0) atomicMin(&sh->first_bad, it);
@@ -497,11 +504,11 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
   if constexpr (MODE == 1) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) cta_max = fmaxf(cta_max, __shfl_xor_sync(0xffffffffu, cta_max, m));
-    if (lane == 0) (&sh->red[0][0][0])[warp] = cta_max;
+    if (lane == 0) sh->red[warp] = cta_max;
     __syncthreads();
     if (threadIdx.x == 0) {
       float mx = 0.0f;
-      for (int w = 0; w < C::NW; ++w) mx = fmaxf(mx, (&sh->red[0][0][0])[w]);
+      for (int w = 0; w < C::NW; ++w) mx = fmaxf(mx, sh->red[w]);
       if (sh->first_bad != INT_MAX) mx = INFINITY;
       atomicMax(reinterpret_cast<int*>(prm.ws), __float_as_int(mx));
     }
