@@ -73,6 +73,12 @@ typedef enum {
  * before the P V product ("FlashAttention-3: async pipelines on Hopper",
  * section "Online Softmax is still the core of exact merging": FP16/BF16
  * keep the rescaling and accumulation state in FP32).
+ * Non-finite inputs are not checked.  A NaN in a query row makes that row's
+ * O and LSE NaN; a NaN in key row j makes NaN every row that sees key j.  A
+ * NaN or infinity in element (j, c) of V reaches column c of O in every row
+ * that sees key j and also, with causal = 1, in the rows of j's 128-row tile
+ * that precede j (P V multiplies their P = 0 by it); rows of earlier tiles,
+ * the other columns and LSE are unaffected.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int64_t B, int64_t H, int64_t N, int64_t d,
