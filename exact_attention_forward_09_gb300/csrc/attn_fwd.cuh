@@ -137,8 +137,11 @@ struct AttnCfg {
   static constexpr int SOFTMAX_REGS = (CSPLIT == 2) ? 96 : (ELEM == kE4M3) ? 216 : 200;
   static_assert(!REALLOC || 128 * CTRL_REGS + SOFTMAX_WARPS * 32 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
-  // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max
-  static constexpr float TAU = (VAR & kVarEagerRescale) ? 0.0f : (ELEM == kE4M3) ? 2.0f : 8.0f;
+  // lazy-rescale threshold (log2 units): p <= 2^TAU against the running max.
+  // FP8 takes the largest TAU its P range allows (below): each rescale reads
+  // and writes all of O in TMEM on the softmax's own chain, and at TAU = 2
+  // rescales cost FP8 about 12% (measured).
+  static constexpr float TAU = (VAR & kVarEagerRescale) ? 0.0f : (ELEM == kE4M3) ? 3.8f : 8.0f;
   // Exponentials of P: POLY of every 8 pairs by the FMA-pipe polynomial
   // (ex2_poly2, degree POLY_DEG), the rest by MUFU ex2.  Off in the shipped
   // kernels: the softmax of a tile is a chain of dependent steps, not a
@@ -149,10 +152,12 @@ struct AttnCfg {
   static constexpr int POLY = !(VAR & kVarPoly) ? 0 : (ELEM == kE4M3) ? 3 : (D <= 64) ? 3 : 1;
   static constexpr int POLY_DEG = (ELEM == kFP16) ? 4 : 3;
   static constexpr bool poly_pair(int k) { return ((k % 8 + 1) * POLY) / 8 > ((k % 8) * POLY) / 8; }
-  // FP8: P is stored as p * 2^6 * (s_Vj / max_j s_Vj) <= 2^6 * 2^TAU = 256,
-  // inside the E4M3 range (448)
-  static constexpr float P8_SCALE = 64.0f;
-  static_assert(ELEM != kE4M3 || P8_SCALE * (1 << (int)TAU) <= 256.0f, "FP8 P would leave the E4M3 range");
+  // FP8: P is stored as p * 2^5 * (s_Vj / max_j s_Vj) <= 2^5 * 2^TAU < 446,
+  // inside the E4M3 range (448).  The scale sets where small p reach E4M3's
+  // subnormals (p below 2^-11); 2^5 against 2^6 left the O error of the FP8
+  // workloads unchanged (measured) and lets TAU rise from 2.8 to 3.8.
+  static constexpr float P8_SCALE = 32.0f;
+  static_assert(ELEM != kE4M3 || TAU <= 3.807f, "FP8 P would leave the E4M3 range: 32 * 2^TAU must stay <= 448");
   static constexpr uint32_t A_FMT = (ELEM == kBF16) ? 1u : 0u;  // bf16=1, f16=0, e4m3=0
   static constexpr uint32_t IDESC_QK = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN);
   // Early Q K^T: keys QK_SPLIT.. of the next tile land on S columns that P
@@ -256,6 +261,24 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int nkv, int off) {
 // q_period) and, when prm.splits > 1, units cover runs of key tiles and
 // write fp32 partial results.  Without it every row is its own position and
 // a unit covers the whole key range.
+// Multiplies this thread's OCOLS columns of O in TMEM by alpha.  Taken only
+// when a row maximum of the warp rose past the lazy threshold, so it is kept
+// out of line: its registers then do not weigh on the softmax's main path
+// (measured +1.3% at N = 16384 bf16, neutral elsewhere).
+template <int OCOLS>
+__device__ __noinline__ void rescale_o_cols(uint32_t o_addr, float alpha) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < OCOLS; c0 += 32) {
+    uint32_t u[32];
+    tmem_ld32(o_addr + c0, u);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+    tmem_st32(o_addr + c0, u);
+  }
+  tmem_wait_st();
+}
+
 template <int ELEM, int D, bool CAUSAL, bool SPLIT, int VAR = 0>
 __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -883,7 +906,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       }
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.0f;       // row sum over this thread's key columns
-      float v_mult = 1.0f;      // FP8: max_j s_Vj / 2^8
+      float v_mult = 1.0f;      // FP8: max_j s_Vj / P8_SCALE
       const int bh_blk = bh * prm.nblk;          // Q descale blocks of this head
       const int kv_blk = w.kvh * prm.nblk_k;     // K/V descale blocks
       float qds = 1.0f, vmax = 1.0f;
@@ -902,7 +925,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
       // loads for tile j+1 are issued when S(j) arrives, the factors are
       // formed after P(j) has been handed over.
       //   f_k:   q-block descale x k-block descale (multiplies the scale)
-      //   f_lpv: log2 of P~'s V-block factor 2^6 * s_Vj / max s_V
+      //   f_lpv: log2 of P~'s V-block factor 2^5 * s_Vj / max s_V
       //   f_inv: that factor's reciprocal (undoes it in the row sum)
       float f_k = 1.0f, f_lpv = 0.0f, f_inv = 1.0f;
       float kd_next = 1.0f, vd_next = 1.0f;
@@ -1173,17 +1196,7 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
             if (!consume_o(gj - 1)) { ok = false; break; }
             tc_fence_after();
           }
-          const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + t * D + ocol0;
-#pragma unroll 1
-          for (int c0 = 0; c0 < OCOLS; c0 += 32) {
-            uint32_t u[32];
-            tmem_ld32(o_addr + c0, u);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(o_addr + c0, u);
-          }
-          tmem_wait_st();
+          rescale_o_cols<OCOLS>(tmem + lane_addr + C::O_COL0 + t * D + ocol0, alpha);
         }
         // P = 2^(s*cj - m) and the row sum (four packed pairs of chains),
         // packed and written back over S a quarter (32 keys) at a time, so
