@@ -263,3 +263,39 @@ def test_fp8_error_study(fa, sigma):
         os.makedirs(out, exist_ok=True)
         with open(os.path.join(out, f"fp8_error_study_sigma{int(sigma)}.json"), "w") as f:
             json.dump({"sigma": sigma, "rows_per_head": 64, "rmse_vs_fp64_oracle": report}, f, indent=1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_fp8_rising_maxima(fa, causal):
+    # keys scaled up along the sequence (0.2x to 3x) with scale 0.5: every
+    # row's running maximum rises past the lazy threshold many times, so O is
+    # rescaled in TMEM again and again and P~ runs up to the top of the E4M3
+    # range.  LSE comes from fp32 p, m and l and must match the oracle on the
+    # dequantised inputs to 1e-3; O may differ from it only by the E4M3
+    # rounding of P~ -- at most half an E4M3 step of each weight, 2^-4
+    # relative for normal values (at most 2^-4 of max|V| on O, as l >= 1) and
+    # 2^-10 absolute in P~ units for subnormal ones (at most N * 2^-15 of
+    # 448 * max s_V ~ max|V|) -- plus its bf16 output rounding.
+    B, H, N, d = 1, 2, 1024, 128
+    q, k, v = (gen.normal((B, H, N, d), 2200, s) for s in range(3))
+    k = (k * np.linspace(0.2, 3.0, N, dtype=np.float32)[None, None, :, None]).astype(np.float32)
+    signs = gen.hadamard_signs(d, 4)
+    qc, qs = oracle.quant_e4m3(q, signs=signs)
+    kc, ks = oracle.quant_e4m3(k, signs=signs)
+    vc, vs = oracle.quant_e4m3(v)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o, lse = fa.fwd_fp8(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=causal, scale=0.5)
+    fa.check_device_error()
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    qd, kd, vd = oracle.dequant_e4m3(qc, qs), oracle.dequant_e4m3(kc, ks), oracle.dequant_e4m3(vc, vs)
+    o_dq, l_dq = oracle.attn_fwd(qd, kd, vd, causal=causal, scale=0.5)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert np.abs(lse - l_dq).max() <= 1e-3
+    # the maxima really rise by many lazy-threshold steps along the rows
+    s_end = 0.5 * math.log2(math.e) * np.einsum("bhd,bhnd->bhn", qd[:, :, -1], kd).max()
+    s_start = 0.5 * math.log2(math.e) * np.einsum("bhd,bhnd->bhn", qd[:, :, -1], kd[:, :, :128]).max()
+    assert s_end - s_start > 4 * 3.8
+    bound = (2.0 ** -4 * np.abs(vd).max() + N * 2.0 ** -15 * 448 * float(vs.max())) * 1.05 \
+        + 2.0 ** -8 * np.abs(o_dq).max()
+    assert np.abs(o - o_dq).max() <= bound, (np.abs(o - o_dq).max(), bound)
