@@ -55,19 +55,21 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 // Streams and events of the host-buffer path (fa_fwd_host), created once
-// per device on first use: two host->device copy streams, a compute stream
-// and a device->host copy stream, fanned out from and joined back into the
+// per device on first use: two host->device copy streams, two compute
+// streams (consecutive chunks alternate, so that a chunk's kernel can start
+// on the SMs the previous chunk's last units leave free) and a
+// device->host copy stream, fanned out from and joined back into the
 // caller's stream with events on every call.
-constexpr int kHostChunks = 4;
+constexpr int kHostChunks = 16;
 struct HostPipe {
   bool ready = false;
   cudaStream_t h2d[2] = {nullptr, nullptr};
-  cudaStream_t comp = nullptr;
+  cudaStream_t comp[2] = {nullptr, nullptr};
   cudaStream_t d2h = nullptr;
   cudaEvent_t start = nullptr;
   cudaEvent_t copied[kHostChunks] = {};
   cudaEvent_t computed[kHostChunks] = {};
-  cudaEvent_t done[4] = {};
+  cudaEvent_t done[5] = {};
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
@@ -406,14 +408,14 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
   HostPipe& P = g_pipe[dev];
   if (!P.ready) {
     bool ok = true;
-    for (auto* sp : {&P.h2d[0], &P.h2d[1], &P.comp, &P.d2h})
+    for (auto* sp : {&P.h2d[0], &P.h2d[1], &P.comp[0], &P.comp[1], &P.d2h})
       ok = ok && cudaStreamCreateWithFlags(sp, cudaStreamNonBlocking) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; i < kHostChunks; ++i) {
       ok = ok && cudaEventCreateWithFlags(&P.copied[i], cudaEventDisableTiming) == cudaSuccess;
       ok = ok && cudaEventCreateWithFlags(&P.computed[i], cudaEventDisableTiming) == cudaSuccess;
     }
-    for (int i = 0; i < 4; ++i) ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 5; ++i) ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) return FA_ERR_CUDA;
     P.ready = true;
   }
@@ -437,7 +439,7 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
   // fan out from the caller's stream
   if (cudaEventRecord(P.start, stream) != cudaSuccess) return FA_ERR_CUDA;
   fa_status result = FA_OK;
-  for (cudaStream_t s : {P.h2d[0], P.h2d[1], P.comp, P.d2h})
+  for (cudaStream_t s : {P.h2d[0], P.h2d[1], P.comp[0], P.comp[1], P.d2h})
     if (cudaStreamWaitEvent(s, P.start, 0) != cudaSuccess) result = FA_ERR_CUDA;
   // chunks of whole key/value heads (each with its g query heads): the
   // copies of chunk c+1 run while chunk c computes and chunk c-1 copies back
@@ -445,7 +447,13 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
   // chunk's LSE rows start 16-byte aligned (g * Nq * step rows of 4 bytes)
   const int64_t rows = g * Nq;
   const int64_t step = (rows % 4 == 0) ? 1 : (rows % 2 == 0) ? 2 : 4;
-  const int64_t nch = BHkv < kHostChunks ? BHkv : kHostChunks;
+  // 4 chunks, or up to 16 when every chunk still holds a wave of units or
+  // more: the first chunk's copy in and the last one's copy out are what the
+  // overlap leaves exposed
+  const int64_t units = BHkv * ((g * Nq + 255) / 256);
+  int64_t nch = units / (int64_t)device_sm_count(dev);
+  nch = nch < 4 ? 4 : nch > kHostChunks ? kHostChunks : nch;
+  if (nch > BHkv) nch = BHkv;
   for (int64_t c = 0; c < nch && result == FA_OK; ++c) {
     const int64_t j0 = (BHkv * c / nch) / step * step;
     const int64_t j1 = (c + 1 == nch) ? BHkv : (BHkv * (c + 1) / nch) / step * step;
@@ -458,18 +466,19 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
             cudaSuccess ||
         cudaMemcpyAsync(vd + j0 * kv_row, vh + j0 * kv_row, (size_t)(nj * kv_row), cudaMemcpyHostToDevice, hs) !=
             cudaSuccess ||
-        cudaEventRecord(P.copied[c], hs) != cudaSuccess || cudaStreamWaitEvent(P.comp, P.copied[c], 0) != cudaSuccess) {
+        cudaEventRecord(P.copied[c], hs) != cudaSuccess ||
+        cudaStreamWaitEvent(P.comp[c & 1], P.copied[c], 0) != cudaSuccess) {
       result = FA_ERR_CUDA;
       break;
     }
     // the chunk as nj batches of one key/value head and its g query heads
     st = fa_fwd_gqa(qd + j0 * q_row, kd + j0 * kv_row, vd + j0 * kv_row, od + j0 * q_row, ld + j0 * g * Nq, nj, g,
-                    1, Nq, Nk, d, causal, scale, dtype, P.comp);
+                    1, Nq, Nk, d, causal, scale, dtype, P.comp[c & 1]);
     if (st != FA_OK) {
       result = st;
       break;
     }
-    if (cudaEventRecord(P.computed[c], P.comp) != cudaSuccess ||
+    if (cudaEventRecord(P.computed[c], P.comp[c & 1]) != cudaSuccess ||
         cudaStreamWaitEvent(P.d2h, P.computed[c], 0) != cudaSuccess ||
         cudaMemcpyAsync(oh + j0 * q_row, od + j0 * q_row, (size_t)(nj * q_row), cudaMemcpyDeviceToHost, P.d2h) !=
             cudaSuccess ||
@@ -482,8 +491,8 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
   // join back into the caller's stream -- after an error too, so that work
   // the caller enqueues next never runs ahead of copies that still read or
   // write its host buffers
-  cudaStream_t all[4] = {P.h2d[0], P.h2d[1], P.comp, P.d2h};
-  for (int i = 0; i < 4; ++i)
+  cudaStream_t all[5] = {P.h2d[0], P.h2d[1], P.comp[0], P.comp[1], P.d2h};
+  for (int i = 0; i < 5; ++i)
     if (cudaEventRecord(P.done[i], all[i]) != cudaSuccess || cudaStreamWaitEvent(stream, P.done[i], 0) != cudaSuccess)
       if (result == FA_OK) result = FA_ERR_CUDA;
   return result;

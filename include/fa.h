@@ -143,9 +143,11 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o
  * device, runs the attention kernel and copies o and lse back, in chunks of
  * whole key/value heads (each with its query heads), so that the copies of
  * one chunk overlap the kernel of the previous one and the copies back of
- * the one before (two host->device streams, a compute stream and a
- * device->host stream, created once per device and joined to `stream` with
- * events; nothing is allocated per call).
+ * the one before (4 chunks, or up to 16 when each still holds a wave of
+ * work units; two host->device streams, two compute streams that
+ * consecutive chunks alternate between, and a device->host stream, created
+ * once per device and joined to `stream` with events; nothing is allocated
+ * per call).
  *   q_host, o_host  [B, Hq, Nq, d]   bf16 or fp16 (dtype), HOST memory
  *   k_host, v_host  [B, Hkv, Nk, d]  same dtype, HOST memory
  *   lse_host        [B, Hq, Nq] fp32, HOST memory
