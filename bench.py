@@ -488,9 +488,10 @@ ABLATE_VARIANTS = {0: "shipped kernel", 1: "split softmax (two warpgroups per Q 
                    8: "one Q tile per CTA, S double-buffered (no two-tile alternation)",
                    16: "no work stealing", 32: "separate P (Q K^T of the next tile starts once S is read)",
                    64: "polynomial exponentials on the FMA pipe for 1/8 (d=128 bf16) or 3/8 (FP8, d=64) of P",
-                   128: "early partial Q K^T (keys beyond P's columns issued at P's first half)"}
-ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64, 128), (False, True, 128): (0, 1, 8, 16),
-                (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128), (False, False, 64): (0, 32, 64, 128),
+                   128: "early partial Q K^T (keys beyond P's columns issued at P's first half)",
+                   256: "direct O stores from registers (no staging boxes, no bulk tensor stores)"}
+ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, True, 128): (0, 1, 8, 16, 256),
+                (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, False, 64): (0, 32, 64, 128, 256),
                 (False, True, 64): (0, 32)}
 
 

@@ -241,6 +241,9 @@ fa_status internal_prepare_fwd(const void* q, const void* k, const void* v, void
   if ((st = encode_map(&L.q, q, dt, es, B * Hq, Nq, d)) != FA_OK) return st;
   if ((st = encode_map(&L.k, k, dt, es, B * Hkv, Nk, d)) != FA_OK) return st;
   if ((st = encode_map(&L.v, v, dt, es, B * Hkv, Nk, d)) != FA_OK) return st;
+  // O (bf16 for the FP8 path) in 64-column x 32-row boxes: one per softmax warp
+  const CUtensorMapDataType dt_o = fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
+  if ((st = encode_map(&L.o, o, dt_o, 2, B * Hq, Nq, d, 32)) != FA_OK) return st;
   L.prm.o = o;
   L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   L.prm.lse = lse;
@@ -323,6 +326,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   if ((st = encode_map(&L.q, q, dt, 2, p.BHp, p.Np, d)) != FA_OK) return st;
   if ((st = encode_map(&L.k, k, dt, 2, p.BHp, Nk, d)) != FA_OK) return st;
   if ((st = encode_map(&L.v, v, dt, 2, p.BHp, Nk, d)) != FA_OK) return st;
+  if ((st = encode_map(&L.o, o, dt, 2, p.BHp, p.Np, d, 32)) != FA_OK) return st;
   L.prm.o = o;
   L.prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   L.prm.lse = lse;

@@ -32,10 +32,13 @@
 // input through a ring of shared-memory slots with TMA (each slot is half a
 // 128-row block: 32-float x 64-row boxes, 128-byte swizzle, rows past N read
 // as zero), with full / empty mbarriers; a group of warps takes a block in
-// one pass, 8 or 16 rows per warp (two groups on alternate blocks).  A row is spread over 4 lanes (lane / 8 picks
-// the quarter, lane % 8 the row), chosen so that the 8 lanes of each
-// shared-memory phase read 8 different rows and the swizzle puts them in
-// different banks.  The rotated rows stay in registers: each warp frees its
+// one pass (two groups on alternate blocks).  A row is spread over 4 lanes
+// (lane / 8 picks the quarter, lane % 8 the row; 8 or 16 rows per warp),
+// chosen so that the 8 lanes of each shared-memory phase read 8 different
+// rows and the swizzle puts them in different banks; with the rotation at
+// d = 128 each lane holds a whole row instead (32 rows per warp, 8 warps),
+// so that no stage of the butterfly crosses lanes, and 8 consecutive lanes
+// are again 8 rows in different banks.  The rotated rows stay in registers: each warp frees its
 // slot as soon as it has read it, takes the block maximum across the 16 warps
 // through a predicate-AND barrier (which also lets a warp that gave up stop
 // the others), and encodes from registers.  HBM-bound: 4 bytes read and 1
@@ -52,29 +55,41 @@
 namespace fa {
 namespace {
 
-template <int D>
+template <int D, int LPR_ = 4>
 struct QCfg {
-  // Warps per CTA.  The rotation and the exact rounding are latency-bound
-  // chains per row, so the warps in flight matter: d = 64 runs 32 warps of
-  // 64 registers (measured 13% faster with the rotation than 16 warps); at
-  // d = 128 that many warps spill and leave 2 ring slots per group instead
-  // of 3 (measured slower), so it keeps 16 warps with two row sets each;
-  // d = 256 runs 16 warps (its rows need 128 registers).
-  static constexpr int NW = (D == 64) ? 32 : 16;
+  // Lanes per row: 4, or 1 for the rotation at d = 128 (the launch picks).
+  // One lane per row keeps every stage of the butterfly inside a lane (with
+  // a row over 4 lanes the two stages that cross lanes took about a third
+  // of the kernel's time, measured: 51.8 -> 43.7 us at B=4 H=16 N=4096),
+  // but its 128-register rows leave 8 warps per SM, too few to cover the
+  // memory latency without the butterfly's work in between (block scales
+  // without the rotation: 32.8 us with 4 lanes per row, 36.9 with 1).
+  static constexpr int LPR = (D == 128) ? LPR_ : 4;
+  static constexpr int RPW = 32 / LPR;           // rows of a warp's row set
+  // Warps per CTA.  With 4 lanes per row the rotation and the exact rounding
+  // are latency-bound chains per row, so the warps in flight matter: d = 64
+  // runs 32 warps of 64 registers (measured 13% faster with the rotation
+  // than 16 warps); d = 256 runs 16 warps (its rows need 128 registers).
+  // d = 128 (a row per lane, 128 independent elements each) runs 8.
+  static constexpr int NW = (D == 64) ? 32 : (LPR == 1) ? 8 : 16;
   static constexpr int THREADS = 32 * NW;
   // Two groups work on alternate blocks, each with its own ring and
   // barrier, so that one group's wait for its block maximum overlaps the
   // other group's work (d = 256: one group; its rows do not fit twice).
   static constexpr int NG = (D == 256) ? 1 : 2;
   static constexpr int WG = NW / NG;             // warps per group
-  static constexpr int RS = 128 / (8 * WG);      // 8-row sets per warp and block
+  static constexpr int RS = 128 / (RPW * WG);    // row sets per warp and block
   static_assert(RS == 1 || RS == 2, "a group covers a 128-row block");
-  static constexpr int E = D / 4;                // elements of a row per lane
+  static constexpr int E = D / LPR;              // elements of a row per lane
   static constexpr int G = E < 32 ? E : 32;      // contiguous run of a lane's elements
   static constexpr int BOXES = D / 32;           // 32-float boxes per row
   static constexpr int SLOT_ROWS = 64;           // half a block per slot
   static constexpr int BOX_BYTES = SLOT_ROWS * 128;
   static constexpr int SLOT_BYTES = BOXES * BOX_BYTES;
+  // warps that read one slot: every warp of the group (two row sets: both
+  // halves of each block) or the warps covering one half
+  static constexpr int READERS = (RS == 2) ? WG : SLOT_ROWS / RPW;
+  static constexpr int MASKW = (E / 32 > 2) ? E / 32 : 2;  // sign-bit words of a lane's elements
   // Slots per group.  With one row set per warp, a warp reads one half of
   // each block, so each slot must serve one half only and the count is even:
   // position q goes to slot q % NSG and to half q % 2.  (An odd count would
@@ -111,16 +126,21 @@ struct QuantParams {
   SignBits sg;
   int N, nblk, total;  // rows per head, blocks per head, blocks in all
   int rot;
+  int x8_vec32;        // x8 is 32-byte aligned
   float rinv;
   int rope;
   int drop_pos;
 };
 
 // Index within the row of a lane's local element e (quarter p of the row).
-template <int D>
+template <int D, int LPR>
 __device__ __forceinline__ int elem_of(int e, int p) {
-  constexpr int G = QCfg<D>::G;
-  return (e & (G - 1)) + G * p + 128 * (e >> 5);
+  if constexpr (QCfg<D, LPR>::LPR == 1) {
+    return e;
+  } else {
+    constexpr int G = QCfg<D, LPR>::G;
+    return (e & (G - 1)) + G * p + 128 * (e >> 5);
+  }
 }
 
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float2 lo, float2 hi) {
@@ -164,15 +184,15 @@ __device__ __forceinline__ uint32_t encode4(const float* v, float2 rh, float2 rl
   return settle4(v[0], v[1], v[2], v[3], ch, cl, s);
 }
 
-template <int D>
-__device__ __forceinline__ void rope_row(float (&v)[QCfg<D>::E], int p, const float* __restrict__ c,
+template <int D, int LPR>
+__device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, const float* __restrict__ c,
                                          const float* __restrict__ s, int mode) {
-  constexpr int E = QCfg<D>::E;
+  constexpr int E = QCfg<D, LPR>::E;
   if (mode == 1) {
     // pairs (2i, 2i+1): adjacent elements of one lane, angle elem / 2
 #pragma unroll
     for (int e0 = 0; e0 < E; e0 += 8) {
-      const int a0 = elem_of<D>(e0, p) >> 1;
+      const int a0 = elem_of<D, LPR>(e0, p) >> 1;
       const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
       const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
       const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
@@ -184,11 +204,25 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D>::E], int p, const fl
       }
     }
   } else if (mode == 2) {
-    if constexpr (D == 256) {
+    if constexpr (QCfg<D, LPR>::LPR == 1) {
+      // pairs (i, i + D/2): both in this lane
+#pragma unroll
+      for (int e0 = 0; e0 < D / 2; e0 += 4) {
+        const float4 C = __ldg(reinterpret_cast<const float4*>(c + e0));
+        const float4 S = __ldg(reinterpret_cast<const float4*>(s + e0));
+        const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x = v[e0 + k], y = v[e0 + k + D / 2];
+          v[e0 + k] = __fsub_rn(__fmul_rn(x, cv[k]), __fmul_rn(y, sv[k]));
+          v[e0 + k + D / 2] = __fadd_rn(__fmul_rn(x, sv[k]), __fmul_rn(y, cv[k]));
+        }
+      }
+    } else if constexpr (D == 256) {
       // pairs (i, i + 128): local elements e and e + 32 of one lane
 #pragma unroll
       for (int e0 = 0; e0 < 32; e0 += 4) {
-        const int a0 = elem_of<D>(e0, p);
+        const int a0 = elem_of<D, LPR>(e0, p);
         const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
         const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
         const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
@@ -204,7 +238,7 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D>::E], int p, const fl
       const bool first = (p & 2) == 0;
 #pragma unroll
       for (int e0 = 0; e0 < E; e0 += 4) {
-        const int a0 = elem_of<D>(e0, p & 1);
+        const int a0 = elem_of<D, LPR>(e0, p & 1);
         const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
         const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
         const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
@@ -220,14 +254,38 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D>::E], int p, const fl
   }
 }
 
-// Sign flip and Walsh-Hadamard butterfly of a row spread over the 4 lanes
-// lane % 8 + 8 * {0, 1, 2, 3}; strides in ascending order.
-template <int D>
-__device__ __forceinline__ void rotate_row(float (&v)[QCfg<D>::E], int p, const uint32_t (&smask)[2]) {
-  constexpr int E = QCfg<D>::E, G = QCfg<D>::G;
+// Sign flip and Walsh-Hadamard butterfly of a row, held by one lane or
+// spread over the 4 lanes lane % 8 + 8 * {0, 1, 2, 3}; strides in ascending
+// order.
+template <int D, int LPR>
+__device__ __forceinline__ void rotate_row(float (&v)[QCfg<D, LPR>::E], int p,
+                                           const uint32_t (&smask)[QCfg<D, LPR>::MASKW]) {
+  constexpr int E = QCfg<D, LPR>::E, G = QCfg<D, LPR>::G;
 #pragma unroll
   for (int e = 0; e < E; ++e)
     v[e] = __uint_as_float(__float_as_uint(v[e]) ^ ((smask[e >> 5] << (31 - (e & 31))) & 0x80000000u));
+  if constexpr (QCfg<D, LPR>::LPR == 1) {
+    // every stride inside the lane: 1 scalar, then 2 .. D/2 in packed pairs
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float a = v[e], b = v[e + 1];
+      v[e] = __fadd_rn(a, b);
+      v[e + 1] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int h = 2; h < E; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        if (!(e & h)) {
+          const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + h], v[e + h + 1]);
+          const float2 s = add2(a, b), d = sub2(a, b);
+          v[e] = s.x; v[e + 1] = s.y;
+          v[e + h] = d.x; v[e + h + 1] = d.y;
+        }
+      }
+    }
+    return;
+  }
   // stride 1 (inside a lane, scalar)
 #pragma unroll
   for (int e = 0; e < E; e += 2) {
@@ -276,10 +334,10 @@ __device__ __forceinline__ void rotate_row(float (&v)[QCfg<D>::E], int p, const 
 // MODE 0: per-block scale.  MODE 1: per-tensor maximum into *ws (one atomic
 // max per CTA).  MODE 2: per-tensor encode with the maximum in *ws.
 // MODE 3: per-block maxima to ws[block] (no atomics).
-template <int D, int MODE, bool ROPE>
-__global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
+template <int D, int MODE, bool ROPE, int LPR>
+__global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
     quant_e4m3_kernel(const __grid_constant__ CUtensorMap map, const QuantParams prm) {
-  using C = QCfg<D>;
+  using C = QCfg<D, LPR>;
   constexpr int E = C::E, RS = C::RS, NSG = C::NSG;
   extern __shared__ __align__(1024) uint8_t qsmem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,13 +347,13 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
   const int G = (int)gridDim.x;
   const int grp = warp / C::WG;     // group of this warp
   const int wg = warp % C::WG;      // warp within the group
-  const int p = lane >> 3;          // quarter of the row held by this lane
-  const int rl = lane & 7;          // row within the warp's 8-row set
+  const int p = (C::LPR == 1) ? 0 : lane >> 3;       // quarter of the row held by this lane
+  const int rl = (C::LPR == 1) ? lane : lane & 7;    // row within the warp's row set
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], 8);  // the 8 warps that read a slot's rows
+      mbar_init(&sh->empty[s], C::READERS);  // the warps that read a slot's rows
       sh->last_pos[s] = -1;
     }
     sh->abort_flag = 0;
@@ -308,8 +366,10 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
   // it = g, g + NG, g + 2 NG, ...  Its j-th block fills group positions 2j
   // (rows 0..63) and 2j + 1 (rows 64..127) of the group's ring of NSG slots.
   // Row set k of this warp: half hk, row r_slot within the half.
-  auto half_of = [&](int k) -> int { return (RS == 2) ? k : wg / 8; };
-  const int r_slot = (wg % 8) * 8 + rl;
+  constexpr int WPH = C::SLOT_ROWS / C::RPW;   // warps covering one half block
+  auto half_of = [&](int k) -> int { return (RS == 2) ? k : wg / WPH; };
+  const int r_slot = (wg % WPH) * C::RPW + rl;
+  const int swz = r_slot & 7;                   // the 128-byte swizzle's row key
   uint8_t* gring = ring + grp * NSG * C::SLOT_BYTES;
   uint64_t* gfull = &sh->full[grp * NSG];
   uint64_t* gempty = &sh->empty[grp * NSG];
@@ -354,12 +414,14 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
 
   // sign bits of this lane's elements (selected, not indexed, so that the
   // parameter block stays out of local memory)
-  uint32_t smask[2] = {0u, 0u};
+  uint32_t smask[C::MASKW] = {};
   if (prm.rot) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t w = prm.sg.w[k];
-      if constexpr (D == 64) {
+      if constexpr (C::LPR == 1) {
+        if (k < C::MASKW) smask[k] = w;
+      } else if constexpr (D == 64) {
         if (k == (p >> 1)) smask[0] = (w >> (16 * (p & 1))) & 0xffffu;
       } else {
         if (k == p) smask[0] = w;
@@ -393,9 +455,9 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
         const uint8_t* src = gring + slot * C::SLOT_BYTES + r_slot * 128;
 #pragma unroll
         for (int e = 0; e < E; e += 4) {
-          const int i = elem_of<D>(e, p);
+          const int i = elem_of<D, LPR>(e, p);
           const int ch = (i & 31) >> 2;
-          const float4 t = *reinterpret_cast<const float4*>(src + (i >> 5) * C::BOX_BYTES + ((ch ^ rl) << 4));
+          const float4 t = *reinterpret_cast<const float4*>(src + (i >> 5) * C::BOX_BYTES + ((ch ^ swz) << 4));
           v[k][e] = t.x; v[k][e + 1] = t.y; v[k][e + 2] = t.z; v[k][e + 3] = t.w;
         }
         __syncwarp();
@@ -415,9 +477,9 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
         }
         if constexpr (ROPE) {
           const size_t nr = (size_t)(n < N ? n : N - 1) * (D / 2);
-          rope_row<D>(v[k], p, prm.rcos + nr, prm.rsin + nr, prm.rope);
+          rope_row<D, LPR>(v[k], p, prm.rcos + nr, prm.rsin + nr, prm.rope);
         }
-        if (prm.rot) rotate_row<D>(v[k], p, smask);
+        if (prm.rot) rotate_row<D, LPR>(v[k], p, smask);
 #pragma unroll
         for (int e = 0; e < E; e += 2) am = max3f(am, fabsf(v[k][e]), fabsf(v[k][e + 1]));
       }
@@ -478,10 +540,16 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, 1)
       const int n = blk * 128 + half_of(k) * C::SLOT_ROWS + r_slot;
       if (n < N) {
         uint8_t* row = prm.x8 + ((size_t)bh * N + n) * D;
+        if (C::LPR == 1 && prm.x8_vec32) {
+          // a whole row per lane: 32-byte stores (full sectors)
 #pragma unroll
-        for (int jj = 0; jj < E / 16; ++jj)
-          *reinterpret_cast<uint4*>(row + elem_of<D>(16 * jj, p)) =
-              make_uint4(words[4 * jj], words[4 * jj + 1], words[4 * jj + 2], words[4 * jj + 3]);
+          for (int jj = 0; jj < E / 32; ++jj) st_global_v8(row + 32 * jj, words + 8 * jj);
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < E / 16; ++jj)
+            *reinterpret_cast<uint4*>(row + elem_of<D, LPR>(16 * jj, p)) =
+                make_uint4(words[4 * jj], words[4 * jj + 1], words[4 * jj + 2], words[4 * jj + 3]);
+        }
       }
     }
     if (wg == 0 && lane == 0) prm.descale[b] = __fmul_rn(s, prm.rinv);
@@ -534,10 +602,10 @@ int sm_count_cached() {
   return sms[dev];
 }
 
-template <int D, int MODE, bool ROPE>
+template <int D, int MODE, bool ROPE, int LPR>
 cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
-  using C = QCfg<D>;
-  auto kern = quant_e4m3_kernel<D, MODE, ROPE>;
+  using C = QCfg<D, LPR>;
+  auto kern = quant_e4m3_kernel<D, MODE, ROPE, LPR>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -559,6 +627,7 @@ cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
   prm.nblk = L.nblk;
   prm.total = L.BH * L.nblk;
   prm.rot = L.rot;
+  prm.x8_vec32 = (reinterpret_cast<uintptr_t>(L.x8) & 31u) == 0;
   prm.rinv = L.rinv;
   prm.rope = L.rope;
   prm.drop_pos = drop_pos;
@@ -568,9 +637,18 @@ cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
   return cudaGetLastError();
 }
 
+template <int D, int MODE, int LPR>
+cudaError_t launch_rope(const QuantLaunch& L, float* ws, int drop_pos) {
+  return L.rope ? launch_one<D, MODE, true, LPR>(L, ws, drop_pos) : launch_one<D, MODE, false, LPR>(L, ws, drop_pos);
+}
+
+// one lane per row for the rotation at d = 128, 4 otherwise
 template <int D, int MODE>
 cudaError_t launch_mode(const QuantLaunch& L, float* ws, int drop_pos) {
-  return L.rope ? launch_one<D, MODE, true>(L, ws, drop_pos) : launch_one<D, MODE, false>(L, ws, drop_pos);
+  if constexpr (D == 128) {
+    if (L.rot) return launch_rope<D, MODE, 1>(L, ws, drop_pos);
+  }
+  return launch_rope<D, MODE, 4>(L, ws, drop_pos);
 }
 
 template <int D>

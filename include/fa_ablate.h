@@ -27,9 +27,13 @@
  *       (written over S from column 0) does not use are multiplied as soon as
  *       the first half of P arrives, the remaining keys after the second half
  *       (two narrower MMAs instead of one of N = 128)
+ *   256 direct O stores: each thread writes its own row of O from registers
+ *       (32-byte vector stores, 32 rows per warp instruction) instead of
+ *       staging 64-column boxes in shared memory for bulk tensor stores; the
+ *       ring keeps the slot the boxes take (d = 128 16-bit: 5 slots, not 4)
  * Built instances: d = 128 bf16 non-causal and FP8 non-causal with codes
- * 0, 1, 2, 4, 8, 16, 64, 128; d = 128 bf16 causal with 0, 1, 8, 16; d = 64
- * bf16 non-causal with 0, 32, 64, 128 and causal with 0, 32.
+ * 0, 1, 2, 4, 8, 16, 64, 128, 256; d = 128 bf16 causal with 0, 1, 8, 16,
+ * 256; d = 64 bf16 non-causal with 0, 32, 64, 128, 256 and causal with 0, 32.
  *   variant      one of the codes above
  *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
  *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8

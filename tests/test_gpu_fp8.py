@@ -50,6 +50,38 @@ def test_quant_bit_exact(fa, d, N, rot, per_tensor):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quant_codes_16_byte_aligned(fa, d, per_tensor):
+    # the C ABI promises 16-byte alignment of the codes only: a buffer 16 bytes
+    # past a 32-byte boundary takes the 16-byte stores and must give the same
+    # codes as the oracle (with the rotation, every lane holding a whole row
+    # at d = 128)
+    import ctypes
+    x = gen.outliers((2, 3, 300, d), 70 + d)
+    signs = gen.hadamard_signs(d, 4)
+    codes_ref, ds_ref = oracle.quant_e4m3(x, signs=signs, per_tensor=per_tensor)
+    xd = torch.from_numpy(x).cuda()
+    buf = torch.zeros(x.size + 64, dtype=torch.uint8, device="cuda")
+    off = (16 - buf.data_ptr() % 32) % 32
+    assert (buf.data_ptr() + off) % 32 == 16
+    x8 = buf[off:off + x.size]
+    ds = torch.empty((2, 3, 3), dtype=torch.float32, device="cuda")
+    ws = torch.empty((1,), dtype=torch.float32, device="cuda")
+    keep = (ctypes.c_int8 * d)(*[int(v) for v in signs])
+    st = fa.lib().fa_quant_fp8(xd.data_ptr(), x8.data_ptr(), ds.data_ptr(), 2, 3, 300, d,
+                               ctypes.cast(keep, ctypes.c_void_p), int(per_tensor),
+                               ws.data_ptr() if per_tensor else None, torch.cuda.current_stream().cuda_stream)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    codes = x8.cpu().numpy().reshape(x.shape)
+    assert int((codes != codes_ref).sum()) == 0
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32))
+    # the bytes around the codes are untouched
+    assert int(buf[:off].sum()) == 0 and int(buf[off + x.size:].sum()) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_quant_many_blocks_per_cta(fa, d):
     # about seven 128-row blocks per CTA of the persistent grid, so the
     # shared-memory ring wraps several times, in every mode
