@@ -284,49 +284,49 @@ __device__ __forceinline__ void rotate_row(float (&v)[QCfg<D, LPR>::E], int p,
         }
       }
     }
-    return;
-  }
-  // stride 1 (inside a lane, scalar)
-#pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const float a = v[e], b = v[e + 1];
-    v[e] = __fadd_rn(a, b);
-    v[e + 1] = __fsub_rn(a, b);
-  }
-  // strides 2 .. G/2 (inside a lane, packed pairs)
-#pragma unroll
-  for (int h = 2; h < G; h <<= 1) {
+  } else {
+    // stride 1 (inside a lane, scalar)
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
-      if (!(e & h)) {
-        const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + h], v[e + h + 1]);
-        const float2 s = add2(a, b), d = sub2(a, b);
-        v[e] = s.x; v[e + 1] = s.y;
-        v[e + h] = d.x; v[e + h + 1] = d.y;
+      const float a = v[e], b = v[e + 1];
+      v[e] = __fadd_rn(a, b);
+      v[e + 1] = __fsub_rn(a, b);
+    }
+    // strides 2 .. G/2 (inside a lane, packed pairs)
+#pragma unroll
+    for (int h = 2; h < G; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        if (!(e & h)) {
+          const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + h], v[e + h + 1]);
+          const float2 s = add2(a, b), d = sub2(a, b);
+          v[e] = s.x; v[e + 1] = s.y;
+          v[e + h] = d.x; v[e + h + 1] = d.y;
+        }
       }
     }
-  }
-  // strides G and 2G: the other quarters of the row (lanes 8 and 16 apart);
-  // the lower index takes a + b, the upper b' - a' as RN(partner - own)
+    // strides G and 2G: the other quarters of the row (lanes 8 and 16 apart);
+    // the lower index takes a + b, the upper b' - a' as RN(partner - own)
 #pragma unroll
-  for (int m = 8; m <= 16; m <<= 1) {
-    const bool upper = (p & (m >> 3)) != 0;
-    const float2 sg2 = make_float2(upper ? -1.0f : 1.0f, upper ? -1.0f : 1.0f);
+    for (int m = 8; m <= 16; m <<= 1) {
+      const bool upper = (p & (m >> 3)) != 0;
+      const float2 sg2 = make_float2(upper ? -1.0f : 1.0f, upper ? -1.0f : 1.0f);
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], m), __shfl_xor_sync(0xffffffffu, v[e + 1], m));
-      const float2 r = fma2(make_float2(v[e], v[e + 1]), sg2, o);
-      v[e] = r.x; v[e + 1] = r.y;
+      for (int e = 0; e < E; e += 2) {
+        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], m), __shfl_xor_sync(0xffffffffu, v[e + 1], m));
+        const float2 r = fma2(make_float2(v[e], v[e + 1]), sg2, o);
+        v[e] = r.x; v[e + 1] = r.y;
+      }
     }
-  }
-  if constexpr (D == 256) {
-    // stride 128: local elements e and e + 32
+    if constexpr (D == 256) {
+      // stride 128: local elements e and e + 32
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + 32], v[e + 33]);
-      const float2 s = add2(a, b), d = sub2(a, b);
-      v[e] = s.x; v[e + 1] = s.y;
-      v[e + 32] = d.x; v[e + 33] = d.y;
+      for (int e = 0; e < 32; e += 2) {
+        const float2 a = make_float2(v[e], v[e + 1]), b = make_float2(v[e + 32], v[e + 33]);
+        const float2 s = add2(a, b), d = sub2(a, b);
+        v[e] = s.x; v[e + 1] = s.y;
+        v[e + 32] = d.x; v[e + 33] = d.y;
+      }
     }
   }
 }
