@@ -32,14 +32,14 @@
 // input through a ring of shared-memory slots with TMA (each slot is half a
 // 128-row block: 32-float x 64-row boxes, 128-byte swizzle, rows past N read
 // as zero), with full / empty mbarriers; a group of warps takes a block in
-// one pass (two groups on alternate blocks).  A row is spread over 4 lanes
+// one pass (two or three groups on alternate blocks).  A row is spread over 4 lanes
 // (lane / 8 picks the quarter, lane % 8 the row; 8 or 16 rows per warp),
 // chosen so that the 8 lanes of each shared-memory phase read 8 different
 // rows and the swizzle puts them in different banks; with the rotation at
-// d = 128 each lane holds a whole row instead (32 rows per warp, 8 warps),
+// d = 128 each lane holds a whole row instead (32 rows per warp, 12 warps),
 // so that no stage of the butterfly crosses lanes, and 8 consecutive lanes
 // are again 8 rows in different banks.  The rotated rows stay in registers: each warp frees its
-// slot as soon as it has read it, takes the block maximum across the 16 warps
+// slot as soon as it has read it, takes the block maximum across its group's warps
 // through a predicate-AND barrier (which also lets a warp that gave up stop
 // the others), and encodes from registers.  HBM-bound: 4 bytes read and 1
 // written per element.
@@ -60,23 +60,26 @@ struct QCfg {
   // Lanes per row: 4, or 1 for the rotation at d = 128 (the launch picks).
   // One lane per row keeps every stage of the butterfly inside a lane (with
   // a row over 4 lanes the two stages that cross lanes took about a third
-  // of the kernel's time, measured: 51.8 -> 43.7 us at B=4 H=16 N=4096),
-  // but its 128-register rows leave 8 warps per SM, too few to cover the
-  // memory latency without the butterfly's work in between (block scales
-  // without the rotation: 32.8 us with 4 lanes per row, 36.9 with 1).
+  // of the kernel's time, measured: 51.8 -> 37.5 us at B=4 H=16 N=4096),
+  // but its 128-register rows leave at most 12 warps per SM, too few to
+  // cover the memory latency without the butterfly's work in between
+  // (block scales without the rotation: 32.8 us with 4 lanes per row, 36.9
+  // with 1 lane per row and 8 warps).
   static constexpr int LPR = (D == 128) ? LPR_ : 4;
   static constexpr int RPW = 32 / LPR;           // rows of a warp's row set
   // Warps per CTA.  With 4 lanes per row the rotation and the exact rounding
   // are latency-bound chains per row, so the warps in flight matter: d = 64
   // runs 32 warps of 64 registers (measured 13% faster with the rotation
   // than 16 warps); d = 256 runs 16 warps (its rows need 128 registers).
-  // d = 128 (a row per lane, 128 independent elements each) runs 8.
-  static constexpr int NW = (D == 64) ? 32 : (LPR == 1) ? 8 : 16;
+  // d = 128 with one row per lane (128 independent elements each) runs 12
+  // in three groups of 4 (168 registers; 8 warps of 254 were 17% slower).
+  static constexpr int NW = (D == 64) ? 32 : (LPR == 1) ? 12 : 16;
   static constexpr int THREADS = 32 * NW;
-  // Two groups work on alternate blocks, each with its own ring and
-  // barrier, so that one group's wait for its block maximum overlaps the
-  // other group's work (d = 256: one group; its rows do not fit twice).
-  static constexpr int NG = (D == 256) ? 1 : 2;
+  // Two (one row per lane: three) groups work on alternate blocks, each with
+  // its own ring and barrier, so that one group's wait for its block maximum
+  // overlaps the other groups' work (d = 256: one group; its rows do not fit
+  // twice).
+  static constexpr int NG = (D == 256) ? 1 : (LPR == 1) ? 3 : 2;
   static constexpr int WG = NW / NG;             // warps per group
   static constexpr int RS = 128 / (RPW * WG);    // row sets per warp and block
   static_assert(RS == 1 || RS == 2, "a group covers a 128-row block");
@@ -534,10 +537,29 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
     const float2 rh2 = make_float2(rh, rh), rl2 = make_float2(rl_, rl_);
 #pragma unroll
     for (int k = 0; k < RS; ++k) {
+      const int n = blk * 128 + half_of(k) * C::SLOT_ROWS + r_slot;
+      if constexpr (C::LPR == 1) {
+        // a whole row per lane: 32 codes at a time, stored as they are made
+        uint8_t* row = prm.x8 + ((size_t)bh * N + (n < N ? n : 0)) * D;
+#pragma unroll
+        for (int jj = 0; jj < E / 32; ++jj) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) w8[q] = encode4(&v[k][32 * jj + 4 * q], rh2, rl2, se);
+          if (n < N) {
+            if (prm.x8_vec32) {
+              st_global_v8(row + 32 * jj, w8);
+            } else {
+              *reinterpret_cast<uint4*>(row + 32 * jj) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+              *reinterpret_cast<uint4*>(row + 32 * jj + 16) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+            }
+          }
+        }
+        continue;
+      }
       uint32_t words[E / 4];
 #pragma unroll
       for (int q = 0; q < E / 4; ++q) words[q] = encode4(&v[k][4 * q], rh2, rl2, se);
-      const int n = blk * 128 + half_of(k) * C::SLOT_ROWS + r_slot;
       if (n < N) {
         uint8_t* row = prm.x8 + ((size_t)bh * N + n) * D;
         if (C::LPR == 1 && prm.x8_vec32) {
