@@ -66,6 +66,8 @@ def _lib():
         lib.fa_splitkv_workspace_bytes.restype = i32
         lib.fa_quant_fp8_rope.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, i32, vp, i32, vp, vp]
         lib.fa_quant_fp8_rope.restype = i32
+        lib.fa_quant_fp8_qkv.argtypes = [vp] * 9 + [i64] * 6 + [vp, vp]
+        lib.fa_quant_fp8_qkv.restype = i32
         lib.fa_quant_fp8_per_tensor_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp]
         lib.fa_quant_fp8_per_tensor_noalloc.restype = i32
         lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i32, f32, i32, vp,
@@ -395,6 +397,48 @@ def quant_fp8(x: torch.Tensor, signs=None, per_tensor: bool = False, workspace: 
     _check(st, name)
     del keep
     return x8, ds
+
+
+def quant_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs=None, out=None):
+    """The FP8 inputs of one attention call (``fa_quant_fp8_qkv``): Q and K
+    with block scales after the rotation given by ``signs`` (or none), V with
+    block scales, the three on internal streams joined back into the current
+    stream.  q: fp32 [B, Hq, Nq, d]; k, v: fp32 [B, Hkv, Nk, d].  Returns
+    (q8, k8, v8, q_descale, k_descale, v_descale), each as ``quant_fp8``
+    would give it; ``out`` may supply those six tensors (written in place)."""
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or t.dim() != 4 \
+                or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{nm} must be a contiguous fp32 [B, H, N, d] CUDA tensor on q's device")
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or dk != d:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+    shapes_ds = [(B, Hq, (Nq + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS)] + \
+                [(B, Hkv, (Nk + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS)] * 2
+    if out is None:
+        outs = [torch.empty(t.shape, dtype=torch.uint8, device=q.device) for t in (q, k, v)]
+        ds = [torch.empty(sh, dtype=torch.float32, device=q.device) for sh in shapes_ds]
+    else:
+        outs, ds = list(out[:3]), list(out[3:])
+        for t, ref in zip(outs, (q, k, v)):
+            if t.dtype != torch.uint8 or tuple(t.shape) != tuple(ref.shape) or not t.is_contiguous() \
+                    or t.device != q.device:
+                raise ValueError("code outputs must be contiguous uint8 tensors shaped like q, k, v")
+        for t, sh in zip(ds, shapes_ds):
+            if t.dtype != torch.float32 or tuple(t.shape) != sh or not t.is_contiguous() or t.device != q.device:
+                raise ValueError(f"descale outputs must be contiguous fp32 {sh}")
+    sp = None
+    keep = None
+    if signs is not None:
+        keep = (ctypes.c_int8 * d)(*[int(s) for s in (signs.tolist() if hasattr(signs, "tolist") else signs)])
+        sp = ctypes.cast(keep, ctypes.c_void_p)
+    with torch.cuda.device(q.device):
+        st = _lib().fa_quant_fp8_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), *[t.data_ptr() for t in outs],
+                                     *[t.data_ptr() for t in ds], B, Hq, Hkv, Nq, Nk, d, sp, _stream(q))
+    _check(st, "fa_quant_fp8_qkv")
+    del keep
+    return outs[0], outs[1], outs[2], ds[0], ds[1], ds[2]
 
 
 def quant_fp8_per_tensor_noalloc(x: torch.Tensor, signs=None, x8: torch.Tensor | None = None,

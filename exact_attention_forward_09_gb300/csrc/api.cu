@@ -73,6 +73,19 @@ struct HostPipe {
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
+
+// Streams of fa_quant_fp8_qkv, created once per device on first use: the
+// three quantisations run one per stream, fanned out from and joined back
+// into the caller's stream, so that each launch's CTAs start on the SMs the
+// others' last CTAs leave free (one CTA per SM each).
+struct QkvPipe {
+  bool ready = false;
+  cudaStream_t s[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t start = nullptr;
+  cudaEvent_t done[3] = {};
+};
+std::mutex g_qkv_mu;
+QkvPipe g_qkv[kMaxDevices];
 std::atomic<int> g_inject{0};  // one-shot failure injection for the next attention launch
 std::atomic<int> g_inject_quant{0};  // ... and for the next quantiser call
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -527,34 +540,42 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, fl
 }
 
 namespace {
-fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
-                     const float* rope_cos, const float* rope_sin, int rope_layout, const int8_t* hadamard_signs,
-                     int per_tensor, float* workspace, cudaStream_t stream) {
+// Argument checks of one quantiser call, before any CUDA call (*empty:
+// nothing to do).
+fa_status quant_check(const float* x, const void* x8, const float* descale, int64_t B, int64_t H, int64_t N,
+                      int64_t d, const float* rope_cos, const float* rope_sin, int rope_layout,
+                      const int8_t* hadamard_signs, int per_tensor, const float* workspace, bool* empty) {
+  *empty = false;
   if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (per_tensor != 0 && per_tensor != 1) return FA_ERR_INVALID_ARG;
   if (rope_layout != 0 && rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (B == 0 || H == 0 || N == 0) {
+    *empty = true;
+    return FA_OK;
+  }
   if (rope_layout != 0 && (!rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin)))
     return FA_ERR_INVALID_ARG;
   if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x8) || ((uintptr_t)descale & 3u)) return FA_ERR_INVALID_ARG;
   if (per_tensor && (!workspace || ((uintptr_t)workspace & 3u))) return FA_ERR_INVALID_ARG;
+  if (hadamard_signs)
+    for (int64_t i = 0; i < d; ++i)
+      if (hadamard_signs[i] != 1 && hadamard_signs[i] != -1) return FA_ERR_INVALID_ARG;
   // 128-row blocks are numbered with int
   if (N > ((int64_t)1 << 31) - 128 || B * H > 0x7fffffffLL / ((N + 127) / 128)) return FA_ERR_UNSUPPORTED;
-  int dev = 0;
-  int* err = nullptr;
-  fa_status st = device_setup(&dev, &err);
-  if (st != FA_OK) return st;
+  return FA_OK;
+}
 
-  fa::QuantLaunch L;
+// The launch of a checked, non-empty quantiser call (after device_setup).
+fa_status quant_fill(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                     const float* rope_cos, const float* rope_sin, int rope_layout, const int8_t* hadamard_signs,
+                     int per_tensor, float* workspace, int* err, cudaStream_t stream, fa::QuantLaunch* out) {
+  fa::QuantLaunch& L = *out;
   std::memset(&L, 0, sizeof(L));
   if (hadamard_signs) {
-    for (int64_t i = 0; i < d; ++i) {
-      const int8_t sgn = hadamard_signs[i];
-      if (sgn != 1 && sgn != -1) return FA_ERR_INVALID_ARG;
-      if (sgn < 0) L.signs.w[i >> 5] |= 1u << (i & 31);
-    }
+    for (int64_t i = 0; i < d; ++i)
+      if (hadamard_signs[i] < 0) L.signs.w[i >> 5] |= 1u << (i & 31);
     L.rot = 1;
     L.rinv = (float)(1.0 / std::sqrt((double)d));
   } else {
@@ -575,7 +596,24 @@ fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_
   L.rope_cos = rope_cos;
   L.rope_sin = rope_sin;
   L.stream = stream;
-  if ((st = fa::internal_encode_quant_map(&L.map, x, B * H, N, d)) != FA_OK) return st;
+  L.drop_pos = -1;
+  return fa::internal_encode_quant_map(&L.map, x, B * H, N, d);
+}
+
+fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
+                     const float* rope_cos, const float* rope_sin, int rope_layout, const int8_t* hadamard_signs,
+                     int per_tensor, float* workspace, cudaStream_t stream) {
+  bool empty = false;
+  fa_status st = quant_check(x, x8, descale, B, H, N, d, rope_cos, rope_sin, rope_layout, hadamard_signs, per_tensor,
+                             workspace, &empty);
+  if (st != FA_OK || empty) return st;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  fa::QuantLaunch L;
+  if ((st = quant_fill(x, x8, descale, B, H, N, d, rope_cos, rope_sin, rope_layout, hadamard_signs, per_tensor,
+                       workspace, err, stream, &L)) != FA_OK)
+    return st;
   L.drop_pos = fa::internal_take_quant_inject();
   return fa::launch_quant(L) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -607,6 +645,63 @@ fa_status fa_quant_fp8_rope(const float* x, void* x8, float* descale, int64_t B,
   if (rope_layout != FA_ROPE_INTERLEAVED && rope_layout != FA_ROPE_HALF) return FA_ERR_INVALID_ARG;
   return quant_impl(x, x8, descale, B, H, N, d, rope_cos, rope_sin, rope_layout, hadamard_signs, per_tensor,
                     workspace, stream);
+}
+
+fa_status fa_quant_fp8_qkv(const float* q, const float* k, const float* v, void* q8, void* k8, void* v8,
+                           float* q_descale, float* k_descale, float* v_descale, int64_t B, int64_t Hq, int64_t Hkv,
+                           int64_t Nq, int64_t Nk, int64_t d, const int8_t* hadamard_signs, cudaStream_t stream) {
+  // every argument of the three is checked before any CUDA call
+  const float* xs[3] = {q, k, v};
+  void* x8s[3] = {q8, k8, v8};
+  float* dss[3] = {q_descale, k_descale, v_descale};
+  const int64_t Hs[3] = {Hq, Hkv, Hkv}, Ns[3] = {Nq, Nk, Nk};
+  const int8_t* sgs[3] = {hadamard_signs, hadamard_signs, nullptr};
+  bool empty[3];
+  fa_status st;
+  for (int i = 0; i < 3; ++i)
+    if ((st = quant_check(xs[i], x8s[i], dss[i], B, Hs[i], Ns[i], d, nullptr, nullptr, 0, sgs[i], 0, nullptr,
+                          &empty[i])) != FA_OK)
+      return st;
+  if (empty[0] && empty[1] && empty[2]) return FA_OK;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  fa::QuantLaunch L[3];
+  for (int i = 0; i < 3; ++i)
+    if (!empty[i] && (st = quant_fill(xs[i], x8s[i], dss[i], B, Hs[i], Ns[i], d, nullptr, nullptr, 0, sgs[i], 0,
+                                      nullptr, err, stream, &L[i])) != FA_OK)
+      return st;
+  std::lock_guard<std::mutex> lk(g_qkv_mu);
+  QkvPipe& P = g_qkv[dev];
+  if (!P.ready) {
+    bool ok = cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 3; ++i) {
+      ok = ok && cudaStreamCreateWithFlags(&P.s[i], cudaStreamNonBlocking) == cudaSuccess;
+      ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (!ok) return FA_ERR_CUDA;
+    P.ready = true;
+  }
+  // fan out from the caller's stream, one quantisation per stream, and join
+  // back -- after an error too, so that work the caller enqueues next never
+  // runs ahead of a launch that was made
+  fa_status result = FA_OK;
+  if (cudaEventRecord(P.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  const int drop = fa::internal_take_quant_inject();
+  for (int i = 0; i < 3; ++i) {
+    if (cudaStreamWaitEvent(P.s[i], P.start, 0) != cudaSuccess) {
+      result = FA_ERR_CUDA;
+      continue;
+    }
+    if (empty[i] || result != FA_OK) continue;
+    L[i].stream = P.s[i];
+    L[i].drop_pos = (i == 0) ? drop : -1;
+    if (fa::launch_quant(L[i]) != cudaSuccess) result = FA_ERR_CUDA;
+  }
+  for (int i = 0; i < 3; ++i)
+    if (cudaEventRecord(P.done[i], P.s[i]) != cudaSuccess || cudaStreamWaitEvent(stream, P.done[i], 0) != cudaSuccess)
+      if (result == FA_OK) result = FA_ERR_CUDA;
+  return result;
 }
 
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, size_t* bytes) {

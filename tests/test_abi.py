@@ -96,6 +96,18 @@ def test_host_argument_checks(fa_lib):
     assert fa_lib.fa_splitkv_workspace_bytes(1, 4, 3, 1, 100, 128, 0, ctypes.byref(nbytes)) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_splitkv_workspace_bytes(0, 4, 2, 1, 100, 128, 0, ctypes.byref(nbytes)) == fa.FA_OK
     assert nbytes.value == 0
+    # Q, K and V in one call: every tensor is checked before anything runs
+    z = [None] * 9
+    pp = [p] * 9
+    assert fa_lib.fa_quant_fp8_qkv(*pp[:8], None, 1, 2, 1, 128, 256, 128, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_qkv(p, p, p + 4, *pp[:6], 1, 2, 1, 128, 256, 128, None,
+                                   None) == fa.FA_ERR_INVALID_ARG  # v 16-byte aligned
+    assert fa_lib.fa_quant_fp8_qkv(*pp, 1, 2, 1, 128, 256, 96, None, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_quant_fp8_qkv(*pp, 1, 2, -1, 128, 256, 128, None, None) == fa.FA_ERR_INVALID_ARG
+    bad = (ctypes.c_int8 * 128)(*([1] * 127 + [0]))
+    assert fa_lib.fa_quant_fp8_qkv(*pp, 1, 2, 1, 128, 256, 128, ctypes.cast(bad, ctypes.c_void_p),
+                                   None) == fa.FA_ERR_INVALID_ARG
+    assert fa_lib.fa_quant_fp8_qkv(*z, 0, 2, 1, 128, 256, 128, None, None) == fa.FA_OK
     # quantiser with rotary embedding: a known layout and both tables are required
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 0, None, 0, None, None) == fa.FA_ERR_INVALID_ARG
     assert fa_lib.fa_quant_fp8_rope(p, p, p, 1, 1, 1, 128, p, p, 3, None, 0, None, None) == fa.FA_ERR_INVALID_ARG

@@ -148,6 +148,87 @@ def test_quant_many_heads(fa):
         assert np.array_equal(ds.cpu().numpy(), ds_ref)
 
 
+@pytest.mark.parametrize("shape", [(2, 4, 2, 300, 700, 128), (1, 3, 3, 129, 129, 64), (1, 2, 1, 1000, 257, 256),
+                                   (4, 16, 16, 4096, 4096, 128)])
+@pytest.mark.parametrize("rot", [False, True])
+def test_quant_qkv_matches_separate_calls(fa, shape, rot):
+    # fa_quant_fp8_qkv gives each tensor exactly what fa_quant_fp8 gives it
+    # (Q and K rotated with the same signs, V never), GQA and Nq != Nk too
+    B, Hq, Hkv, Nq, Nk, d = shape
+    g = torch.Generator(device="cuda")
+    g.manual_seed(900 + Nq + d)
+    q = torch.randn((B, Hq, Nq, d), device="cuda", generator=g) * 3
+    k = torch.randn((B, Hkv, Nk, d), device="cuda", generator=g)
+    v = torch.randn((B, Hkv, Nk, d), device="cuda", generator=g) * 0.5
+    signs = gen.hadamard_signs(d, 4) if rot else None
+    got = fa.quant_fp8_qkv(q, k, v, signs=signs)
+    ref = fa.quant_fp8(q, signs=signs) + fa.quant_fp8(k, signs=signs) + fa.quant_fp8(v)
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    for a, b in zip(got, (ref[0], ref[2], ref[4], ref[1], ref[3], ref[5])):
+        assert torch.equal(a, b)
+
+
+def test_quant_qkv_against_oracle_and_stream_order(fa):
+    # on a side stream, the attention enqueued right after the call reads the
+    # finished codes; the codes are the oracle quantiser's, bit for bit
+    x = [gen.outliers((1, 2, 300, 128), 950 + i) for i in range(3)]
+    signs = gen.hadamard_signs(128, 4)
+    refs = [oracle.quant_e4m3(x[0], signs=signs), oracle.quant_e4m3(x[1], signs=signs), oracle.quant_e4m3(x[2])]
+    xd = [torch.from_numpy(a).cuda() for a in x]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        q8, k8, v8, qs, ks, vs = fa.quant_fp8_qkv(*xd, signs=signs)
+        o, lse = fa.fwd_fp8(q8, k8, v8, qs, ks, vs)
+    s.synchronize()
+    fa.check_device_error()
+    for (c, dsc), (rc, rds) in zip(((q8, qs), (k8, ks), (v8, vs)), refs):
+        assert np.array_equal(c.cpu().numpy(), rc) and np.array_equal(dsc.cpu().numpy(), rds)
+    o2, lse2 = fa.fwd_fp8(*[torch.from_numpy(a).cuda() for a in (refs[0][0], refs[1][0], refs[2][0],
+                                                                  refs[0][1], refs[1][1], refs[2][1])])
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_quant_qkv_cuda_graph(fa):
+    x = [torch.randn((2, 4, 500, 128), device="cuda") for _ in range(3)]
+    signs = gen.hadamard_signs(128, 4)
+    ref = fa.quant_fp8_qkv(*x, signs=signs)
+    out = tuple(torch.empty_like(t) for t in ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        fa.quant_fp8_qkv(*x, signs=signs, out=out)   # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fa.quant_fp8_qkv(*x, signs=signs, out=out)
+    for t in out:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
+
+
+def test_quant_qkv_empty_and_errors(fa):
+    q = torch.randn((1, 2, 0, 128), device="cuda")
+    k = torch.randn((1, 1, 200, 128), device="cuda")
+    q8, k8, v8, qs, ks, vs = fa.quant_fp8_qkv(q, k, k.clone())
+    torch.cuda.synchronize()
+    assert q8.numel() == 0 and torch.equal(k8, fa.quant_fp8(k)[0])
+    with pytest.raises(ValueError):
+        fa.quant_fp8_qkv(q, k, torch.randn((1, 1, 100, 128), device="cuda"))
+    lib = fa.lib()
+    p = k.data_ptr()
+    bad = [p] * 9
+    bad[5] = None   # v8 missing
+    assert lib.fa_quant_fp8_qkv(*bad, 1, 1, 1, 200, 200, 128, None,
+                                torch.cuda.current_stream().cuda_stream) == fa.FA_ERR_INVALID_ARG
+
+
 def _fp8_case(fa, B, H, N, d, causal, rot, per_tensor, seed, rows=None, sigma=10.0):
     q, k, v = gen.qkv_outliers((B, H, N, d), seed, sigma=sigma)
     signs = gen.hadamard_signs(d, 4) if rot else None
