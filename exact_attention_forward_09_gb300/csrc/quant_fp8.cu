@@ -57,14 +57,15 @@ namespace {
 
 template <int D, int LPR_ = 4>
 struct QCfg {
-  // Lanes per row: 4, or 1 for the rotation at d = 128 (the launch picks).
-  // One lane per row keeps every stage of the butterfly inside a lane (with
-  // a row over 4 lanes the two stages that cross lanes took about a third
-  // of the kernel's time, measured: 51.8 -> 37.5 us at B=4 H=16 N=4096),
-  // but its 128-register rows leave at most 12 warps per SM, too few to
-  // cover the memory latency without the butterfly's work in between
-  // (block scales without the rotation: 32.8 us with 4 lanes per row, 36.9
-  // with 1 lane per row and 8 warps).
+  // Lanes per row: 1 at d = 128, 4 otherwise (the launch picks).  One lane
+  // per row keeps every stage of the butterfly inside a lane (with a row
+  // over 4 lanes the two stages that cross lanes took about a third of the
+  // kernel's time, measured: 51.8 -> 37.5 us at B=4 H=16 N=4096); its
+  // 128-register rows leave 12 warps per SM, which also carry the plain
+  // modes a little faster (block scales 31.4-32.8 -> 30.7 us, per tensor
+  // 56.9 -> 52.9 us).  A rotary embedding without the rotation keeps 4 lanes
+  // per row: with one, each lane loads its own row's angle tables, 32 rows
+  // per instruction (60 -> 68 us).
   static constexpr int LPR = (D == 128) ? LPR_ : 4;
   static constexpr int RPW = 32 / LPR;           // rows of a warp's row set
   // Warps per CTA.  With 4 lanes per row the rotation and the exact rounding
@@ -664,11 +665,12 @@ cudaError_t launch_rope(const QuantLaunch& L, float* ws, int drop_pos) {
   return L.rope ? launch_one<D, MODE, true, LPR>(L, ws, drop_pos) : launch_one<D, MODE, false, LPR>(L, ws, drop_pos);
 }
 
-// one lane per row for the rotation at d = 128, 4 otherwise
+// one lane per row at d = 128 (except a rotary embedding without the
+// rotation), 4 otherwise
 template <int D, int MODE>
 cudaError_t launch_mode(const QuantLaunch& L, float* ws, int drop_pos) {
   if constexpr (D == 128) {
-    if (L.rot) return launch_rope<D, MODE, 1>(L, ws, drop_pos);
+    if (L.rot || !L.rope) return launch_rope<D, MODE, 1>(L, ws, drop_pos);
   }
   return launch_rope<D, MODE, 4>(L, ws, drop_pos);
 }
