@@ -91,7 +91,7 @@ class ClockSampler:
     region (50 ms period)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.limit")
 
     def __init__(self, index: int):
         self.index = index
@@ -117,7 +117,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, power, reasons = [], 0.0, [], set()
+        sm, smax, power, reasons, limit = [], 0.0, [], set(), None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -133,11 +133,16 @@ class ClockSampler:
                 for n, val in zip(names, parts[5:9]):
                     if val.lower() == "active":
                         reasons.add(n)
+                if len(parts) > 9:
+                    try:
+                        limit = float(parts[9])
+                    except ValueError:
+                        pass
         os.unlink(self.path)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+                "samples": len(sm), "power_w_max": max(power) if power else None, "power_limit_w": limit}
 
 
 class Flusher:
