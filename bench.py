@@ -349,14 +349,21 @@ def run_fp8_point(device, flush):
         attn()
 
     attn()
-    ts = _launch_times(attn, 10, device, flush)
+    # 200 flushed launches (about 0.3 s) with the clocks sampled meanwhile
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    time.sleep(0.1)
+    ts = _launch_times(attn, 200, device, flush)
+    clocks = sampler.stop()
     ms, ms_mean = statistics.median(ts), sum(ts) / len(ts)
     ms_step = _time_launches(whole, 10, device, flush)
     fl = gen.flops(B, H, N, d, False)
     tf = fl / (ms * 1e-3) / 1e12
     fa.check_device_error(device)
     return {"workload": f"fp8_16k: B={B} H={H} N={N} d={d} non-causal, Q/K block scales + Hadamard, V block scales",
-            "value": tf, "unit": "TFLOPS", "ms": ms, "ms_mean": ms_mean, "timing": "median of 10 flushed launches",
+            "value": tf, "unit": "TFLOPS", "ms": ms, "ms_mean": ms_mean, "timing": "median of 200 flushed launches",
+            "clocks": clocks,
             "peak": fp8_peak, "frac": tf / fp8_peak,
             "peak_source": f"{src} bf16 burst (cuBLAS GEMM) x 2, the nominal dense fp8:bf16 ratio",
             "kernel": f"attn_fwd_kernel<e4m3,{d},non-causal>", "traffic": load_traffic("fp8_16k"),
