@@ -679,7 +679,18 @@ fa_status fa_quant_fp8_qkv(const float* q, const float* k, const float* v, void*
       ok = ok && cudaStreamCreateWithFlags(&P.s[i], cudaStreamNonBlocking) == cudaSuccess;
       ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
     }
-    if (!ok) return FA_ERR_CUDA;
+    if (!ok) {
+      // release what was made, so that a later call starts again from nothing
+      if (P.start) cudaEventDestroy(P.start);
+      P.start = nullptr;
+      for (int i = 0; i < 3; ++i) {
+        if (P.s[i]) cudaStreamDestroy(P.s[i]);
+        if (P.done[i]) cudaEventDestroy(P.done[i]);
+        P.s[i] = nullptr;
+        P.done[i] = nullptr;
+      }
+      return FA_ERR_CUDA;
+    }
     P.ready = true;
   }
   // fan out from the caller's stream, one quantisation per stream, and join
