@@ -433,7 +433,27 @@ fa_status fa_fwd_host(const void* q_host, const void* k_host, const void* v_host
       ok = ok && cudaEventCreateWithFlags(&P.computed[i], cudaEventDisableTiming) == cudaSuccess;
     }
     for (int i = 0; i < 5; ++i) ok = ok && cudaEventCreateWithFlags(&P.done[i], cudaEventDisableTiming) == cudaSuccess;
-    if (!ok) return FA_ERR_CUDA;
+    if (!ok) {
+      // release what was made, so that a later call starts again from nothing
+      for (cudaStream_t* sp : {&P.h2d[0], &P.h2d[1], &P.comp[0], &P.comp[1], &P.d2h}) {
+        if (*sp) cudaStreamDestroy(*sp);
+        *sp = nullptr;
+      }
+      for (cudaEvent_t* ep : {&P.start}) {
+        if (*ep) cudaEventDestroy(*ep);
+        *ep = nullptr;
+      }
+      for (int i = 0; i < kHostChunks; ++i) {
+        if (P.copied[i]) cudaEventDestroy(P.copied[i]);
+        if (P.computed[i]) cudaEventDestroy(P.computed[i]);
+        P.copied[i] = P.computed[i] = nullptr;
+      }
+      for (int i = 0; i < 5; ++i) {
+        if (P.done[i]) cudaEventDestroy(P.done[i]);
+        P.done[i] = nullptr;
+      }
+      return FA_ERR_CUDA;
+    }
     P.ready = true;
   }
   // device copies inside the workspace: q, o, k, v, lse
