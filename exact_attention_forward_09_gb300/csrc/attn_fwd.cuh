@@ -173,7 +173,7 @@ struct AttnCfg {
   // workloads unchanged (measured) and lets TAU rise from 2.8 to 3.8.
   static constexpr float P8_SCALE = 32.0f;
   // short units' masked tiles without the per-score select (see the softmax)
-  static constexpr bool MASK_NOSEL = (D == 128) && (ELEM != kE4M3);
+  static constexpr bool MASK_NOSEL = (ELEM != kE4M3) && (D == 128 || CAUSAL);
   static_assert(ELEM != kE4M3 || TAU <= 3.807f, "FP8 P would leave the E4M3 range: 32 * 2^TAU must stay <= 448");
   static constexpr uint32_t A_FMT = (ELEM == kBF16) ? 1u : 0u;  // bf16=1, f16=0, e4m3=0
   static constexpr uint32_t IDESC_QK = instr_desc(A_FMT, A_FMT, 0, 0, 128, kBN);
@@ -1307,10 +1307,11 @@ __global__ void __launch_bounds__(AttnCfg<ELEM, D, CAUSAL, VAR>::THREADS, 1)
           }
         };
         // Masked tiles (causal diagonal, ragged end) zero the masked p one by
-        // one, except in the 16-bit d = 128 kernels' units of up to 32 key
-        // tiles with a nonzero scale, where the masked tiles are a large share
-        // (select-free form: causal mid +7%, N = 512 causal +16%, measured;
-        // the other kernels, and long units, ran 1-2.5% slower with it).
+        // one, except in the 16-bit d = 128 and causal kernels' units of up to
+        // 32 key tiles with a nonzero scale, where the masked tiles are a large
+        // share (select-free form: causal mid +7%, causal N = 512 +16% at
+        // d = 128 and +20% at d = 64, measured; the non-causal d = 64 / 256
+        // and FP8 kernels, and long units, ran 1-2.5% slower with it).
         if (need_mask && (!C::MASK_NOSEL || cj == 0.0f || Jn > 32)) emit(true);
         else emit(false);
         {
