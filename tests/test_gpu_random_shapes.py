@@ -1,0 +1,148 @@
+"""Seeded random shapes through the C ABI against the fp64 oracle on sampled
+query rows: BF16/FP16 forward (any head dimension, grouped heads, Nq != Nk,
+causal or not, the default scale, 0, a negative and an enlarged scale), the
+E4M3 quantiser bit for bit, and the FP8 forward on its codes.  The shapes
+come from one fixed generator, so a failure names a case that reruns
+exactly; they fill the gaps between the hand-picked sizes of the other
+parity tests (odd lengths, lengths below one tile, one head per group)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle
+from gpu_util import FP8_O_RMSE, LSE_ABS, O_MAXABS
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw_fwd(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([64, 128, 256]))
+        g = int(rng.choice([1, 1, 2, 4]))
+        Hkv = int(rng.integers(1, 3))
+        Nq = int(rng.integers(1, 1500))
+        Nk = int(rng.choice([Nq, int(rng.integers(1, 1500))]))
+        scale = float(rng.choice([1.0 / math.sqrt(d), 0.0, -0.2, 0.3]))
+        cases.append(dict(i=i, B=int(rng.integers(1, 3)), Hq=Hkv * g, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
+                          causal=bool(rng.integers(0, 2)), scale=scale,
+                          fp16=bool(rng.integers(0, 2)), rows_seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+def _draw_quant(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [dict(i=i, d=int(rng.choice([64, 128, 256])), N=int(rng.integers(1, 900)),
+                 B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), rot=bool(rng.integers(0, 2)),
+                 per_tensor=bool(rng.integers(0, 2))) for i in range(n)]
+
+
+def _draw_fp8(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([128, 256]))
+        g = int(rng.choice([1, 2, 4]))
+        Hkv = int(rng.integers(1, 3))
+        Nq = int(rng.integers(1, 1300))
+        Nk = int(rng.choice([Nq, int(rng.integers(1, 1300))]))
+        cases.append(dict(i=i, B=int(rng.integers(1, 3)), Hq=Hkv * g, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
+                          causal=bool(rng.integers(0, 2)), rot=bool(rng.integers(0, 2)),
+                          rows_seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+FWD = _draw_fwd(150, 20261203)
+QUANT = _draw_quant(40, 20261204)
+FP8 = _draw_fp8(60, 20261205)
+
+
+def _ids(cases):
+    return [",".join(f"{k}={v}" for k, v in c.items() if k != "rows_seed") for c in cases]
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_09_gb300 as fa
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+    return fa
+
+
+def _rows(Nq, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.unique(np.concatenate([rng.integers(0, Nq, 24), [0, Nq - 1]]))
+
+
+def _check_lse(lse, l_ref, tol, what):
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: rows without keys must have LSE = -inf"
+    if (~empty).any():
+        e = np.abs(lse[~empty] - l_ref[~empty]).max()
+        assert e <= tol, f"{what}: max|dLSE| = {e:.3e}"
+
+
+@pytest.mark.parametrize("c", FWD, ids=_ids(FWD))
+def test_random_fwd(fa, c):
+    dt = torch.float16 if c["fp16"] else torch.bfloat16
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    seed = 5000 + c["i"]
+    q = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 0)).to(dt)
+    k = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 1)).to(dt)
+    v = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 2)).to(dt)
+    o, lse = fa.fwd_gqa(q.cuda(), k.cuda(), v.cuda(), causal=c["causal"], scale=c["scale"])
+    fa.check_device_error()
+    rows = _rows(Nq, c["rows_seed"])
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=c["causal"], scale=c["scale"], rows=rows)
+    o = o.float().cpu().numpy().astype(np.float64)[:, :, rows]
+    lse = lse.cpu().numpy().astype(np.float64)[:, :, rows]
+    assert np.isfinite(o).all()
+    _check_lse(lse, l_ref, LSE_ABS, "forward")
+    # at |scale| above 1/sqrt(d) the softmax is peakier and one rounded P
+    # weight carries more of O, so the bound doubles there
+    tol = O_MAXABS if c["scale"] == 1.0 / math.sqrt(d) or c["scale"] == 0.0 else 2 * O_MAXABS
+    e = np.abs(o - o_ref).max()
+    assert e <= tol, f"forward: max|dO| = {e:.3e}"
+
+
+@pytest.mark.parametrize("c", QUANT, ids=_ids(QUANT))
+def test_random_quant(fa, c):
+    x = gen.outliers((c["B"], c["H"], c["N"], c["d"]), 7000 + c["i"])
+    signs = gen.hadamard_signs(c["d"], 4) if c["rot"] else None
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs, per_tensor=c["per_tensor"])
+    fa.check_device_error()
+    rc, rs = oracle.quant_e4m3(x, signs=signs, per_tensor=c["per_tensor"])
+    assert np.array_equal(ds.cpu().numpy(), rs), "descales"
+    assert np.array_equal(codes.cpu().numpy(), rc), "codes"
+
+
+@pytest.mark.parametrize("c", FP8, ids=_ids(FP8))
+def test_random_fp8(fa, c):
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    seed = 9000 + c["i"]
+    signs = gen.hadamard_signs(d, 4) if c["rot"] else None
+    xq = gen.outliers((B, Hq, Nq, d), seed, 0)
+    xk = gen.outliers((B, Hkv, Nk, d), seed, 1)
+    xv = gen.outliers((B, Hkv, Nk, d), seed, 2)
+    # codes from the oracle quantiser, so this case does not depend on the
+    # quantiser kernel
+    qc, qs = oracle.quant_e4m3(xq, signs=signs)
+    kc, ks = oracle.quant_e4m3(xk, signs=signs)
+    vc, vs = oracle.quant_e4m3(xv)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd_fp8_gqa(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=c["causal"], scale=scale)
+    fa.check_device_error()
+    rows = _rows(Nq, c["rows_seed"])
+    deq = [oracle.dequant_e4m3(a, s) for a, s in ((qc, qs), (kc, ks), (vc, vs))]
+    o_ref, l_ref = oracle.attn_fwd(*deq, causal=c["causal"], scale=scale, rows=rows)
+    o = o.float().cpu().numpy().astype(np.float64)[:, :, rows]
+    lse = lse.cpu().numpy().astype(np.float64)[:, :, rows]
+    assert np.isfinite(o).all()
+    _check_lse(lse, l_ref, LSE_ABS, "fp8 forward")
+    rmse = math.sqrt(float(((o - o_ref) ** 2).mean()))
+    assert rmse <= FP8_O_RMSE, f"fp8 forward: O rmse = {rmse:.3e}"
