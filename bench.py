@@ -527,7 +527,7 @@ ABLATE_VARIANTS = {0: "shipped kernel", 1: "split softmax (two warpgroups per Q 
                    128: "early partial Q K^T (keys beyond P's columns issued at P's first half)",
                    256: "direct O stores from registers (no staging boxes, no bulk tensor stores)"}
 ABLATE_BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, True, 128): (0, 1, 8, 16, 256),
-                (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, False, 64): (0, 32, 64, 128, 256),
+                (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, False, 64): (0, 1, 32, 64, 128, 256),
                 (False, True, 64): (0, 32)}
 
 

@@ -33,7 +33,7 @@
  *       ring keeps the slot the boxes take (d = 128 16-bit: 5 slots, not 4)
  * Built instances: d = 128 bf16 non-causal and FP8 non-causal with codes
  * 0, 1, 2, 4, 8, 16, 64, 128, 256; d = 128 bf16 causal with 0, 1, 8, 16,
- * 256; d = 64 bf16 non-causal with 0, 32, 64, 128, 256 and causal with 0, 32.
+ * 256; d = 64 bf16 non-causal with 0, 1, 32, 64, 128, 256 and causal with 0, 32.
  *   variant      one of the codes above
  *   fp8          0: q, k, v bf16 (descales ignored, may be NULL); 1: E4M3
  *                codes with [B, H, ceil(N/128)] fp32 descales as fa_fwd_fp8

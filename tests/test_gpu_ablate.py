@@ -16,7 +16,7 @@ from gpu_util import FP8_O_RMSE, assert_bf16_parity, errors, make_qkv, oracle_ro
 pytestmark = pytest.mark.gpu
 
 BUILT = {(False, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, True, 128): (0, 1, 8, 16, 256),
-         (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, False, 64): (0, 32, 64, 128, 256),
+         (True, False, 128): (0, 1, 2, 4, 8, 16, 64, 128, 256), (False, False, 64): (0, 1, 32, 64, 128, 256),
          (False, True, 64): (0, 32)}
 
 
