@@ -459,6 +459,8 @@ def run_extra(device, flush):
                                ("per_tensor", lambda: fa.quant_fp8(x[2], per_tensor=True), 0),
                                ("rope_half_hadamard", lambda: fa.quant_fp8(x[0], signs=signs,
                                                                           rope=(cos, sin, fa.FA_ROPE_HALF)),
+                                (cos.numel() + sin.numel()) * 4),
+                               ("rope_half", lambda: fa.quant_fp8(x[0], rope=(cos, sin, fa.FA_ROPE_HALF)),
                                 (cos.numel() + sin.numel()) * 4)):
         qms = _time_launches(qfn, 5, device, flush)
         gbs = (qbytes + extra_b) / (qms * 1e-3) / 1e9

@@ -617,7 +617,10 @@ fa_status quant_fill(const float* x, void* x8, float* descale, int64_t B, int64_
   L.rope_sin = rope_sin;
   L.stream = stream;
   L.drop_pos = -1;
-  return fa::internal_encode_quant_map(&L.map, x, B * H, N, d);
+  fa_status st = fa::internal_encode_quant_map(&L.map, x, B * H, N, d);
+  if (st == FA_OK && rope_layout != 0 && d != 256)
+    st = fa::internal_encode_rope_maps(&L.map_cos, &L.map_sin, rope_cos, rope_sin, N, d);
+  return st;
 }
 
 fa_status quant_impl(const float* x, void* x8, float* descale, int64_t B, int64_t H, int64_t N, int64_t d,
@@ -647,6 +650,14 @@ fa_status internal_device_setup(int* dev, int** err) { return device_setup(dev, 
 fa_status internal_encode_quant_map(CUtensorMap* map, const float* x, int64_t BH, int64_t N, int64_t d) {
   // 32-float (128-byte) x 64-row boxes, 128-byte swizzle, rows past N read as 0
   return encode_map(map, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 64);
+}
+
+fa_status internal_encode_rope_maps(CUtensorMap* map_cos, CUtensorMap* map_sin, const float* rope_cos,
+                                    const float* rope_sin, int64_t N, int64_t d) {
+  // each table as one head of N rows of d/2 floats: 32-float x 128-row boxes
+  fa_status st = encode_map(map_cos, rope_cos, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 1, N, d / 2, 128);
+  if (st != FA_OK) return st;
+  return encode_map(map_sin, rope_sin, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 1, N, d / 2, 128);
 }
 
 int internal_take_quant_inject() { return g_inject_quant.exchange(0) ? 1 : -1; }

@@ -35,8 +35,9 @@
 // one pass (two or three groups on alternate blocks).  A row is spread over 4 lanes
 // (lane / 8 picks the quarter, lane % 8 the row; 8 or 16 rows per warp),
 // chosen so that the 8 lanes of each shared-memory phase read 8 different
-// rows and the swizzle puts them in different banks; with the rotation at
-// d = 128 each lane holds a whole row instead (32 rows per warp, 12 warps),
+// rows and the swizzle puts them in different banks; at d = 128 each lane
+// holds a whole row instead (32 rows per warp, 12 warps; 8 with the rotary
+// embedding, whose angle tables take shared memory too),
 // so that no stage of the butterfly crosses lanes, and 8 consecutive lanes
 // are again 8 rows in different banks.  The rotated rows stay in registers: each warp frees its
 // slot as soon as it has read it, takes the block maximum across its group's warps
@@ -55,7 +56,7 @@
 namespace fa {
 namespace {
 
-template <int D, int LPR_ = 4>
+template <int D, int LPR_ = 4, bool ROPE_ = false>
 struct QCfg {
   // Lanes per row: 1 at d = 128, 4 otherwise (the launch picks).  One lane
   // per row keeps every stage of the butterfly inside a lane (with a row
@@ -63,10 +64,24 @@ struct QCfg {
   // kernel's time, measured: 51.8 -> 37.5 us at B=4 H=16 N=4096); its
   // 128-register rows leave 12 warps per SM, which also carry the plain
   // modes a little faster (block scales 31.4-32.8 -> 30.7 us, per tensor
-  // 56.9 -> 52.9 us).  A rotary embedding without the rotation keeps 4 lanes
-  // per row: with one, each lane loads its own row's angle tables, 32 rows
-  // per instruction (60 -> 68 us).
+  // 56.9 -> 52.9 us), and with the angle tables staged in shared memory
+  // (below) also the rotary embedding without the rotation (rope half
+  // 54 -> 48 us, interleaved unchanged).
   static constexpr int LPR = (D == 128) ? LPR_ : 4;
+  // Rotary embedding with staged angle tables (d = 64 and 128): the CTA
+  // takes a contiguous range of blocks in position-major order (the heads of
+  // one 128-row position block next to each other), so one copy of the
+  // block's cos and sin rows in shared memory serves every head of its range
+  // at that position, read with the same 128-byte swizzle as x.  Loaded per
+  // lane from global memory instead, the tables took about half of each
+  // call, a chain of dependent loads per row (B=4 H=16 N=4096, d = 128:
+  // rope + rotation 82 -> 56 us, rope alone 99 -> 48 us; d = 64, B=8 H=32
+  // N=2048: 103 -> 66 and 93 -> 58 us).  d = 256's tables (128 KB) do not
+  // fit beside the ring, and it keeps the per-lane loads.
+  static constexpr bool TBL = ROPE_ && D != 256;
+  static constexpr int TBL_BOXES = D / 2 / 32;                     // 32-float boxes per table row
+  static constexpr int TBL_TAB_BYTES = TBL ? TBL_BOXES * 128 * 128 : 0;  // one table, 128 rows
+  static constexpr int TBL_BYTES = 2 * TBL_TAB_BYTES;            // cos and sin
   static constexpr int RPW = 32 / LPR;           // rows of a warp's row set
   // Warps per CTA.  With 4 lanes per row the rotation and the exact rounding
   // are latency-bound chains per row, so the warps in flight matter: d = 64
@@ -74,13 +89,15 @@ struct QCfg {
   // than 16 warps); d = 256 runs 16 warps (its rows need 128 registers).
   // d = 128 with one row per lane (128 independent elements each) runs 12
   // in three groups of 4 (168 registers; 8 warps of 254 were 17% slower).
-  static constexpr int NW = (D == 64) ? 32 : (LPR == 1) ? 12 : 16;
+  // With staged tables and one lane per row, 8 warps in two groups (the
+  // tables take the third group's ring).
+  static constexpr int NW = (D == 64) ? 32 : (LPR == 1) ? (TBL ? 8 : 12) : 16;
   static constexpr int THREADS = 32 * NW;
   // Two (one row per lane: three) groups work on alternate blocks, each with
   // its own ring and barrier, so that one group's wait for its block maximum
   // overlaps the other groups' work (d = 256: one group; its rows do not fit
   // twice).
-  static constexpr int NG = (D == 256) ? 1 : (LPR == 1) ? 3 : 2;
+  static constexpr int NG = (D == 256) ? 1 : (LPR == 1 && !TBL) ? 3 : 2;
   static constexpr int WG = NW / NG;             // warps per group
   static constexpr int RS = 128 / (RPW * WG);    // row sets per warp and block
   static_assert(RS == 1 || RS == 2, "a group covers a 128-row block");
@@ -102,12 +119,13 @@ struct QCfg {
   // mbarrier's phase parity cannot tell from the previous phase.)  With two
   // row sets every warp of a group reads both halves, in order, so any
   // count works.
-  static constexpr int NSG_RAW = 196608 / SLOT_BYTES / NG;
+  static constexpr int NSG_RAW = (196608 - TBL_BYTES) / SLOT_BYTES / NG;
   static constexpr int NSG_CAP = NSG_RAW > 8 ? 8 : NSG_RAW;
   static constexpr int NSG = (RS == 1) ? (NSG_CAP & ~1) : NSG_CAP;
   static_assert(NSG >= 2 && (RS == 2 || NSG % 2 == 0), "ring too shallow or odd");
   static constexpr int NSLOT = NG * NSG;
-  static constexpr int SMEM_BYTES = NSLOT * SLOT_BYTES + 1024 + 1024;  // ring + barriers + alignment
+  // ring, tables, barriers, alignment
+  static constexpr int SMEM_BYTES = NSLOT * SLOT_BYTES + TBL_BYTES + 1024 + 1024;
 };
 
 template <int NS>
@@ -116,6 +134,9 @@ struct QShared {
   uint64_t empty[NS];
   float red[64];       // [group][block parity][warp of group]; MODE 1: [warp]
   int last_pos[NS];
+  uint64_t tbl_full;   // staged tables: one completion per table phase
+  int tbl_cnt;         // staged tables: warps that have left their table phases, in all
+  int tbl_issued;      // staged tables: last table phase issued
   int abort_flag;
   int first_bad;       // first block iteration (of the CTA) some warp could not finish
 };
@@ -135,6 +156,17 @@ struct QuantParams {
   int rope;
   int drop_pos;
 };
+
+// Atomic add on a shared-memory int, acquire-release at CTA scope (the
+// staged tables' phase count): returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_cta(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)
+               : "memory");
+  return old;
+}
 
 // Index within the row of a lane's local element e (quarter p of the row).
 template <int D, int LPR>
@@ -188,17 +220,18 @@ __device__ __forceinline__ uint32_t encode4(const float* v, float2 rh, float2 rl
   return settle4(v[0], v[1], v[2], v[3], ch, cl, s);
 }
 
-template <int D, int LPR>
-__device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, const float* __restrict__ c,
-                                         const float* __restrict__ s, int mode) {
+// ld(t, col): the four table entries col .. col + 3 of this lane's row, of
+// the cos (t = 0) or sin (t = 1) table.
+template <int D, int LPR, class Ld>
+__device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, const Ld& ld, int mode) {
   constexpr int E = QCfg<D, LPR>::E;
   if (mode == 1) {
     // pairs (2i, 2i+1): adjacent elements of one lane, angle elem / 2
 #pragma unroll
     for (int e0 = 0; e0 < E; e0 += 8) {
       const int a0 = elem_of<D, LPR>(e0, p) >> 1;
-      const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
-      const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+      const float4 C = ld(0, a0);
+      const float4 S = ld(1, a0);
       const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -212,8 +245,8 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, con
       // pairs (i, i + D/2): both in this lane
 #pragma unroll
       for (int e0 = 0; e0 < D / 2; e0 += 4) {
-        const float4 C = __ldg(reinterpret_cast<const float4*>(c + e0));
-        const float4 S = __ldg(reinterpret_cast<const float4*>(s + e0));
+        const float4 C = ld(0, e0);
+        const float4 S = ld(1, e0);
         const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -227,8 +260,8 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, con
 #pragma unroll
       for (int e0 = 0; e0 < 32; e0 += 4) {
         const int a0 = elem_of<D, LPR>(e0, p);
-        const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
-        const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+        const float4 C = ld(0, a0);
+        const float4 S = ld(1, a0);
         const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -243,8 +276,8 @@ __device__ __forceinline__ void rope_row(float (&v)[QCfg<D, LPR>::E], int p, con
 #pragma unroll
       for (int e0 = 0; e0 < E; e0 += 4) {
         const int a0 = elem_of<D, LPR>(e0, p & 1);
-        const float4 C = __ldg(reinterpret_cast<const float4*>(c + a0));
-        const float4 S = __ldg(reinterpret_cast<const float4*>(s + a0));
+        const float4 C = ld(0, a0);
+        const float4 S = ld(1, a0);
         const float cv[4] = {C.x, C.y, C.z, C.w}, sv[4] = {S.x, S.y, S.z, S.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -339,13 +372,16 @@ __device__ __forceinline__ void rotate_row(float (&v)[QCfg<D, LPR>::E], int p,
 // max per CTA).  MODE 2: per-tensor encode with the maximum in *ws.
 // MODE 3: per-block maxima to ws[block] (no atomics).
 template <int D, int MODE, bool ROPE, int LPR>
-__global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
-    quant_e4m3_kernel(const __grid_constant__ CUtensorMap map, const QuantParams prm) {
-  using C = QCfg<D, LPR>;
+__global__ void __launch_bounds__(QCfg<D, LPR, ROPE>::THREADS, 1)
+    quant_e4m3_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap map_cos,
+                      const __grid_constant__ CUtensorMap map_sin, const QuantParams prm) {
+  using C = QCfg<D, LPR, ROPE>;
   constexpr int E = C::E, RS = C::RS, NSG = C::NSG;
+  static_assert(C::G == QCfg<D, LPR>::G && C::E == QCfg<D, LPR>::E, "the row helpers use the same lane layout");
   extern __shared__ __align__(1024) uint8_t qsmem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
-  QShared<C::NSLOT>* sh = reinterpret_cast<QShared<C::NSLOT>*>(ring + C::NSLOT * C::SLOT_BYTES);
+  uint8_t* tbl = ring + C::NSLOT * C::SLOT_BYTES;  // staged tables: cos boxes, then sin boxes
+  QShared<C::NSLOT>* sh = reinterpret_cast<QShared<C::NSLOT>*>(tbl + C::TBL_BYTES);
   volatile int* abort_flag = &sh->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (int)gridDim.x;
@@ -360,11 +396,82 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
       mbar_init(&sh->empty[s], C::READERS);  // the warps that read a slot's rows
       sh->last_pos[s] = -1;
     }
+    mbar_init(&sh->tbl_full, 1);
+    sh->tbl_cnt = 0;
+    sh->tbl_issued = -1;
     sh->abort_flag = 0;
     sh->first_bad = INT_MAX;
     fence_barrier_init();
   }
   __syncthreads();
+
+  // Block of this CTA's iteration `it` (-1: none left), its head and its
+  // 128-row block within the head; the returned index is bh * nblk + blk.
+  // Without staged tables the CTAs stride over the blocks head by head
+  // (b = blockIdx.x + it * G); with them each CTA takes the contiguous range
+  // [t_start, t_end) of the position-major order b' = blk * BH + bh.
+  const int nblk_ = prm.nblk, total_ = prm.total, BH = total_ / (nblk_ > 0 ? nblk_ : 1);
+  const long long t_start = (long long)blockIdx.x * total_ / G;
+  const long long t_end = (long long)(blockIdx.x + 1) * total_ / G;
+  auto block_of = [&](int it, int& bh, int& blk) -> int {
+    if constexpr (C::TBL) {
+      const long long bp = t_start + it;
+      if (bp >= t_end) return -1;
+      blk = (int)(bp / BH);
+      bh = (int)(bp - (long long)blk * BH);
+      return bh * nblk_ + blk;
+    } else {
+      const int b = blockIdx.x + it * G;
+      if (b >= total_) return -1;
+      bh = b / nblk_;
+      blk = b - bh * nblk_;
+      return b;
+    }
+  };
+
+  // Staged tables: phase k holds the cos and sin rows of position block
+  // blk_first + k (rows past N read as 0).  Every warp passes through every
+  // phase of the CTA in order, waiting for each table (so the barrier's
+  // parity never skips a phase) and counting itself out when it moves on;
+  // the warp whose count completes phase k issues phase k + 1 into the same
+  // buffer, so a table is replaced only after every warp is done with it.
+  const int blk_first = C::TBL ? (int)(t_start / BH) : 0;
+  const int nphase = C::TBL ? (int)((t_end - 1) / BH) - blk_first + 1 : 0;
+  auto tbl_issue = [&](int k) {
+    mbar_arrive_expect_tx(&sh->tbl_full, C::TBL_BYTES);
+    const int row0 = (blk_first + k) * 128;
+#pragma unroll
+    for (int bx = 0; bx < C::TBL_BOXES; ++bx) {
+      tma_load_3d(tbl + bx * 16384, &map_cos, &sh->tbl_full, 32 * bx, row0, 0);
+      tma_load_3d(tbl + C::TBL_TAB_BYTES + bx * 16384, &map_sin, &sh->tbl_full, 32 * bx, row0, 0);
+    }
+    sh->tbl_issued = k;
+  };
+  if (C::TBL && threadIdx.x == 0) {
+    tma_prefetch_desc(&map_cos);
+    tma_prefetch_desc(&map_sin);
+    tbl_issue(0);
+  }
+  int tk = -1;  // table phase this warp holds
+  // hold phase k: count out of the phases before it and wait for each table
+  auto tbl_to = [&](int k) -> bool {
+    bool okk = true;
+    while (tk < k) {
+      if (tk >= 0) {
+        __syncwarp();
+        if (lane == 0) {
+          const int old = atom_add_acq_rel_cta(&sh->tbl_cnt, 1);
+          if (old == C::NW * (tk + 1) - 1 && tk + 1 < nphase && !*abort_flag) {
+            fence_proxy_async_smem();
+            tbl_issue(tk + 1);
+          }
+        }
+      }
+      ++tk;
+      okk = __all_sync(0xffffffffu, mbar_wait(&sh->tbl_full, (uint32_t)(tk & 1), abort_flag, prm.err)) && okk;
+    }
+    return okk;
+  };
 
   // Block iteration `it` of this CTA is blockIdx.x + it * G; group g takes
   // it = g, g + NG, g + 2 NG, ...  Its j-th block fills group positions 2j
@@ -390,9 +497,8 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
       for (; more && issued < limit; ++issued) {
         const int q = issued;
         const int it = C::NG * (q >> 1) + grp;
-        const int b = blockIdx.x + it * G;
-        if (b >= prm.total) { more = false; break; }
-        const int bh = b / prm.nblk, blk = b - bh * prm.nblk;
+        int bh, blk;
+        if (block_of(it, bh, blk) < 0) { more = false; break; }
         const int slot = q % NSG;
         if (!mbar_wait(&gempty[slot], (uint32_t)(((q / NSG) & 1) ^ 1), abort_flag, prm.err)) {
           ok = false;
@@ -439,14 +545,15 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
     s_t = (am > 0.0f) ? __fdiv_rn(am, 448.0f) : 1.0f;
   }
   float cta_max = 0.0f;  // MODE 1
-  const int N = prm.N, nblk = prm.nblk, total = prm.total;
+  const int N = prm.N;
 
   for (int j = 0;; ++j) {
     const int it = C::NG * j + grp;
-    const int b = blockIdx.x + it * G;
-    if (b >= total) break;
-    const int bh = b / nblk, blk = b - bh * nblk;
+    int bh, blk;
+    const int b = block_of(it, bh, blk);
+    if (b < 0) break;
     bool ok = __shfl_sync(0xffffffffu, (int)issue_upto(2 * j + NSG), 0) != 0;
+    if constexpr (C::TBL) ok = tbl_to(blk - blk_first) && ok;
     float v[RS][E];
     float am = 0.0f;
 #pragma unroll
@@ -479,9 +586,23 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < E; ++e) v[k][e] = 0.0f;
         }
-        if constexpr (ROPE) {
+        if constexpr (C::TBL) {
+          // row r of the staged block: 16-byte chunk c of each 128-byte box
+          // row at position c ^ (r % 8)
+          const uint8_t* trow = tbl + (half_of(k) * C::SLOT_ROWS + r_slot) * 128;
+          auto ld = [&](int t, int col) -> float4 {
+            return *reinterpret_cast<const float4*>(trow + t * C::TBL_TAB_BYTES + (col >> 5) * 16384 +
+                                                    ((((col & 31) >> 2) ^ swz) << 4));
+          };
+          rope_row<D, LPR>(v[k], p, ld, prm.rope);
+        } else if constexpr (ROPE) {
           const size_t nr = (size_t)(n < N ? n : N - 1) * (D / 2);
-          rope_row<D, LPR>(v[k], p, prm.rcos + nr, prm.rsin + nr, prm.rope);
+          const float* rc = prm.rcos + nr;
+          const float* rs = prm.rsin + nr;
+          auto ld = [&](int t, int col) -> float4 {
+            return __ldg(reinterpret_cast<const float4*>((t ? rs : rc) + col));
+          };
+          rope_row<D, LPR>(v[k], p, ld, prm.rope);
         }
         if (prm.rot) rotate_row<D, LPR>(v[k], p, smask);
 #pragma unroll
@@ -556,18 +677,12 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
             }
           }
         }
-        continue;
-      }
-      uint32_t words[E / 4];
+      } else {
+        uint32_t words[E / 4];
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) words[q] = encode4(&v[k][4 * q], rh2, rl2, se);
-      if (n < N) {
-        uint8_t* row = prm.x8 + ((size_t)bh * N + n) * D;
-        if (C::LPR == 1 && prm.x8_vec32) {
-          // a whole row per lane: 32-byte stores (full sectors)
-#pragma unroll
-          for (int jj = 0; jj < E / 32; ++jj) st_global_v8(row + 32 * jj, words + 8 * jj);
-        } else {
+        for (int q = 0; q < E / 4; ++q) words[q] = encode4(&v[k][4 * q], rh2, rl2, se);
+        if (n < N) {
+          uint8_t* row = prm.x8 + ((size_t)bh * N + n) * D;
 #pragma unroll
           for (int jj = 0; jj < E / 16; ++jj)
             *reinterpret_cast<uint4*>(row + elem_of<D, LPR>(16 * jj, p)) =
@@ -577,6 +692,9 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
     }
     if (wg == 0 && lane == 0) prm.descale[b] = __fmul_rn(s, prm.rinv);
   }
+  // staged tables: pass through the phases still ahead (counting out of
+  // each, which the other warps may be waiting for), up to the last one
+  if constexpr (C::TBL) (void)tbl_to(nphase - 1);
   // never leave with copies in flight: after a timeout, each issuer waits
   // (bounded) for the last fill of every slot of its group that was filled
   if (issuer && *abort_flag) {
@@ -592,6 +710,12 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
   // from the first one some warp could not finish, so that no caller reads
   // a stale or unwritten scale without the error word being set
   __syncthreads();
+  // and for the table load in flight, if one was issued and not waited for
+  if (C::TBL && threadIdx.x == 0 && *abort_flag && sh->tbl_issued >= 0) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&sh->tbl_full, (uint32_t)(sh->tbl_issued & 1)) && globaltimer() - t0 < FA_WAIT_LIMIT_NS) {
+    }
+  }
   if constexpr (MODE == 1) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) cta_max = fmaxf(cta_max, __shfl_xor_sync(0xffffffffu, cta_max, m));
@@ -605,7 +729,10 @@ __global__ void __launch_bounds__(QCfg<D, LPR>::THREADS, 1)
     }
   } else {
     if (threadIdx.x == 0 && sh->first_bad != INT_MAX) {
-      for (int bb = blockIdx.x + sh->first_bad * G; bb < total; bb += G) {
+      for (int it = sh->first_bad;; ++it) {
+        int bh, blk;
+        const int bb = block_of(it, bh, blk);
+        if (bb < 0) break;
         if constexpr (MODE == 3) prm.ws[bb] = INFINITY;
         else prm.descale[bb] = __int_as_float(0x7fc00000);
       }
@@ -627,7 +754,7 @@ int sm_count_cached() {
 
 template <int D, int MODE, bool ROPE, int LPR>
 cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
-  using C = QCfg<D, LPR>;
+  using C = QCfg<D, LPR, ROPE>;
   auto kern = quant_e4m3_kernel<D, MODE, ROPE, LPR>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -656,7 +783,7 @@ cudaError_t launch_one(const QuantLaunch& L, float* ws, int drop_pos) {
   prm.drop_pos = drop_pos;
   const int sms = sm_count_cached();
   const int grid = prm.total < sms ? prm.total : sms;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.map, prm);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(L.map, L.map_cos, L.map_sin, prm);
   return cudaGetLastError();
 }
 
@@ -665,14 +792,10 @@ cudaError_t launch_rope(const QuantLaunch& L, float* ws, int drop_pos) {
   return L.rope ? launch_one<D, MODE, true, LPR>(L, ws, drop_pos) : launch_one<D, MODE, false, LPR>(L, ws, drop_pos);
 }
 
-// one lane per row at d = 128 (except a rotary embedding without the
-// rotation), 4 otherwise
+// one lane per row at d = 128, 4 otherwise
 template <int D, int MODE>
 cudaError_t launch_mode(const QuantLaunch& L, float* ws, int drop_pos) {
-  if constexpr (D == 128) {
-    if (L.rot || !L.rope) return launch_rope<D, MODE, 1>(L, ws, drop_pos);
-  }
-  return launch_rope<D, MODE, 4>(L, ws, drop_pos);
+  return launch_rope<D, MODE, (D == 128) ? 1 : 4>(L, ws, drop_pos);
 }
 
 template <int D>

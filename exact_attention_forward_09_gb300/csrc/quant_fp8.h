@@ -33,6 +33,11 @@ struct QuantLaunch {
   const float* rope_cos;
   const float* rope_sin;
   int rope;
+  // the tables as [N, d/2] maps of 32-float x 128-row boxes (128-byte
+  // swizzle, rows past N read as 0), for the kernels that stage them in
+  // shared memory (d = 64 and 128); unused otherwise
+  CUtensorMap map_cos;
+  CUtensorMap map_sin;
   // test hook: the first CTA of the first launch of this call never fills
   // this slot position (-1: none), so the bounded waits on it run out
   int drop_pos;
@@ -53,6 +58,8 @@ cudaError_t launch_quant_per_tensor_partials(const QuantLaunch& L, float* partia
 fa_status internal_device_setup(int* dev, int** err);
 // Tensor map of a contiguous fp32 [BH, N, d] tensor for the quantiser.
 fa_status internal_encode_quant_map(CUtensorMap* map, const float* x, int64_t BH, int64_t N, int64_t d);
+fa_status internal_encode_rope_maps(CUtensorMap* map_cos, CUtensorMap* map_sin, const float* rope_cos,
+                                    const float* rope_sin, int64_t N, int64_t d);
 // Consume a pending quantiser failure injection (fa_debug_inject flag 2):
 // the slot position to leave unfilled, or -1.
 int internal_take_quant_inject();

@@ -69,19 +69,24 @@ def test_backward_pipeline_timeout_is_reported_and_context_survives(fa, d):
 
 
 @pytest.mark.parametrize("per_tensor", [False, True])
-def test_quantiser_timeout_is_reported_and_next_call_exact(fa, per_tensor):
+@pytest.mark.parametrize("rope", [False, True])
+def test_quantiser_timeout_is_reported_and_next_call_exact(fa, per_tensor, rope):
     """The quantiser's first CTA never gets one input slot: the bounded waits
     run out, FA_ERR_TIMEOUT is reported, the blocks that CTA could not finish
     carry a NaN descale (per tensor: an infinite maximum, so every descale is
-    infinite) instead of old values, and the next call is bit-exact."""
+    infinite) instead of old values, and the next call is bit-exact.  With
+    the rotary embedding the angle tables are staged in shared memory, and
+    the other warps of that CTA stop at their table waits too."""
     x = gen.outliers((2, 4, 1000, 128), 33)
     xd = torch.from_numpy(x).cuda()
+    tables = gen.rope_tables(1000, 128) if rope else None
+    rp = (torch.from_numpy(tables[0]).cuda(), torch.from_numpy(tables[1]).cuda(), 2) if rope else None
     lib = fa.lib()
     stream = torch.cuda.current_stream().cuda_stream
     assert lib.fa_check_device_error(stream) == fa.FA_OK
     assert lib.fa_debug_inject(2) == fa.FA_OK
     t0 = time.time()
-    _, ds = fa.quant_fp8(xd, per_tensor=per_tensor)
+    _, ds = fa.quant_fp8(xd, per_tensor=per_tensor, rope=rp)
     st = lib.fa_check_device_error(stream)
     assert st == fa.FA_ERR_TIMEOUT, lib.fa_status_string(st)
     assert time.time() - t0 < 30.0
@@ -91,9 +96,9 @@ def test_quantiser_timeout_is_reported_and_next_call_exact(fa, per_tensor):
     else:
         assert np.isnan(ds.reshape(-1)[0])
     assert lib.fa_check_device_error(stream) == fa.FA_OK
-    codes, ds = fa.quant_fp8(xd, per_tensor=per_tensor)
+    codes, ds = fa.quant_fp8(xd, per_tensor=per_tensor, rope=rp)
     assert lib.fa_check_device_error(stream) == fa.FA_OK
-    codes_ref, ds_ref = oracle.quant_e4m3(x, per_tensor=per_tensor)
+    codes_ref, ds_ref = oracle.quant_e4m3(x, per_tensor=per_tensor, rope=(tables[0], tables[1], 2) if rope else None)
     assert np.array_equal(codes.cpu().numpy(), codes_ref)
     assert np.array_equal(ds.cpu().numpy(), ds_ref)
 

@@ -306,6 +306,41 @@ def test_quant_rope_bit_exact(fa, d, layout, rot, per_tensor):
     assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
 
 
+@pytest.mark.parametrize("shape", [(2, 16, 4096, 128), (1, 1, 65536, 128), (4, 8, 1000, 64), (1, 3, 20000, 64),
+                                   (3, 5, 777, 128)])
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("rot", [False, True])
+def test_quant_rope_many_blocks_per_cta(fa, shape, layout, rot):
+    # d = 64 and 128 stage the angle tables of one 128-row position block at
+    # a time in shared memory, shared by the heads of the CTA's block range:
+    # many heads per position (several per CTA), one head of 512 positions
+    # (a new table for every block), ragged lengths
+    B, H, N, d = shape
+    x = gen.outliers(shape, 90 + N % 97 + layout)
+    cos, sin = gen.rope_tables(N, d, offset=3)
+    signs = gen.hadamard_signs(d, 4) if rot else None
+    codes_ref, ds_ref = oracle.quant_e4m3(x, signs=signs, rope=(cos, sin, layout))
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs,
+                             rope=(torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(), layout))
+    fa.check_device_error()
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
+    mism = int((codes.cpu().numpy() != codes_ref).sum())
+    assert mism == 0, f"{mism} E4M3 codes differ from the oracle quantiser"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_quant_rope_per_tensor_many_blocks(fa, d):
+    x = gen.outliers((2, 8, 3000, d), 95 + d)
+    cos, sin = gen.rope_tables(3000, d, offset=1)
+    signs = gen.hadamard_signs(d, 4)
+    codes_ref, ds_ref = oracle.quant_e4m3(x, signs=signs, per_tensor=True, rope=(cos, sin, 2))
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs, per_tensor=True,
+                             rope=(torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(), 2))
+    fa.check_device_error()
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_ref.view(np.uint32)), "descales differ"
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+
+
 @pytest.mark.parametrize("layout", [1, 2])
 def test_fwd_fp8_with_rope(fa, layout):
     # Q and K get the rotary embedding (and the Hadamard rotation) in the
