@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(QCfg<D, LPR, ROPE>::THREADS, 1)
     return okk;
   };
 
-  // Block iteration `it` of this CTA is blockIdx.x + it * G; group g takes
+  // Block iteration `it` of this CTA is block_of(it); group g takes
   // it = g, g + NG, g + 2 NG, ...  Its j-th block fills group positions 2j
   // (rows 0..63) and 2j + 1 (rows 64..127) of the group's ring of NSG slots.
   // Row set k of this warp: half hk, row r_slot within the half.
