@@ -73,3 +73,31 @@ def assert_bf16_bound(o_gpu, o_ref, v_absmax, what=""):
     bad = np.abs(o - o_ref) > tol
     assert not bad.any(), f"{what}: {int(bad.sum())} elements outside the derived bound; worst excess " \
                           f"{float((np.abs(o - o_ref) - tol).max()):.3e}"
+
+
+# unit roundoff of the backward's element types
+BWD_UNIT = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+
+
+def bwd_check(got, ref, dtype, what):
+    """Backward errors normalised by the reference: the largest error within
+    2.5 u of the largest |reference| entry, the rms error within 1.25 u of
+    the reference's rms (u the element type's unit roundoff)."""
+    u = BWD_UNIT[dtype]
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.float().cpu().numpy().astype(np.float64)
+        assert g.shape == r.shape, f"{what} {name}: shape"
+        assert np.isfinite(g).all(), f"{what} {name}: non-finite values"
+        if r.size == 0:
+            continue
+        e = g - r
+        rmax = np.abs(r).max()
+        rrms = math.sqrt((r ** 2).mean())
+        if rmax == 0.0:
+            # an exactly zero gradient (a single key: dS = 0) comes out as
+            # fp32 rounding residue of P (dP - D)
+            assert np.abs(g).max() <= 1e-5, f"{what} {name}: expected zeros, got {np.abs(g).max():.3e}"
+            continue
+        assert np.abs(e).max() <= 2.5 * u * rmax, f"{what} {name}: max error {np.abs(e).max() / rmax:.3e} of max|ref|"
+        assert math.sqrt((e ** 2).mean()) <= 1.25 * u * rrms, \
+            f"{what} {name}: rms error {math.sqrt((e ** 2).mean()) / rrms:.3e} of rms(ref)"

@@ -23,11 +23,9 @@ import torch
 
 import attn_inputs as gen
 import oracle
+from gpu_util import bwd_check as _check
 
 pytestmark = pytest.mark.gpu
-
-UNIT = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
-
 
 @pytest.fixture(scope="module")
 def fa():
@@ -58,27 +56,6 @@ def _gpu_grads(fa, q, k, v, do, causal, scale, forward="oracle"):
     dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
     fa.check_device_error()
     return dq, dk, dv
-
-
-def _check(got, ref, dtype, what):
-    u = UNIT[dtype]
-    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
-        g = g.float().cpu().numpy().astype(np.float64)
-        assert g.shape == r.shape, f"{what} {name}: shape"
-        assert np.isfinite(g).all(), f"{what} {name}: non-finite values"
-        if r.size == 0:
-            continue
-        e = g - r
-        rmax = np.abs(r).max()
-        rrms = math.sqrt((r ** 2).mean())
-        if rmax == 0.0:
-            # an exactly zero gradient (a single key: dS = 0) comes out as
-            # fp32 rounding residue of P (dP - D)
-            assert np.abs(g).max() <= 1e-5, f"{what} {name}: expected zeros, got {np.abs(g).max():.3e}"
-            continue
-        assert np.abs(e).max() <= 2.5 * u * rmax, f"{what} {name}: max error {np.abs(e).max() / rmax:.3e} of max|ref|"
-        assert math.sqrt((e ** 2).mean()) <= 1.25 * u * rrms, \
-            f"{what} {name}: rms error {math.sqrt((e ** 2).mean()) / rrms:.3e} of rms(ref)"
 
 
 @pytest.mark.parametrize("d", [64, 128])

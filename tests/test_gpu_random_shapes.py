@@ -1,7 +1,8 @@
 """Seeded random shapes through the C ABI against the fp64 oracle on sampled
 query rows: BF16/FP16 forward (any head dimension, grouped heads, Nq != Nk,
 causal or not, the default scale, 0, a negative and an enlarged scale), the
-E4M3 quantiser bit for bit, and the FP8 forward on its codes.  The shapes
+E4M3 quantiser bit for bit, the FP8 forward on its codes, and the backward
+(whole gradients, with the backward tests' bounds).  The shapes
 come from one fixed generator, so a failure names a case that reruns
 exactly; they fill the gaps between the hand-picked sizes of the other
 parity tests (odd lengths, lengths below one tile, one head per group)."""
@@ -13,7 +14,7 @@ import torch
 
 import attn_inputs as gen
 import oracle
-from gpu_util import FP8_O_RMSE, LSE_ABS, O_MAXABS
+from gpu_util import FP8_O_RMSE, LSE_ABS, O_MAXABS, bwd_check
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +57,24 @@ def _draw_fp8(n, seed):
     return cases
 
 
+def _draw_bwd(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([64, 128]))
+        g = int(rng.choice([1, 2, 4]))
+        Hkv = int(rng.integers(1, 3))
+        Nq = int(rng.integers(1, 500))
+        Nk = int(rng.choice([Nq, int(rng.integers(1, 500))]))
+        cases.append(dict(i=i, B=int(rng.integers(1, 3)), Hq=Hkv * g, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
+                          causal=bool(rng.integers(0, 2)),
+                          scale=float(rng.choice([1.0 / math.sqrt(d), 0.0, -0.2, 0.3])),
+                          fp16=bool(rng.integers(0, 2))))
+    return cases
+
+
 FWD = _draw_fwd(150, 20261203)
+BWD = _draw_bwd(40, 20261206)
 QUANT = _draw_quant(40, 20261204)
 FP8 = _draw_fp8(60, 20261205)
 
@@ -146,3 +164,23 @@ def test_random_fp8(fa, c):
     _check_lse(lse, l_ref, LSE_ABS, "fp8 forward")
     rmse = math.sqrt(float(((o - o_ref) ** 2).mean()))
     assert rmse <= FP8_O_RMSE, f"fp8 forward: O rmse = {rmse:.3e}"
+
+
+@pytest.mark.parametrize("c", BWD, ids=_ids(BWD))
+def test_random_bwd(fa, c):
+    # the backward gets the oracle's O (rounded to the element type) and LSE,
+    # so that its own error is measured, as in the backward tests
+    dt = torch.float16 if c["fp16"] else torch.bfloat16
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    seed = 11000 + c["i"]
+    q = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 0)).to(dt)
+    k = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 1)).to(dt)
+    v = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 2)).to(dt)
+    do = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 3)).to(dt)
+    o64, l64 = oracle.attn_fwd(q, k, v, causal=c["causal"], scale=c["scale"])
+    o = torch.from_numpy(o64).to(dt).cuda()
+    lse = torch.from_numpy(l64).to(torch.float32).cuda()
+    got = fa.bwd(q.cuda(), k.cuda(), v.cuda(), o, lse, do.cuda(), causal=c["causal"], scale=c["scale"])
+    fa.check_device_error()
+    ref = oracle.attn_bwd(q, k, v, do, causal=c["causal"], scale=c["scale"])
+    bwd_check(got, ref, dt, "backward")
