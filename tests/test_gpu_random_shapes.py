@@ -1,8 +1,10 @@
 """Seeded random shapes through the C ABI against the fp64 oracle on sampled
 query rows: BF16/FP16 forward (any head dimension, grouped heads, Nq != Nk,
 causal or not, the default scale, 0, a negative and an enlarged scale), the
-E4M3 quantiser bit for bit, the FP8 forward on its codes, and the backward
-(whole gradients, with the backward tests' bounds).  The shapes
+E4M3 quantiser bit for bit (also with the rotary embedding), the FP8 forward
+on its codes, the split-KV forward (with the split-KV tests' element-wise
+bound), the host-buffer forward (bit-identical to the device call), and the
+backward (whole gradients, with the backward tests' bounds).  The shapes
 come from one fixed generator, so a failure names a case that reruns
 exactly; they fill the gaps between the hand-picked sizes of the other
 parity tests (odd lengths, lengths below one tile, one head per group)."""
@@ -73,7 +75,43 @@ def _draw_bwd(n, seed):
     return cases
 
 
+def _draw_splitkv(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        Hkv = int(rng.integers(1, 3))
+        g = int(rng.choice([1, 2, 4, 8]))
+        Nq = int(rng.choice([1, int(rng.integers(1, 17)), int(rng.integers(1, 300))]))
+        cases.append(dict(i=i, B=int(rng.integers(1, 3)), Hq=Hkv * g, Hkv=Hkv, Nq=Nq,
+                          Nk=int(rng.integers(1, 6000)), d=int(rng.choice([64, 128, 256])),
+                          causal=bool(rng.integers(0, 2)), splits=int(rng.choice([0, 1, 2, 3, 7, 64])),
+                          rows_seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+def _draw_rope(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [dict(i=i, d=int(rng.choice([64, 128, 256])), N=int(rng.integers(1, 3000)),
+                 B=int(rng.integers(1, 3)), H=int(rng.integers(1, 5)), layout=int(rng.integers(1, 3)),
+                 rot=bool(rng.integers(0, 2)), per_tensor=bool(rng.integers(0, 2))) for i in range(n)]
+
+
+def _draw_host(n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        Hkv = int(rng.integers(1, 3))
+        Nq = int(rng.integers(1, 2000))
+        cases.append(dict(i=i, B=int(rng.integers(1, 3)), Hq=Hkv * int(rng.choice([1, 2])), Hkv=Hkv, Nq=Nq,
+                          Nk=int(rng.choice([Nq, int(rng.integers(1, 2000))])), d=int(rng.choice([64, 128, 256])),
+                          causal=bool(rng.integers(0, 2)), pinned=bool(rng.integers(0, 2))))
+    return cases
+
+
 FWD = _draw_fwd(150, 20261203)
+SPLITKV = _draw_splitkv(30, 20261207)
+ROPE = _draw_rope(24, 20261208)
+HOST = _draw_host(12, 20261209)
 BWD = _draw_bwd(40, 20261206)
 QUANT = _draw_quant(40, 20261204)
 FP8 = _draw_fp8(60, 20261205)
@@ -184,3 +222,54 @@ def test_random_bwd(fa, c):
     fa.check_device_error()
     ref = oracle.attn_bwd(q, k, v, do, causal=c["causal"], scale=c["scale"])
     bwd_check(got, ref, dt, "backward")
+
+
+@pytest.mark.parametrize("c", SPLITKV, ids=_ids(SPLITKV))
+def test_random_splitkv(fa, c):
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    seed = 13000 + c["i"]
+    q = torch.from_numpy(gen.normal((B, Hq, Nq, d), seed, 0)).to(torch.bfloat16)
+    k = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 1)).to(torch.bfloat16)
+    v = torch.from_numpy(gen.normal((B, Hkv, Nk, d), seed, 2)).to(torch.bfloat16)
+    o, lse = fa.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=c["causal"], num_splits=c["splits"])
+    fa.check_device_error()
+    rows = _rows(Nq, c["rows_seed"])
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=c["causal"], rows=rows)
+    o = o.float().cpu().numpy().astype(np.float64)[:, :, rows]
+    lse = lse.cpu().numpy().astype(np.float64)[:, :, rows]
+    assert np.isfinite(o).all()
+    _check_lse(lse, l_ref, LSE_ABS, "split-KV")
+    # runs merged by their LSE weights in fp32: the split-KV tests' bound,
+    # 2^-8 (|O| + max|V|) + 1e-4 per element
+    vmax = float(np.abs(v.float().numpy()).max())
+    tol = 2.0 ** -8 * (np.abs(o_ref) + vmax) + 1e-4
+    assert (np.abs(o - o_ref) <= tol).all(), f"split-KV: {int((np.abs(o - o_ref) > tol).sum())} beyond the bound"
+
+
+@pytest.mark.parametrize("c", ROPE, ids=_ids(ROPE))
+def test_random_rope_quant(fa, c):
+    B, H, N, d = c["B"], c["H"], c["N"], c["d"]
+    x = gen.outliers((B, H, N, d), 15000 + c["i"])
+    cos, sin = gen.rope_tables(N, d, offset=c["i"])
+    signs = gen.hadamard_signs(d, 4) if c["rot"] else None
+    rc, rs = oracle.quant_e4m3(x, signs=signs, per_tensor=c["per_tensor"], rope=(cos, sin, c["layout"]))
+    codes, ds = fa.quant_fp8(torch.from_numpy(x).cuda(), signs=signs, per_tensor=c["per_tensor"],
+                             rope=(torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(), c["layout"]))
+    fa.check_device_error()
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), rs.view(np.uint32)), "descales"
+    assert np.array_equal(codes.cpu().numpy(), rc), "codes"
+
+
+@pytest.mark.parametrize("c", HOST, ids=_ids(HOST))
+def test_random_host(fa, c):
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    seed = 17000 + c["i"]
+    q, k, v = (torch.from_numpy(gen.normal(shape, seed, j)).to(torch.bfloat16)
+               for j, shape in enumerate(((B, Hq, Nq, d), (B, Hkv, Nk, d), (B, Hkv, Nk, d))))
+    if c["pinned"]:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_dev, l_dev = fa.fwd_gqa(q.cuda(), k.cuda(), v.cuda(), causal=c["causal"])
+    o_h, l_h = fa.fwd_host(q, k, v, causal=c["causal"])
+    torch.cuda.current_stream().synchronize()
+    fa.check_device_error()
+    assert torch.equal(o_h, o_dev.cpu()) and torch.equal(l_h, l_dev.cpu()), "host path differs from the device path"
